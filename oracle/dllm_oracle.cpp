@@ -1,0 +1,458 @@
+// dllm_oracle.cpp -- plain CPU oracle of the diffusion-LM commit step.
+//
+// TEST INFRASTRUCTURE ONLY: the slow, obviously correct reference the GPU
+// library is checked against.  Only the tests, the smoke check and the bench's
+// CPU-baseline leg load it.  It shares no code with the GPU library.
+//
+// Sources (page title, section):
+//   [ARS]  "dLLM block decoding" research notes (mlx-arsenal): "The pattern",
+//          "What mlx-arsenal ships" (function table), "Reference loop",
+//          "Token editing (LLaDA2.1)", "Deviations from the references".
+//   [MOJO] mojo-dllm manual: "The loop LLaDA uses"; "The GPU path", paragraph
+//          "Row statistics on the device".
+//   [MLXC] "Block Diffusion" (mlxcel manual): "Samplers and Reveal Policies".
+//
+// Every floating-point statistic is computed in double, two passes per row.
+// The Gumbel score is an fp32 value by definition (see gumbel_score), so the
+// oracle computes it in fp32 with explicit fused multiply-adds; build with
+// -ffp-contract=off so no other operation is fused.
+//
+// Parity pins (the tests): worked examples per rule, closed forms for the
+// statistics, invariants, brute force on tiny inputs, Philox against
+// PyTorch's and cuRAND's implementations, ln_p against the true logarithm
+// within its derived bound, and a chi-square check of Gumbel-max sampling.
+
+#include "dllm_oracle.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+#if defined(__linux__)
+#include <sched.h>
+#endif
+
+namespace {
+
+constexpr float kNegInfThreshold = -0x1p+100f;  // -2^100
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10, from its definition in Salmon et al., "Parallel random
+// numbers: as easy as 1, 2, 3" (SC'11): ten rounds of two 32x32->64
+// multiplies; the key is bumped by the Weyl constants between rounds.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+void philox(const uint32_t in[4], const uint32_t key_in[2], uint32_t out[4]) {
+  uint32_t x0 = in[0], x1 = in[1], x2 = in[2], x3 = in[3];
+  uint32_t k0 = key_in[0], k1 = key_in[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += kPhiloxW0;
+      k1 += kPhiloxW1;
+    }
+    const uint64_t prod0 = static_cast<uint64_t>(kPhiloxM0) * x0;
+    const uint64_t prod1 = static_cast<uint64_t>(kPhiloxM1) * x2;
+    const uint32_t hi0 = static_cast<uint32_t>(prod0 >> 32), lo0 = static_cast<uint32_t>(prod0);
+    const uint32_t hi1 = static_cast<uint32_t>(prod1 >> 32), lo1 = static_cast<uint32_t>(prod1);
+    const uint32_t y0 = hi1 ^ x1 ^ k0;
+    const uint32_t y1 = lo1;
+    const uint32_t y2 = hi0 ^ x3 ^ k1;
+    const uint32_t y3 = lo0;
+    x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+  }
+  out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+// ---------------------------------------------------------------------------
+// ln_p: the project's fp32 natural log.  x = 2^e * m with m in
+// (sqrt(1/2), sqrt(2)]; ln m = 2 atanh(s), s = (m-1)/(m+1), |s| <= 0.1716,
+// atanh(s) = s + s^3/3 + s^5/5 + ... + s^11/11 (the next term is below
+// 2^-33 |s|).  ln x = e*ln2 + 2 atanh(s).  Valid for positive normal x, the
+// only inputs the Gumbel transform produces.
+// ---------------------------------------------------------------------------
+float ln_p(float x) {
+  uint32_t bits;
+  std::memcpy(&bits, &x, 4);
+  int e = static_cast<int>(bits >> 23) - 127;
+  const uint32_t mbits = (bits & 0x007FFFFFu) | 0x3F800000u;
+  float m;
+  std::memcpy(&m, &mbits, 4);
+  if (m > 0x1.6a09e6p+0f) {  // sqrt(2) rounded to fp32: fold m into (sqrt(1/2), sqrt(2)]
+    m = m * 0.5f;
+    e += 1;
+  }
+  const float s = (m - 1.0f) / (m + 1.0f);
+  const float s2 = s * s;
+  // Series coefficients 1/11, 1/9, 1/7, 1/5, 1/3 rounded to fp32.
+  float poly = 0x1.745d18p-4f;
+  poly = std::fma(poly, s2, 0x1.c71c72p-4f);
+  poly = std::fma(poly, s2, 0x1.24924ap-3f);
+  poly = std::fma(poly, s2, 0x1.99999ap-3f);
+  poly = std::fma(poly, s2, 0x1.555556p-2f);
+  const float s3 = s * s2;
+  const float atanh_s = std::fma(s3, poly, s);
+  return std::fma(static_cast<float>(e), 0x1.62e430p-1f /* ln 2 in fp32 */, 2.0f * atanh_s);
+}
+
+// Gumbel-perturbed score of id v in global row `row` (fp32 by definition):
+//   r = Philox4x32-10(counter = (v >> 2, row_lo, row_hi, 0), key = (key_lo, key_hi))[v & 3]
+//   u = (2 (r >> 9) + 1) 2^-24            exact, u in (0, 1)
+//   g = -ln_p(-ln_p(u))                   standard Gumbel noise
+//   s = fmaf(t, g, z)
+// argmax_v s_v is a sample of softmax(z / t): the Gumbel-max trick LLaDA
+// applies before its argmax ([MOJO] "The loop LLaDA uses"; [ARS] token_stats
+// "greedy or Gumbel-max sampling with an explicit key").
+float gumbel_score(float z, float t, uint64_t key, int64_t row, int64_t v) {
+  const uint32_t ctr[4] = {static_cast<uint32_t>(static_cast<uint64_t>(v) >> 2),
+                           static_cast<uint32_t>(static_cast<uint64_t>(row)),
+                           static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32), 0u};
+  const uint32_t k[2] = {static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32)};
+  uint32_t out[4];
+  philox(ctr, k, out);
+  const uint32_t r = out[v & 3];
+  const float u = static_cast<float>(2u * (r >> 9) + 1u) * 0x1p-24f;
+  const float E = -ln_p(u);
+  const float g = -ln_p(E);
+  return std::fma(t, g, z);
+}
+
+// A logit as the statistics see it: bf16 widens exactly to fp32; NaN and
+// anything at or below -2^100 count as -inf (no probability mass).
+inline float load_logit(const void* base, int dtype, int64_t idx) {
+  float z;
+  if (dtype == 1) {
+    const uint32_t b = static_cast<uint32_t>(static_cast<const uint16_t*>(base)[idx]) << 16;
+    std::memcpy(&z, &b, 4);
+  } else {
+    z = static_cast<const float*>(base)[idx];
+  }
+  if (std::isnan(z) || z <= kNegInfThreshold) z = -std::numeric_limits<float>::infinity();
+  return z;
+}
+
+struct RowOut {
+  int32_t x0;
+  double prob;
+  double entropy;
+};
+
+// token_stats for one row.  [ARS] "What mlx-arsenal ships" and "Deviations":
+// per position the proposal x0, its probability and the entropy, computed
+// without NaN trouble, by argmax or by Gumbel-max with a caller key; the
+// suppressed ids take no part in the softmax.  [MOJO] "Row statistics on the
+// device": the row max, sum exp(z - max) and sum exp(z - max)(z - max) give
+// both numbers; the argmax tie rule keeps the smallest id; the argmax has
+// p = 1 / sum.
+RowOut stats_row(const void* logits, int dtype, int64_t row_off, int64_t V, int64_t grow,
+                 float t, uint64_t key, const std::vector<uint8_t>& absent, int64_t v_eff) {
+  const double inf = std::numeric_limits<double>::infinity();
+  // Pass 1: the max over the token set A (ids not suppressed).
+  float m = -std::numeric_limits<float>::infinity();
+  for (int64_t v = 0; v < V; ++v) {
+    if (absent[v]) continue;
+    m = std::max(m, load_logit(logits, dtype, row_off + v));
+  }
+  // x0: lowest id in A maximizing z (greedy) or the Gumbel score (t > 0).
+  int64_t x0 = -1;
+  if (t > 0.0f) {
+    float best = 0.0f;
+    for (int64_t v = 0; v < V; ++v) {
+      if (absent[v]) continue;
+      const float s = gumbel_score(load_logit(logits, dtype, row_off + v), t, key, grow, v);
+      if (x0 < 0 || s > best) {
+        best = s;
+        x0 = v;
+      }
+    }
+  } else {
+    for (int64_t v = 0; v < V; ++v) {
+      if (absent[v]) continue;
+      if (load_logit(logits, dtype, row_off + v) == m) {
+        x0 = v;
+        break;
+      }
+    }
+  }
+  const double zx0 = load_logit(logits, dtype, row_off + x0);
+  RowOut out{static_cast<int32_t>(x0), 0.0, 0.0};
+  if (m == -std::numeric_limits<float>::infinity()) {
+    // No finite mass anywhere: the uniform limit over A.
+    out.prob = 1.0 / static_cast<double>(v_eff);
+    out.entropy = std::log(static_cast<double>(v_eff));
+    return out;
+  }
+  if (m == std::numeric_limits<float>::infinity()) {
+    // The +inf entries share all the mass.
+    int64_t n_inf = 0;
+    for (int64_t v = 0; v < V; ++v)
+      if (!absent[v] && load_logit(logits, dtype, row_off + v) == std::numeric_limits<float>::infinity()) ++n_inf;
+    out.prob = (zx0 == inf) ? 1.0 / static_cast<double>(n_inf) : 0.0;
+    out.entropy = std::log(static_cast<double>(n_inf));
+    return out;
+  }
+  // Pass 2: Z = sum exp(z - m), S = sum exp(z - m)(z - m); -inf terms add 0.
+  const double md = m;
+  double Z = 0.0, S = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    if (absent[v]) continue;
+    const double z = load_logit(logits, dtype, row_off + v);
+    if (z == -inf) continue;
+    const double d = z - md;
+    const double e = std::exp(d);
+    Z += e;
+    S += e * d;
+  }
+  out.prob = std::exp(zx0 - md) / Z;
+  // H = -sum p log p = log Z - S / Z, clamped to its range [0, log |A|].
+  double H = std::log(Z) - S / Z;
+  H = std::min(std::max(H, 0.0), std::log(static_cast<double>(v_eff)));
+  out.entropy = H;
+  return out;
+}
+
+// A confidence as the rules see it: NaN ranks as -inf.
+inline float conf_of(float c) { return std::isnan(c) ? -std::numeric_limits<float>::infinity() : c; }
+// An entropy as the entropy-bound rule sees it: NaN ranks as +inf.
+inline float ent_of(float h) { return std::isnan(h) ? std::numeric_limits<float>::infinity() : h; }
+
+// Candidate positions of batch row b, ranked by descending confidence.  The
+// sort is stable: among equal confidences the smaller position ranks first
+// ([ARS] "Deviations", the paragraph on ties).
+std::vector<int64_t> rank_desc(const float* conf, const uint8_t* cand, int64_t b, int64_t L) {
+  std::vector<int64_t> pos;
+  for (int64_t l = 0; l < L; ++l)
+    if (cand[b * L + l]) pos.push_back(l);
+  std::stable_sort(pos.begin(), pos.end(), [&](int64_t a, int64_t c) {
+    return conf_of(conf[b * L + a]) > conf_of(conf[b * L + c]);
+  });
+  return pos;
+}
+
+int resolve_threads(int n) {
+  if (n > 0) return n;
+  return orc_default_threads();
+}
+
+}  // namespace
+
+extern "C" {
+
+int orc_default_threads(void) {
+#if defined(__linux__)
+  cpu_set_t set;
+  if (sched_getaffinity(0, sizeof(set), &set) == 0) {
+    const int c = CPU_COUNT(&set);
+    if (c > 0) return c;
+  }
+#endif
+  const unsigned h = std::thread::hardware_concurrency();
+  return h ? static_cast<int>(h) : 1;
+}
+
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  philox(ctr, key, out);
+}
+
+float orc_ln_p(float x) { return ln_p(x); }
+
+void orc_ln_p_many(const float* x, int64_t n, float* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = ln_p(x[i]);
+}
+
+float orc_gumbel_score(float z, float temperature, uint64_t key, int64_t row, int64_t v) {
+  return gumbel_score(z, temperature, key, row, v);
+}
+
+int orc_token_stats(const void* logits, int dtype, int64_t n_rows, int64_t V, int64_t row_stride,
+                    const int64_t* row_ids, float temperature, uint64_t key,
+                    const int32_t* suppress_ids, int32_t n_suppress,
+                    int32_t* x0, double* prob, double* entropy, int n_threads) {
+  if (n_rows < 0 || V <= 0 || row_stride < V || (dtype != 0 && dtype != 1)) return -1;
+  if (!(temperature >= 0.0f) || n_suppress < 0) return -1;
+  if (n_rows == 0) return 0;
+  if (!logits || !x0 || !prob || !entropy) return -1;
+  std::vector<uint8_t> absent(static_cast<size_t>(V), 0);
+  for (int32_t i = 0; i < n_suppress; ++i) {
+    if (suppress_ids[i] < 0 || suppress_ids[i] >= V) return -1;
+    absent[suppress_ids[i]] = 1;
+  }
+  int64_t v_eff = 0;
+  for (int64_t v = 0; v < V; ++v) v_eff += absent[v] ? 0 : 1;
+  if (v_eff == 0) return -1;  // an empty token set has no distribution
+
+  const int nt = static_cast<int>(std::min<int64_t>(resolve_threads(n_threads), n_rows));
+  auto work = [&](int tid) {
+    for (int64_t r = tid; r < n_rows; r += nt) {
+      const int64_t grow = row_ids ? row_ids[r] : r;
+      const RowOut o = stats_row(logits, dtype, r * row_stride, V, grow, temperature, key, absent, v_eff);
+      x0[r] = o.x0;
+      prob[r] = o.prob;
+      entropy[r] = o.entropy;
+    }
+  };
+  if (nt <= 1) {
+    work(0);
+  } else {
+    std::vector<std::thread> pool;
+    for (int i = 0; i < nt; ++i) pool.emplace_back(work, i);
+    for (auto& th : pool) th.join();
+  }
+  return 0;
+}
+
+// threshold_transfer.  [ARS] function table: a candidate commits when its
+// confidence reaches tau (exceeds it in strict mode); a row where nobody
+// qualifies commits exactly one.  [ARS] "Deviations": that one is the earliest
+// of the maximal confidences.  [MLXC] "Samplers and Reveal Policies": the
+// forced commit is what makes every step progress.
+int orc_threshold_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
+                           float tau, int strict, uint8_t* commit) {
+  if (B < 0 || L < 0) return -1;
+  for (int64_t b = 0; b < B; ++b) {
+    bool any_cand = false, any_pass = false;
+    int64_t best = -1;
+    for (int64_t l = 0; l < L; ++l) {
+      const int64_t i = b * L + l;
+      commit[i] = 0;
+      if (!cand[i]) continue;
+      any_cand = true;
+      const float c = conf_of(conf[i]);
+      const bool pass = strict ? (c > tau) : (c >= tau);
+      if (pass) {
+        commit[i] = 1;
+        any_pass = true;
+      }
+      if (best < 0 || c > conf_of(conf[b * L + best])) best = l;
+    }
+    if (any_cand && !any_pass) commit[b * L + best] = 1;
+  }
+  return 0;
+}
+
+// topk_transfer.  [ARS] function table: each row commits its k best
+// candidates, with its own k.  [MOJO] "The loop LLaDA uses": this is LLaDA's
+// low-confidence remasking.  k is clamped to [0, number of candidates].
+int orc_topk_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
+                      const int32_t* k, uint8_t* commit) {
+  if (B < 0 || L < 0) return -1;
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t l = 0; l < L; ++l) commit[b * L + l] = 0;
+    const std::vector<int64_t> order = rank_desc(conf, cand, b, L);
+    const int64_t kk = std::min<int64_t>(std::max<int64_t>(k[b], 0), static_cast<int64_t>(order.size()));
+    for (int64_t i = 0; i < kk; ++i) commit[b * L + order[i]] = 1;
+  }
+  return 0;
+}
+
+// factor_transfer.  [ARS] function table: the longest prefix of the ranking
+// with (i+1)(1 - c_(i)) <= f, c_(i) the i-th largest confidence; [ARS]
+// "Deviations": the Fast-dLLM off-by-one is not reproduced.  The product is
+// evaluated in double, and a row with candidates commits at least one.
+int orc_factor_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
+                        float factor, uint8_t* commit) {
+  if (B < 0 || L < 0) return -1;
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t l = 0; l < L; ++l) commit[b * L + l] = 0;
+    const std::vector<int64_t> order = rank_desc(conf, cand, b, L);
+    const int64_t n_cand = static_cast<int64_t>(order.size());
+    int64_t n = 0;
+    while (n < n_cand) {
+      const double c = conf_of(conf[b * L + order[n]]);
+      const double lhs = static_cast<double>(n + 1) * (1.0 - c);
+      if (!(lhs <= static_cast<double>(factor))) break;
+      ++n;
+    }
+    if (n_cand > 0) n = std::max<int64_t>(n, 1);
+    for (int64_t i = 0; i < n; ++i) commit[b * L + order[i]] = 1;
+  }
+  return 0;
+}
+
+// entropy_bound_transfer.  [ARS] function table: rank by ascending entropy
+// and take the longest prefix whose members satisfy sum_{j<i} H_(j) <= gamma.
+// [MLXC] "Samplers and Reveal Policies": the rule always accepts one position
+// or more.  The prefix sum is accumulated in double, strictly in ranking order.
+int orc_entropy_bound_transfer(const float* entropy, const uint8_t* cand, int64_t B, int64_t L,
+                               float gamma, uint8_t* commit) {
+  if (B < 0 || L < 0) return -1;
+  for (int64_t b = 0; b < B; ++b) {
+    std::vector<int64_t> order;
+    for (int64_t l = 0; l < L; ++l) {
+      commit[b * L + l] = 0;
+      if (cand[b * L + l]) order.push_back(l);
+    }
+    std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t c) {
+      return ent_of(entropy[b * L + a]) < ent_of(entropy[b * L + c]);
+    });
+    const int64_t n_cand = static_cast<int64_t>(order.size());
+    double prefix = 0.0;  // sum of the entropies ranked before position i
+    int64_t n = 0;
+    while (n < n_cand && prefix <= static_cast<double>(gamma)) {
+      prefix += static_cast<double>(ent_of(entropy[b * L + order[n]]));
+      ++n;
+    }
+    if (n_cand > 0) n = std::max<int64_t>(n, 1);
+    for (int64_t i = 0; i < n; ++i) commit[b * L + order[i]] = 1;
+  }
+  return 0;
+}
+
+// edit_transfer.  [ARS] function table and "Token editing (LLaDA2.1)": an
+// already decoded (editable) position is rewritten with the proposal when the
+// proposal differs from the current token and its probability is strictly
+// above tau_edit.
+int orc_edit_transfer(const int32_t* x0, const float* prob, const int32_t* tokens,
+                      const uint8_t* editable, int64_t n, float tau_edit, uint8_t* edit) {
+  if (n < 0) return -1;
+  for (int64_t i = 0; i < n; ++i) {
+    const float p = conf_of(prob[i]);
+    edit[i] = (editable[i] && x0[i] != tokens[i] && p > tau_edit) ? 1 : 0;
+  }
+  return 0;
+}
+
+// transfer_schedule.  [ARS] function table: a (B, steps) table of per-step
+// quotas in LLaDA's linear style; [MOJO] "The loop LLaDA uses": a block's
+// masked count is divided evenly among its steps.  The remainder goes to the
+// first steps; a negative count is treated as zero.
+int orc_transfer_schedule(const int32_t* counts, int64_t B, int32_t steps, int32_t* quotas) {
+  if (B < 0 || steps <= 0) return -1;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t n = std::max<int32_t>(counts[b], 0);
+    for (int32_t s = 0; s < steps; ++s)
+      quotas[b * steps + s] = static_cast<int32_t>(n / steps + (s < n % steps ? 1 : 0));
+  }
+  return 0;
+}
+
+// block_ranges.  [ARS] function table, "Reference loop" and "Token editing
+// (LLaDA2.1)": block boundaries either counted from the end of the prompt or
+// aligned on absolute multiples of the block length.  Prompt-relative blocks
+// start at P; aligned blocks start at floor(P / bl) * bl.  Every block ends at
+// min(start + bl, P + gen_len).
+int orc_block_ranges(int64_t P, int64_t gen_len, int64_t block_len, int align,
+                     int64_t* ranges, int64_t cap, int64_t* n_out) {
+  if (P < 0 || gen_len < 0 || block_len <= 0 || cap < 0 || !n_out) return -1;
+  const int64_t first = align ? (P / block_len) * block_len : P;
+  const int64_t stop = P + gen_len;
+  int64_t n = 0;
+  if (gen_len > 0) {
+    for (int64_t start = first; start < stop; start += block_len) {
+      if (n < cap && ranges) {
+        ranges[2 * n] = start;
+        ranges[2 * n + 1] = std::min(start + block_len, stop);
+      }
+      ++n;
+    }
+  }
+  *n_out = n;
+  return n > cap ? -2 : 0;
+}
+
+}  // extern "C"

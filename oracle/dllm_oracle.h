@@ -1,0 +1,65 @@
+/*
+ * dllm_oracle.h -- plain CPU oracle of the diffusion-LM commit step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This header, its implementation and the Python
+ * wrapper beside them are the slow, obviously correct reference that the GPU
+ * library is checked against.  Only the tests, the smoke check and the
+ * bench's CPU-baseline leg may load them; the product path never does.
+ *
+ * All functions are synchronous host code on host pointers and return 0 on
+ * success, a negative value on invalid arguments.
+ */
+#ifndef DLLM_ORACLE_H
+#define DLLM_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): out = philox(ctr, key). */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* The project's fp32 natural logarithm (exponent split + atanh series). */
+float orc_ln_p(float x);
+void orc_ln_p_many(const float* x, int64_t n, float* out);
+
+/* The fp32 Gumbel-perturbed score of vocabulary id v in global row `row`. */
+float orc_gumbel_score(float z, float temperature, uint64_t key, int64_t row, int64_t v);
+
+/* Statistics pass: x0, prob and entropy per row, in double.
+ * logits: (n_rows, row_stride) row-major; dtype 0 = float32, 1 = bf16 bits.
+ * row_ids (nullable): the global row index of each given row (feeds the
+ * Gumbel counter); NULL means row i is global row i.
+ * n_threads: 0 = every core the process may use. */
+int orc_token_stats(const void* logits, int dtype, int64_t n_rows, int64_t V, int64_t row_stride,
+                    const int64_t* row_ids, float temperature, uint64_t key,
+                    const int32_t* suppress_ids, int32_t n_suppress,
+                    int32_t* x0, double* prob, double* entropy, int n_threads);
+
+/* Commit rules over (B, L) row-major confidences and 0/1 candidate masks. */
+int orc_threshold_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
+                           float tau, int strict, uint8_t* commit);
+int orc_topk_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
+                      const int32_t* k, uint8_t* commit);
+int orc_factor_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
+                        float factor, uint8_t* commit);
+int orc_entropy_bound_transfer(const float* entropy, const uint8_t* cand, int64_t B, int64_t L,
+                               float gamma, uint8_t* commit);
+int orc_edit_transfer(const int32_t* x0, const float* prob, const int32_t* tokens,
+                      const uint8_t* editable, int64_t n, float tau_edit, uint8_t* edit);
+
+/* Schedules. */
+int orc_transfer_schedule(const int32_t* counts, int64_t B, int32_t steps, int32_t* quotas);
+int orc_block_ranges(int64_t P, int64_t gen_len, int64_t block_len, int align,
+                     int64_t* ranges, int64_t cap, int64_t* n_out);
+
+/* Threads orc_token_stats uses when asked for 0. */
+int orc_default_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DLLM_ORACLE_H */

@@ -1,0 +1,213 @@
+"""Pins of the CPU oracle to what the pages and the mathematics fix.
+
+Worked examples (tests/golden), closed forms, textbook routines (scipy),
+and the NaN / infinity / suppression conventions.  CPU only.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+import torch
+
+import oracle
+from dllm_workloads import f32_to_bf16_bits
+
+
+def test_token_stats_worked_examples(golden):
+    for ex in golden["token_stats"]:
+        z = np.asarray([ex["logits"]], dtype=np.float32)
+        x0, p, h = oracle.token_stats(z, suppress_ids=ex["suppress_ids"])
+        assert x0[0] == ex["x0"], ex["cite"]
+        # the fp32 rounding of ln 3 moves p by ~1e-8
+        assert p[0] == pytest.approx(ex["prob"], rel=1e-7), ex["cite"]
+        assert h[0] == pytest.approx(ex["entropy"], rel=1e-7), ex["cite"]
+
+
+def test_closed_form_uniform_row():
+    for V in (1, 7, 4096, 126464):
+        z = np.full((1, V), 1.25, dtype=np.float32)
+        x0, p, h = oracle.token_stats(z)
+        assert x0[0] == 0
+        assert p[0] == pytest.approx(1.0 / V, rel=1e-12)
+        assert h[0] == pytest.approx(math.log(V), rel=1e-12, abs=1e-15)
+
+
+def test_closed_form_two_level_row():
+    # one logit a above V-1 equal ones: p = e^a / (e^a + V - 1),
+    # H = ln(e^a + V - 1) - a e^a / (e^a + V - 1)
+    for a, V, pos in ((8.0, 4096, 17), (3.0, 1000, 999), (0.5, 2, 0)):
+        z = np.zeros((1, V), dtype=np.float32)
+        z[0, pos] = a
+        x0, p, h = oracle.token_stats(z)
+        ea = math.exp(a)
+        assert x0[0] == pos
+        assert p[0] == pytest.approx(ea / (ea + V - 1), rel=1e-12)
+        assert h[0] == pytest.approx(math.log(ea + V - 1) - a * ea / (ea + V - 1), rel=1e-11)
+    # the values quoted for a=8, V=4096
+    z = np.zeros((1, 4096), dtype=np.float32)
+    z[0, 0] = 8.0
+    _, p, h = oracle.token_stats(z)
+    assert p[0] == pytest.approx(0.4212798, abs=1e-7)
+    assert h[0] == pytest.approx(5.494220, abs=1e-6)
+
+
+def test_textbook_softmax_entropy_scipy():
+    rng = np.random.default_rng(11)
+    for V, scale in ((3, 1.0), (50, 4.0), (4096, 3.0), (20000, 0.3)):
+        z = (rng.standard_normal((6, V)) * scale).astype(np.float32)
+        x0, p, h = oracle.token_stats(z)
+        for r in range(z.shape[0]):
+            q = scipy.special.softmax(z[r].astype(np.float64))
+            assert x0[r] == int(np.argmax(z[r]))
+            assert p[r] == pytest.approx(q[x0[r]], rel=1e-12)
+            assert h[r] == pytest.approx(scipy.stats.entropy(q), rel=1e-10, abs=1e-13)
+
+
+def test_suppression_equals_deleting_columns():
+    rng = np.random.default_rng(12)
+    V = 300
+    z = (rng.standard_normal((5, V)) * 2).astype(np.float32)
+    sup = [0, 3, 17, 299, 150]
+    x0, p, h = oracle.token_stats(z, suppress_ids=sup)
+    keep = np.array([v for v in range(V) if v not in sup])
+    for r in range(5):
+        q = scipy.special.softmax(z[r, keep].astype(np.float64))
+        j = int(np.argmax(z[r, keep]))
+        assert x0[r] == keep[j]
+        assert p[r] == pytest.approx(q[j], rel=1e-12)
+        assert h[r] == pytest.approx(scipy.stats.entropy(q), rel=1e-10)
+    # suppressing the argmax moves x0 to the runner-up
+    z2 = np.array([[0.0, 5.0, 4.0, 1.0]], dtype=np.float32)
+    assert oracle.token_stats(z2, suppress_ids=[1])[0][0] == 2
+
+
+def test_nan_and_neg_inf_carry_no_mass():
+    z = np.array([[np.nan, 1.0, -np.inf, 2.0, np.nan, -3e30]], dtype=np.float32)
+    x0, p, h = oracle.token_stats(z)
+    q = scipy.special.softmax(np.array([1.0, 2.0]))
+    assert x0[0] == 3
+    assert p[0] == pytest.approx(q[1], rel=1e-12)
+    assert h[0] == pytest.approx(scipy.stats.entropy(q), rel=1e-12)
+
+
+def test_all_masked_row_is_uniform_limit():
+    V = 9
+    for fill in (np.nan, -np.inf, -2.0**100):
+        z = np.full((1, V), fill, dtype=np.float32)
+        x0, p, h = oracle.token_stats(z, suppress_ids=[0, 4])
+        assert x0[0] == 1
+        assert p[0] == pytest.approx(1.0 / 7)
+        assert h[0] == pytest.approx(math.log(7))
+
+
+def test_positive_infinity_shares_mass():
+    z = np.array([[0.0, np.inf, 5.0, np.inf, np.inf, 1.0]], dtype=np.float32)
+    x0, p, h = oracle.token_stats(z)
+    assert x0[0] == 1 and p[0] == pytest.approx(1 / 3) and h[0] == pytest.approx(math.log(3))
+
+
+def test_bf16_widening_matches_torch():
+    rng = np.random.default_rng(13)
+    z = (rng.standard_normal((3, 777)) * 5).astype(np.float32)
+    bits = f32_to_bf16_bits(z)
+    widened = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    xa, pa, ha = oracle.token_stats(bits, dtype="bf16")
+    xb, pb, hb = oracle.token_stats(widened)
+    assert np.array_equal(xa, xb) and np.array_equal(pa, pb) and np.array_equal(ha, hb)
+    # the generator's rounding agrees with torch's float -> bf16 conversion
+    tb = torch.from_numpy(z).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(tb, bits)
+
+
+def test_stats_invariants_random():
+    rng = np.random.default_rng(14)
+    for trial in range(20):
+        V = int(rng.integers(2, 3000))
+        z = (rng.standard_normal((4, V)) * rng.uniform(0.1, 30)).astype(np.float32)
+        nsup = int(rng.integers(0, min(V - 1, 5) + 1))
+        sup = rng.choice(V, size=nsup, replace=False).tolist()
+        t = float(rng.choice([0.0, 0.7, 1.3]))
+        x0, p, h = oracle.token_stats(z, temperature=t, key=int(rng.integers(1, 2**62)), suppress_ids=sup)
+        veff = V - nsup
+        assert np.all(p > 0) and np.all(p <= 1)
+        assert np.all(h >= 0) and np.all(h <= math.log(veff) + 1e-12)
+        assert not set(x0.tolist()) & set(sup)
+
+
+def test_thread_count_does_not_change_results():
+    rng = np.random.default_rng(15)
+    z = (rng.standard_normal((37, 1000)) * 3).astype(np.float32)
+    a = oracle.token_stats(z, temperature=0.9, key=77, n_threads=1)
+    b = oracle.token_stats(z, temperature=0.9, key=77, n_threads=5)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+@pytest.mark.parametrize("rule", ["threshold_transfer", "topk_transfer", "factor_transfer",
+                                  "entropy_bound_transfer"])
+def test_rule_worked_examples(golden, rule):
+    for ex in golden[rule]:
+        if rule == "threshold_transfer":
+            got = oracle.threshold_transfer(ex["conf"], ex["cand"], ex["tau"], ex["strict"])
+        elif rule == "topk_transfer":
+            got = oracle.topk_transfer(ex["conf"], ex["cand"], ex["k"])
+        elif rule == "factor_transfer":
+            got = oracle.factor_transfer(ex["conf"], ex["cand"], ex["factor"])
+        else:
+            got = oracle.entropy_bound_transfer(ex["entropy"], ex["cand"], ex["gamma"])
+        assert got[0].tolist() == ex["commit"], ex["cite"]
+
+
+def test_edit_worked_examples(golden):
+    for ex in golden["edit_transfer"]:
+        got = oracle.edit_transfer(ex["x0"], ex["prob"], ex["tokens"], ex["editable"], ex["tau_edit"])
+        assert got.tolist() == ex["edit"], ex["cite"]
+
+
+def test_schedule_worked_examples(golden):
+    for ex in golden["transfer_schedule"]:
+        assert oracle.transfer_schedule(ex["counts"], ex["steps"]).tolist() == ex["quotas"], ex["cite"]
+    for ex in golden["block_ranges"]:
+        got = oracle.block_ranges(ex["P"], ex["gen_len"], ex["block_len"], ex["align"])
+        assert [list(r) for r in got] == ex["ranges"], ex["cite"]
+
+
+def test_schedule_invariants_determine_it():
+    # A non-increasing sequence of `steps` integers summing to n whose entries
+    # differ by at most one is unique, so these checks pin the schedule fully.
+    rng = np.random.default_rng(16)
+    for _ in range(200):
+        steps = int(rng.integers(1, 70))
+        counts = rng.integers(0, 600, size=3)
+        q = oracle.transfer_schedule(counts, steps)
+        for b in range(3):
+            assert q[b].sum() == counts[b]
+            assert np.all(np.diff(q[b]) <= 0)
+            assert q[b].max() - q[b].min() <= 1
+    assert oracle.transfer_schedule([-4], 3).tolist() == [[0, 0, 0]]
+    assert oracle.transfer_schedule([256], 32)[0, 0] == 8
+
+
+def test_block_ranges_tile_the_generation_region():
+    rng = np.random.default_rng(17)
+    for _ in range(300):
+        P, gen, bl = int(rng.integers(0, 300)), int(rng.integers(0, 500)), int(rng.integers(1, 70))
+        for align in (False, True):
+            r = oracle.block_ranges(P, gen, bl, align)
+            if gen == 0:
+                assert r == []
+                continue
+            covered = []
+            for (s, e) in r:
+                assert 0 < e - s <= bl
+                covered.extend(range(max(s, P), e))
+                if align:
+                    assert s % bl == 0
+            assert covered == list(range(P, P + gen))
+            assert all(r[i][1] == r[i + 1][0] for i in range(len(r) - 1))
+            if not align:
+                assert r[0][0] == P
+    assert len(oracle.block_ranges(128, 1024, 32)) == 32
+    assert oracle.block_ranges(128, 1024, 32, True) == oracle.block_ranges(128, 1024, 32, False)

@@ -1,0 +1,219 @@
+/*
+ * dllmcommit.h -- C ABI of libdllmcommit, the commit step of masked
+ * (absorbing-state) diffusion-LM block decoding on NVIDIA GB300 (sm_103a).
+ *
+ * The commit step splits into a statistics pass over the (B, L, V) logits and
+ * a commit rule over each batch row's masked candidates, plus the schedules
+ * that go with the rules.  Citations name the page and its section:
+ *   [ARS]  "dLLM block decoding" research notes (mlx-arsenal): "The pattern",
+ *          "What mlx-arsenal ships", "Reference loop", "Token editing
+ *          (LLaDA2.1)", "Deviations from the references".
+ *   [MOJO] mojo-dllm manual: "The loop LLaDA uses"; "The GPU path",
+ *          paragraph "Row statistics on the device".
+ *   [MLXC] "Block Diffusion" (mlxcel manual): "Samplers and Reveal Policies".
+ *
+ * Conventions shared by every entry point:
+ *   - The caller owns every buffer.  "device" pointers are CUDA device
+ *     memory; "host" pointers are ordinary host memory.  Nothing here
+ *     allocates memory.
+ *   - Every device-side call is asynchronous on the given stream (0 = the
+ *     legacy default stream) and is launched with programmatic dependent
+ *     launch, so its prologue may overlap the previous kernel in the stream;
+ *     it reads no input before that kernel has finished.
+ *   - Arguments are validated on the host first; on any error nothing is
+ *     launched and the status says why.  A failed launch returns
+ *     DLLM_ERR_CUDA (the CUDA error is left for cudaGetLastError).
+ *   - Boolean masks are uint8 0/1 (any non-zero byte reads as 1); token ids
+ *     are int32; (B, L) arrays are row-major and contiguous; strides are in
+ *     elements.
+ *   - B == 0 or L == 0 is a valid empty call: nothing is launched.
+ *   - Calls on different streams must not share output buffers or a
+ *     workspace.
+ */
+#ifndef DLLMCOMMIT_H
+#define DLLMCOMMIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dllm_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  DLLM_OK = 0,
+  DLLM_ERR_INVALID_ARGUMENT = 1, /* a shape, pointer, value or alignment is wrong */
+  DLLM_ERR_UNSUPPORTED = 2,      /* valid, but outside what this build handles */
+  DLLM_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
+  DLLM_ERR_CUDA = 4,             /* a CUDA launch or query failed */
+  DLLM_ERR_DEVICE = 5            /* a kernel reported a fault through the workspace */
+} dllm_status;
+
+typedef enum { DLLM_F32 = 0, DLLM_BF16 = 1 } dllm_dtype;
+
+/* Largest suppress_ids list a statistics call accepts. */
+#define DLLM_MAX_SUPPRESS 64
+/* Largest L the sorting rules (top-k, factor, entropy bound) accept. */
+#define DLLM_MAX_SORT_L 16384
+
+const char* dllm_status_string(dllm_status status);
+const char* dllm_version(void);
+
+/* ------------------------------------------------------------------------
+ * Statistics pass ([ARS] "What mlx-arsenal ships", token_stats; [MOJO] "Row
+ * statistics on the device").
+ *
+ * For each of the T = B*L logit rows, over the token set A = {0..V-1} minus
+ * suppress_ids:
+ *   x0      the proposal: the lowest id in A maximising z (temperature == 0),
+ *           or maximising the Gumbel score fmaf(t, g_v, z_v) (temperature
+ *           t > 0), g_v = -ln_p(-ln_p(u_v)), u_v from Philox4x32-10 with
+ *           counter (v >> 2, row lo, row hi, 0), key (key lo, key hi), word
+ *           v & 3, u = (2 (r >> 9) + 1) 2^-24; row = b*L + l.
+ *   prob    exp(z_x0 - m) / sum_A exp(z - m) of the untempered softmax.
+ *   entropy ln Z - S / Z of the same softmax, clamped to [0, ln |A|].
+ * bf16 logits widen exactly to fp32; NaN and values <= -2^100 carry no
+ * mass; a row whose every entry carries none yields the uniform limit
+ * (x0 = min A, prob = 1/|A|, entropy = ln |A|); +inf entries share all the
+ * mass equally.  Sums are accumulated in fp32.
+ *
+ * logits        device, T rows of row_stride elements (dtype dt); the base
+ *               pointer and row_stride * sizeof(element) must be multiples of
+ *               16 bytes (else DLLM_ERR_UNSUPPORTED).
+ * suppress_ids  HOST array of n_suppress ids in [0, V) (duplicates allowed),
+ *               0 <= n_suppress <= DLLM_MAX_SUPPRESS, fewer than |V| distinct.
+ * x0, prob, entropy   device outputs, T entries each.
+ * workspace     device, >= dllm_token_stats_workspace_size(B, L, V, dt)
+ *               bytes, zero-filled before its first use; every call leaves it
+ *               zeroed again (the library resets what it uses).
+ * ------------------------------------------------------------------------ */
+size_t dllm_token_stats_workspace_size(int64_t B, int64_t L, int64_t V, dllm_dtype dt);
+
+dllm_status dllm_token_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,
+                             int64_t row_stride, float temperature, uint64_t key,
+                             const int32_t* suppress_ids, int32_t n_suppress,
+                             int32_t* x0, float* prob, float* entropy,
+                             void* workspace, size_t workspace_bytes, dllm_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Commit rules.  One batch row b of L positions; cand (device, (B, L)) marks
+ * the masked candidates; commit (device, (B, L)) is written for every
+ * position (0 for non-candidates).  Ranking: higher confidence first (NaN
+ * ranks as -inf), ties to the lower position; for the entropy bound, lower
+ * entropy first (NaN ranks as +inf), ties to the lower position.
+ *
+ * Optional canvas update, the where(commit, x0, x) of the reference loops:
+ * when x0 (device, (B, L)) and canvas (device) are both non-NULL, every
+ * committed (b, l) sets canvas[b * canvas_stride + canvas_offset + l] =
+ * x0[b * L + l].  Pass NULL for both to skip it.
+ * ------------------------------------------------------------------------ */
+
+/* [ARS] threshold_transfer; [MLXC] forced progress: commit cand with
+ * conf >= tau (conf > tau when strict != 0); a row with candidates and none
+ * passing commits exactly one, the earliest maximal confidence. */
+dllm_status dllm_threshold_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
+                                    float tau, int strict, uint8_t* commit,
+                                    const int32_t* x0, int32_t* canvas, int64_t canvas_stride,
+                                    int64_t canvas_offset, dllm_stream_t stream);
+
+/* [ARS] topk_transfer; [MOJO] "The loop LLaDA uses": commit the first
+ * min(max(k[b], 0), n_cand) candidates of the ranking.  k: device (B,). */
+dllm_status dllm_topk_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
+                               const int32_t* k, uint8_t* commit,
+                               const int32_t* x0, int32_t* canvas, int64_t canvas_stride,
+                               int64_t canvas_offset, dllm_stream_t stream);
+
+/* [ARS] factor_transfer (without Fast-dLLM's off-by-one): commit the longest
+ * prefix of the ranking with (i+1)(1 - c_(i)) <= f, the product evaluated in
+ * double; at least one when the row has candidates. */
+dllm_status dllm_factor_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
+                                 float factor, uint8_t* commit,
+                                 const int32_t* x0, int32_t* canvas, int64_t canvas_stride,
+                                 int64_t canvas_offset, dllm_stream_t stream);
+
+/* [ARS] entropy_bound_transfer; [MLXC] at least one accepted: commit the
+ * longest prefix of the ascending-entropy ranking whose members have
+ * sum_{j<i} H_(j) <= gamma, the sum accumulated in double in ranking order;
+ * at least one when the row has candidates. */
+dllm_status dllm_entropy_bound_transfer(const float* entropy, const uint8_t* cand, int64_t B,
+                                        int64_t L, float gamma, uint8_t* commit,
+                                        const int32_t* x0, int32_t* canvas, int64_t canvas_stride,
+                                        int64_t canvas_offset, dllm_stream_t stream);
+
+/* [ARS] edit_transfer and "Token editing (LLaDA2.1)": edit[i] = editable[i]
+ * && x0[i] != tokens[i] && prob[i] > tau_edit (NaN prob never edits).  All
+ * arrays device, B*L entries. */
+dllm_status dllm_edit_transfer(const int32_t* x0, const float* prob, const int32_t* tokens,
+                               const uint8_t* editable, int64_t B, int64_t L, float tau_edit,
+                               uint8_t* edit, dllm_stream_t stream);
+
+/* [ARS] transfer_schedule; [MOJO] even split over a block's steps:
+ * quotas[b, s] = n_b / steps + (s < n_b mod steps), n_b = max(counts[b], 0).
+ * counts: device (B,); quotas: device (B, steps).  steps > 0. */
+dllm_status dllm_transfer_schedule(const int32_t* counts, int64_t B, int32_t steps,
+                                   int32_t* quotas, dllm_stream_t stream);
+
+/* [ARS] block_ranges, "Reference loop", "Token editing": host-only, pure.
+ * Blocks start at P (align == 0) or at floor(P / block_len) * block_len
+ * (align != 0) and step by block_len; each ends at min(start + block_len,
+ * P + gen_len).  gen_len == 0 gives no block.  ranges: HOST (cap, 2) int64
+ * (may be NULL when cap == 0); *n_out receives the block count even when it
+ * exceeds cap, in which case DLLM_ERR_WORKSPACE is returned and the first
+ * cap ranges are written. */
+dllm_status dllm_block_ranges(int64_t P, int64_t gen_len, int64_t block_len, int align,
+                              int64_t* ranges, int64_t cap, int64_t* n_out);
+
+/* ------------------------------------------------------------------------
+ * Fused commit step: the statistics pass and one commit rule (plus the
+ * optional edit rule and canvas update) in one launch.  The rule of batch
+ * row b runs as soon as its L rows' statistics are complete, inside the same
+ * kernel ([MOJO] spec "possible future fused kernel": softmax, entropy and
+ * confidence, top-k, sample, scatter).  Requires L <= 1024 for the sorting
+ * rules.
+ * ------------------------------------------------------------------------ */
+typedef enum {
+  DLLM_RULE_NONE = 0,
+  DLLM_RULE_THRESHOLD = 1,     /* on prob */
+  DLLM_RULE_TOPK = 2,          /* on prob */
+  DLLM_RULE_FACTOR = 3,        /* on prob */
+  DLLM_RULE_ENTROPY_BOUND = 4  /* on entropy */
+} dllm_rule;
+
+typedef struct {
+  int32_t rule;             /* a dllm_rule */
+  int32_t strict;           /* threshold: > instead of >= */
+  float tau;                /* threshold */
+  float factor;             /* factor */
+  float gamma;              /* entropy bound */
+  const int32_t* k;         /* top-k: device (B,) */
+  const uint8_t* cand;      /* device (B, L), or NULL: cand = (canvas token == mask_id) */
+  int32_t mask_id;          /* used when cand == NULL */
+  int32_t edit;             /* non-zero: also run edit_transfer with editable = !cand */
+  float tau_edit;
+  uint8_t* commit;          /* device (B, L) output, required unless rule == NONE */
+  uint8_t* edit_mask;       /* device (B, L) output, required when edit != 0 */
+  int32_t* canvas;          /* device; NULL = no canvas update (then cand must be given) */
+  int64_t canvas_stride;    /* elements between batch rows of the canvas */
+  int64_t canvas_offset;    /* canvas column of position l = 0 */
+  int32_t* counts;          /* device (B, 3) or NULL: per batch row [candidates, commits, edits] */
+} dllm_commit_params;
+
+dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,
+                             int64_t row_stride, float temperature, uint64_t key,
+                             const int32_t* suppress_ids, int32_t n_suppress,
+                             int32_t* x0, float* prob, float* entropy,
+                             const dllm_commit_params* params,
+                             void* workspace, size_t workspace_bytes, dllm_stream_t stream);
+
+/* Reads and clears the device fault word of a workspace (synchronises the
+ * stream).  *fault = 0 when no kernel reported a fault; otherwise a code
+ * naming the wait that gave up (the kernel stopped early; outputs of that
+ * call are undefined).  Returns DLLM_ERR_CUDA if the copy fails. */
+dllm_status dllm_workspace_fault(void* workspace, dllm_stream_t stream, int32_t* fault);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DLLMCOMMIT_H */

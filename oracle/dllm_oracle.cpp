@@ -37,6 +37,7 @@
 namespace {
 
 constexpr float kNegInfThreshold = -0x1p+100f;  // -2^100
+constexpr float kPosClamp = 0x1p+100f;          // 2^100
 
 // ---------------------------------------------------------------------------
 // Philox4x32-10, from its definition in Salmon et al., "Parallel random
@@ -123,7 +124,9 @@ float gumbel_score(float z, float t, uint64_t key, int64_t row, int64_t v) {
 }
 
 // A logit as the statistics see it: bf16 widens exactly to fp32; NaN and
-// anything at or below -2^100 count as -inf (no probability mass).
+// anything at or below -2^100 count as -inf (no probability mass); anything
+// at or above 2^100 (+inf included) counts as 2^100, so the largest entries
+// share the mass equally.
 inline float load_logit(const void* base, int dtype, int64_t idx) {
   float z;
   if (dtype == 1) {
@@ -132,7 +135,8 @@ inline float load_logit(const void* base, int dtype, int64_t idx) {
   } else {
     z = static_cast<const float*>(base)[idx];
   }
-  if (std::isnan(z) || z <= kNegInfThreshold) z = -std::numeric_limits<float>::infinity();
+  if (std::isnan(z) || z <= kNegInfThreshold) return -std::numeric_limits<float>::infinity();
+  if (z >= kPosClamp) return kPosClamp;
   return z;
 }
 
@@ -185,15 +189,6 @@ RowOut stats_row(const void* logits, int dtype, int64_t row_off, int64_t V, int6
     // No finite mass anywhere: the uniform limit over A.
     out.prob = 1.0 / static_cast<double>(v_eff);
     out.entropy = std::log(static_cast<double>(v_eff));
-    return out;
-  }
-  if (m == std::numeric_limits<float>::infinity()) {
-    // The +inf entries share all the mass.
-    int64_t n_inf = 0;
-    for (int64_t v = 0; v < V; ++v)
-      if (!absent[v] && load_logit(logits, dtype, row_off + v) == std::numeric_limits<float>::infinity()) ++n_inf;
-    out.prob = (zx0 == inf) ? 1.0 / static_cast<double>(n_inf) : 0.0;
-    out.entropy = std::log(static_cast<double>(n_inf));
     return out;
   }
   // Pass 2: Z = sum exp(z - m), S = sum exp(z - m)(z - m); -inf terms add 0.

@@ -103,9 +103,12 @@ def test_all_masked_row_is_uniform_limit():
 
 
 def test_positive_infinity_shares_mass():
-    z = np.array([[0.0, np.inf, 5.0, np.inf, np.inf, 1.0]], dtype=np.float32)
+    # +inf and values >= 2^100 count as 2^100: the top entries share the mass
+    z = np.array([[0.0, np.inf, 5.0, 2.0**101, np.inf, 1.0]], dtype=np.float32)
     x0, p, h = oracle.token_stats(z)
     assert x0[0] == 1 and p[0] == pytest.approx(1 / 3) and h[0] == pytest.approx(math.log(3))
+    x0, p, h = oracle.token_stats(z, temperature=0.5, key=3)
+    assert x0[0] in (1, 3, 4) and p[0] == pytest.approx(1 / 3)
 
 
 def test_bf16_widening_matches_torch():

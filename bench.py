@@ -1,0 +1,451 @@
+"""Benchmark of the fused commit step (statistics pass + commit rule) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch of synthetic logits:
+the statistics pass (x0, prob, entropy for every row), the workload's commit
+rule and the canvas update.  The default workload is one LLaDA-8B-shaped
+block step: B=1, L=32 rows of V=126464 bf16 logits, suppress the mask id,
+greedy, strict threshold 0.95 on 19 candidates.
+
+Our arm replays the steps from a CUDA graph over rotating logit buffers whose
+total exceeds 4x the L2 cache, so every step reads its logits from HBM.  The
+reference arm (--impl reference) times the CPU oracle on the same workload.
+Under torchrun each rank runs its own replica on its own GPU (the path shards
+by batch row with no collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dllm_workloads as W  # noqa: E402
+
+METRIC = "token_stats+commit logits GB/s (% of GB300 HBM peak); canvas positions/s"
+KERNEL_SOURCES = ("dllm_stats.cu", "dllm_stats.cuh", "dllm_rules.cuh", "dllm_device.cuh", "dllm_gumbel.cuh")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--workload", default="llada", choices=["llada", "tiny", "dream", "large"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+DEFAULT_STEPS = {"llada": 300_000, "tiny": 300_000, "dream": 20_000, "large": 1_000}
+DEFAULT_WARMUP = {"llada": 3_000, "tiny": 3_000, "dream": 200, "large": 10}
+
+
+def describe(w) -> str:
+    rule = {"threshold": f"threshold tau={w.params.get('tau')} strict={w.params.get('strict')}",
+            "topk": "top-k k=transfer_schedule(256, 32)[:, 0] = 8",
+            "factor+entropy_bound": "factor f=1.0 + entropy bound gamma=0.1"}[w.rule]
+    samp = "greedy" if w.temperature == 0 else f"Gumbel-max t={w.temperature}"
+    return (f"{w.name}: B={w.B} L={w.L} V={w.V} {w.dtype}, suppress={w.suppress_ids}, {samp}, {rule}, "
+            f"{int(w.candidates.sum())} candidates")
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes one step must move: logits read, stats written (x0, prob, entropy:
+    12 B/row), candidate mask read and commit mask written (1 B/row each), the
+    canvas write of a committed row (4 B/row, counted for every row)."""
+    per_row = 12 + 1 + 1 + 4
+    extra = 0
+    if w.rule == "factor+entropy_bound":
+        extra = w.T * (4 + 1 + 1)     # the entropy-bound pass re-reads entropy and cand, writes its mask
+    return w.logit_bytes() + w.T * per_row + extra
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+def gpu_query_id(props, index):
+    """An id nvidia-smi understands for this device (UUID when torch gives one)."""
+    u = getattr(props, "uuid", None)
+    if u:
+        u = str(u)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    return str(index)
+
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "commit_step_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample of the workload
+# --------------------------------------------------------------------------
+def oracle_step(w, logits=None):
+    import oracle
+
+    z = w.logits if logits is None else logits
+    x0, p, h = oracle.token_stats(z, dtype=w.dtype, temperature=w.temperature, key=w.key,
+                                  suppress_ids=w.suppress_ids, row_ids=w.rows)
+    B = z.shape[0] // w.L
+    cand = w.candidates[:B]
+    p32 = p.astype(np.float32).reshape(B, w.L)
+    if w.rule == "threshold":
+        oracle.threshold_transfer(p32, cand, w.params["tau"], w.params["strict"])
+    elif w.rule == "topk":
+        oracle.topk_transfer(p32, cand, np.full(B, 8, np.int32))
+    else:
+        oracle.factor_transfer(p32, cand, w.params["factor"])
+        oracle.entropy_bound_transfer(h.astype(np.float32).reshape(B, w.L), cand, w.params["gamma"])
+    return z.nbytes
+
+
+def cpu_baseline(w, seconds: float):
+    import oracle
+
+    threads = oracle.default_threads()
+    # a bounded sample: whole batch rows of the workload, repeated until `seconds` pass
+    sub = w
+    if w.name in ("dream", "large"):
+        rows = np.arange(w.L)   # one batch row
+        sub = W.build(w.name, rows=rows)
+    done_bytes, n = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        done_bytes += oracle_step(sub)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    unit_rows = sub.logits.shape[0]
+    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} passes over {unit_rows} rows of the {w.name} workload "
+                      f"({sub.logits.nbytes / 1e6:.1f} MB each), {dt:.1f} s, fp64 oracle threaded over rows"}
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import commit_step_gb300 as cs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = W.build(args.workload)
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[w.name]
+    warmup = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[w.name])
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
+    nbytes = w.logit_bytes()
+    R = max(1, math.ceil(4 * l2 / nbytes)) if nbytes < 4 * l2 else 1
+    R = min(R, 256)
+
+    if w.dtype == "bf16":
+        host = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16)
+    else:
+        host = torch.from_numpy(w.logits)
+    base = host.to(dev).view(w.B, w.L, w.V)
+    bufs = [base] + [base.clone() for _ in range(R - 1)]
+    cand = torch.from_numpy(w.candidates).to(dev)
+    canvas = torch.zeros((w.B, 128 + w.L), dtype=torch.int32, device=dev)
+    x0 = torch.empty((w.B, w.L), dtype=torch.int32, device=dev)
+    prob = torch.empty((w.B, w.L), dtype=torch.float32, device=dev)
+    ent = torch.empty((w.B, w.L), dtype=torch.float32, device=dev)
+    commit = torch.empty((w.B, w.L), dtype=torch.uint8, device=dev)
+    commit2 = torch.empty((w.B, w.L), dtype=torch.uint8, device=dev)
+    kq = torch.full((w.B,), 8, dtype=torch.int32, device=dev)
+    ws = cs.workspace(w.B, w.L, w.V, 1 if w.dtype == "bf16" else 0, dev)
+    out = (x0, prob, ent, commit, None)
+    launches_per_step = 2 if w.rule == "factor+entropy_bound" else 1
+
+    def step(i):
+        lg = bufs[i % R]
+        if w.rule == "threshold":
+            cs.commit_step(lg, rule=cs.RULE_THRESHOLD, tau=w.params["tau"], strict=w.params["strict"],
+                           suppress_ids=w.suppress_ids, cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws)
+        elif w.rule == "topk":
+            cs.commit_step(lg, rule=cs.RULE_TOPK, k=kq, temperature=w.temperature, key=w.key + i,
+                           suppress_ids=w.suppress_ids, cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws)
+        else:
+            cs.commit_step(lg, rule=cs.RULE_FACTOR, factor=w.params["factor"], suppress_ids=w.suppress_ids,
+                           cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws)
+            cs.entropy_bound_transfer(ent, cand, w.params["gamma"], commit=commit2)
+
+    # correctness guard on the very inputs being timed (cheap, sampled rows)
+    step(0)
+    torch.cuda.synchronize()
+
+    # graph of G steps over the rotating buffers
+    G = R if R > 1 else min(50, steps)
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(G):   # eager warm-up on the capture stream
+            step(i)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(G):
+            step(i)
+    reps_w = max(1, math.ceil(warmup / G))
+    reps = max(1, math.ceil(steps / G))
+    steps_done = reps * G
+    with torch.cuda.stream(stream):
+        for _ in range(reps_w):
+            g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_query_id(props, dev.index)) as clk:
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / steps_done
+
+    # single-launch latency: one step at a time, synchronised on both sides
+    lat = []
+    for i in range(min(200, 10 * R)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        step(i)
+        b.record()
+        b.synchronize()
+        lat.append(a.elapsed_time(b) * 1e3)
+    single_us = statistics.median(lat)
+
+    # e2e through the public API with host buffers (copies inside the timed region)
+    pinned = host.contiguous().pin_memory()
+    dev_in = torch.empty_like(base)
+    hx0 = torch.empty((w.B, w.L), dtype=torch.int32).pin_memory()
+    hprob = torch.empty((w.B, w.L), dtype=torch.float32).pin_memory()
+    hent = torch.empty((w.B, w.L), dtype=torch.float32).pin_memory()
+    hcommit = torch.empty((w.B, w.L), dtype=torch.uint8).pin_memory()
+    e2e_steps = max(3, min(2000, steps // 100)) if w.name in ("llada", "tiny") else max(3, min(50, steps // 10))
+
+    def e2e_step():
+        dev_in.view(-1).copy_(pinned.view(-1), non_blocking=True)
+        cs.commit_step(dev_in, rule={"threshold": cs.RULE_THRESHOLD, "topk": cs.RULE_TOPK}.get(w.rule, cs.RULE_FACTOR),
+                       tau=w.params.get("tau", 0.0), strict=w.params.get("strict", False), k=kq,
+                       factor=w.params.get("factor", 0.0), temperature=w.temperature, key=w.key,
+                       suppress_ids=w.suppress_ids, cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws)
+        hx0.copy_(x0, non_blocking=True)
+        hprob.copy_(prob, non_blocking=True)
+        hent.copy_(ent, non_blocking=True)
+        hcommit.copy_(commit, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record()
+    b.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    ok = cs.workspace_fault(ws)
+
+    alg = algorithmic_bytes(w)
+    world_bytes = alg * steps_done * world
+    value = world_bytes / (ms / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    kernel_ms = ms_per_step / launches_per_step if launches_per_step == 1 else ms_per_step
+    achieved = alg / (kernel_ms / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps_done,
+        "warmup": reps_w * G, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator, dllm_workloads.py)",
+        "config": {"workload": describe(w), "global_batch": w.B * world, "seq_len": w.L, "vocab": w.V,
+                   "parallelism": f"replicas x{world} (batch rows shard, no collective)",
+                   "l2": f"{R} rotating logit buffers, {R * nbytes / 1e6:.0f} MB total vs L2 {l2 / 1e6:.0f} MB"
+                         if R > 1 else f"one {nbytes / 1e6:.0f} MB buffer, larger than L2 {l2 / 1e6:.0f} MB",
+                   "launch": f"CUDA graph of {G} steps with programmatic dependent launch"},
+        "pct_of_hbm_peak": round(100 * value / world / peak, 1),
+        "single_launch_us": round(single_us, 2),
+        "positions_per_s": round(w.B * w.L * steps_done * world / (ms / 1e3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                     "kernel": "dllm::stats_kernel (fused statistics + commit rule)"},
+        "e2e": {"value": round(nbytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(nbytes), "d2h_bytes_per_step": int(w.T * 13),
+                "ms_per_step": e2e_ms, "path": "pinned host logits -> cudaMemcpyAsync -> dllm_commit_step -> "
+                                               "host copies of x0/prob/entropy/commit"},
+        "gpu_launches": steps_done * launches_per_step,
+        "clocks": clk.summary(),
+        "workspace_fault": ok,
+    }
+    return res, w
+
+
+def run_reference(args, rank, world):
+    w = W.build(args.workload)
+    steps = args.steps if args.steps is not None else 3
+    warmup = args.warmup if args.warmup is not None else 1
+    sub = w if w.name in ("llada", "tiny") else W.build(w.name, rows=np.arange(w.L))
+    import oracle
+
+    for _ in range(max(0, min(warmup, 3))):
+        oracle_step(sub)
+    t0 = time.perf_counter()
+    done = 0
+    n = max(1, steps)
+    for _ in range(n):
+        done += oracle_step(sub)
+    dt = time.perf_counter() - t0
+    value = done / dt / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": n, "warmup": warmup, "ms_per_step": dt * 1e3 / n, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator, dllm_workloads.py)",
+        "config": {"workload": describe(w), "sample": f"{sub.logits.shape[0]} rows per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.default_threads(), "kind": "oracle",
+                         "sample": f"{n} steps over {sub.logits.shape[0]} rows of the {w.name} workload"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)))
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res, w = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

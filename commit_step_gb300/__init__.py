@@ -1,0 +1,325 @@
+"""Python binding of libdllmcommit, the GB300 commit step of diffusion-LM decoding.
+
+Argument marshalling only: every step runs in the library's CUDA kernels
+(``libdllmcommit.so``, built in-tree by ``commit_step_gb300.build``).  PyTorch
+supplies device memory and streams.  The functions carry the names of the C
+entry points without their ``dllm_`` prefix (``token_stats`` calls
+``dllm_token_stats`` and so on); see ``include/dllmcommit.h`` for the contract
+of each.
+
+Importing this package raises if the library is missing: there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdllmcommit.so")
+
+DLLM_OK = 0
+DLLM_F32, DLLM_BF16 = 0, 1
+RULE_NONE, RULE_THRESHOLD, RULE_TOPK, RULE_FACTOR, RULE_ENTROPY_BOUND = 0, 1, 2, 3, 4
+MAX_SUPPRESS = 64
+MAX_SORT_L = 16384
+FUSED_SORT_CAP = 1024
+
+EXPORTS = (
+    "dllm_status_string", "dllm_version", "dllm_token_stats_workspace_size", "dllm_token_stats",
+    "dllm_threshold_transfer", "dllm_topk_transfer", "dllm_factor_transfer", "dllm_entropy_bound_transfer",
+    "dllm_edit_transfer", "dllm_transfer_schedule", "dllm_block_ranges", "dllm_commit_step",
+    "dllm_workspace_fault",
+)
+
+
+class DllmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)}")
+        self.status = status
+
+
+class CommitParams(C.Structure):
+    """Mirror of ``dllm_commit_params``."""
+
+    _fields_ = [
+        ("rule", C.c_int32), ("strict", C.c_int32), ("tau", C.c_float), ("factor", C.c_float),
+        ("gamma", C.c_float), ("k", C.c_void_p), ("cand", C.c_void_p), ("mask_id", C.c_int32),
+        ("edit", C.c_int32), ("tau_edit", C.c_float), ("commit", C.c_void_p), ("edit_mask", C.c_void_p),
+        ("canvas", C.c_void_p), ("canvas_stride", C.c_int64), ("canvas_offset", C.c_int64),
+        ("counts", C.c_void_p),
+    ]
+
+
+def _load() -> C.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = C.CDLL(LIB_PATH)
+    P, i64, i32, f32, u64, sz = C.c_void_p, C.c_int64, C.c_int32, C.c_float, C.c_uint64, C.c_size_t
+    lib.dllm_status_string.argtypes = [C.c_int]
+    lib.dllm_status_string.restype = C.c_char_p
+    lib.dllm_version.restype = C.c_char_p
+    lib.dllm_token_stats_workspace_size.argtypes = [i64, i64, i64, C.c_int]
+    lib.dllm_token_stats_workspace_size.restype = sz
+    stats_args = [P, C.c_int, i64, i64, i64, i64, f32, u64, P, i32, P, P, P]
+    lib.dllm_token_stats.argtypes = stats_args + [P, sz, P]
+    lib.dllm_commit_step.argtypes = stats_args + [C.POINTER(CommitParams), P, sz, P]
+    tail = [P, P, i64, i64, P]
+    lib.dllm_threshold_transfer.argtypes = [P, P, i64, i64, f32, C.c_int, P] + tail
+    lib.dllm_topk_transfer.argtypes = [P, P, i64, i64, P, P] + tail
+    lib.dllm_factor_transfer.argtypes = [P, P, i64, i64, f32, P] + tail
+    lib.dllm_entropy_bound_transfer.argtypes = [P, P, i64, i64, f32, P] + tail
+    lib.dllm_edit_transfer.argtypes = [P, P, P, P, i64, i64, f32, P, P]
+    lib.dllm_transfer_schedule.argtypes = [P, i64, i32, P, P]
+    lib.dllm_block_ranges.argtypes = [i64, i64, i64, C.c_int, P, i64, P]
+    lib.dllm_workspace_fault.argtypes = [P, P, C.POINTER(C.c_int32)]
+    for name in EXPORTS[3:]:
+        if name != "dllm_token_stats_workspace_size":
+            getattr(lib, name).restype = C.c_int
+    return lib
+
+
+_lib = _load()
+
+
+def status_string(status: int) -> str:
+    return _lib.dllm_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return _lib.dllm_version().decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != DLLM_OK:
+        raise DllmError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DLLM_BF16
+    if t.dtype == torch.float32:
+        return DLLM_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("device tensors are required")
+
+
+_WS = {}
+
+
+def workspace(B: int, L: int, V: int, dtype_code: int, device: torch.device, stream=None) -> torch.Tensor:
+    """A zero-filled workspace for the statistics pass, cached per device and stream."""
+    need = int(_lib.dllm_token_stats_workspace_size(B, L, V, dtype_code))
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    key = (device.index, s.cuda_stream)
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < need:
+        with torch.cuda.stream(s):
+            ws = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=device)
+        _WS[key] = ws
+    return ws
+
+
+def _logits_view(logits: torch.Tensor):
+    if logits.dim() == 3:
+        B, L, V = logits.shape
+        if logits.stride(2) != 1 or logits.stride(0) != L * logits.stride(1):
+            raise ValueError("logits must be (B, L, V) with unit stride over V and rows evenly spaced")
+        return B, L, V, logits.stride(1)
+    if logits.dim() == 2:
+        T, V = logits.shape
+        if logits.stride(1) != 1:
+            raise ValueError("logits must have unit stride over V")
+        return 1, T, V, logits.stride(0)
+    raise ValueError("logits must be (B, L, V) or (T, V)")
+
+
+def token_stats(logits: torch.Tensor, temperature: float = 0.0, key: int = 0, suppress_ids: Sequence[int] = (),
+                out=None, ws: Optional[torch.Tensor] = None, stream=None):
+    """(x0 int32, prob float32, entropy float32), each shaped like logits without V."""
+    _need_cuda(logits)
+    B, L, V, stride = _logits_view(logits)
+    dt = _dtype_code(logits)
+    shape = logits.shape[:-1]
+    if out is None:
+        x0 = torch.empty(shape, dtype=torch.int32, device=logits.device)
+        prob = torch.empty(shape, dtype=torch.float32, device=logits.device)
+        ent = torch.empty(shape, dtype=torch.float32, device=logits.device)
+    else:
+        x0, prob, ent = out
+    sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
+    if ws is None:
+        ws = workspace(B, L, V, dt, logits.device, stream)
+    _check(_lib.dllm_token_stats(_ptr(logits), dt, B, L, V, stride, float(temperature), int(key) & (2**64 - 1),
+                                 sup, len(suppress_ids), _ptr(x0), _ptr(prob), _ptr(ent), _ptr(ws), ws.numel(),
+                                 _stream(stream)), "dllm_token_stats")
+    return x0, prob, ent
+
+
+def _canvas_args(x0, canvas, canvas_offset):
+    if canvas is None:
+        return None, None, 0, 0
+    if x0 is None:
+        raise ValueError("a canvas update needs x0")
+    if canvas.dim() != 2 or canvas.stride(1) != 1 or canvas.dtype != torch.int32:
+        raise ValueError("canvas must be a (B, N) int32 tensor with unit column stride")
+    return _ptr(x0), _ptr(canvas), canvas.stride(0), int(canvas_offset)
+
+
+def _rule_io(conf, cand, commit):
+    _need_cuda(conf, cand)
+    if conf.dtype != torch.float32 or conf.dim() != 2 or not conf.is_contiguous():
+        raise ValueError("scores must be a contiguous (B, L) float32 tensor")
+    if cand.shape != conf.shape or cand.dtype not in (torch.uint8, torch.bool) or not cand.is_contiguous():
+        raise ValueError("candidates must be a contiguous (B, L) bool/uint8 tensor")
+    if commit is None:
+        commit = torch.empty(conf.shape, dtype=torch.uint8, device=conf.device)
+    return conf.shape[0], conf.shape[1], commit
+
+
+def threshold_transfer(conf, cand, tau: float, strict: bool = False, commit=None, x0=None, canvas=None,
+                       canvas_offset: int = 0, stream=None):
+    B, L, commit = _rule_io(conf, cand, commit)
+    a = _canvas_args(x0, canvas, canvas_offset)
+    _check(_lib.dllm_threshold_transfer(_ptr(conf), _ptr(cand), B, L, float(tau), int(bool(strict)), _ptr(commit),
+                                        *a, _stream(stream)), "dllm_threshold_transfer")
+    return commit
+
+
+def topk_transfer(conf, cand, k, commit=None, x0=None, canvas=None, canvas_offset: int = 0, stream=None):
+    B, L, commit = _rule_io(conf, cand, commit)
+    if not torch.is_tensor(k):
+        k = torch.full((B,), int(k), dtype=torch.int32, device=conf.device)
+    if k.dtype != torch.int32 or k.numel() != B or not k.is_cuda:
+        raise ValueError("k must be a (B,) int32 device tensor")
+    a = _canvas_args(x0, canvas, canvas_offset)
+    _check(_lib.dllm_topk_transfer(_ptr(conf), _ptr(cand), B, L, _ptr(k), _ptr(commit), *a, _stream(stream)),
+           "dllm_topk_transfer")
+    return commit
+
+
+def factor_transfer(conf, cand, factor: float, commit=None, x0=None, canvas=None, canvas_offset: int = 0, stream=None):
+    B, L, commit = _rule_io(conf, cand, commit)
+    a = _canvas_args(x0, canvas, canvas_offset)
+    _check(_lib.dllm_factor_transfer(_ptr(conf), _ptr(cand), B, L, float(factor), _ptr(commit), *a, _stream(stream)),
+           "dllm_factor_transfer")
+    return commit
+
+
+def entropy_bound_transfer(entropy, cand, gamma: float, commit=None, x0=None, canvas=None, canvas_offset: int = 0,
+                           stream=None):
+    B, L, commit = _rule_io(entropy, cand, commit)
+    a = _canvas_args(x0, canvas, canvas_offset)
+    _check(_lib.dllm_entropy_bound_transfer(_ptr(entropy), _ptr(cand), B, L, float(gamma), _ptr(commit), *a,
+                                            _stream(stream)), "dllm_entropy_bound_transfer")
+    return commit
+
+
+def edit_transfer(x0, prob, tokens, editable, tau_edit: float, edit=None, stream=None):
+    _need_cuda(x0, prob, tokens, editable)
+    if not (x0.shape == prob.shape == tokens.shape == editable.shape) or x0.dim() != 2:
+        raise ValueError("edit_transfer inputs must share one (B, L) shape")
+    for t, dt in ((x0, torch.int32), (prob, torch.float32), (tokens, torch.int32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise ValueError("edit_transfer: x0/tokens int32, prob float32, all contiguous")
+    if edit is None:
+        edit = torch.empty(x0.shape, dtype=torch.uint8, device=x0.device)
+    B, L = x0.shape
+    _check(_lib.dllm_edit_transfer(_ptr(x0), _ptr(prob), _ptr(tokens), _ptr(editable), B, L, float(tau_edit),
+                                   _ptr(edit), _stream(stream)), "dllm_edit_transfer")
+    return edit
+
+
+def transfer_schedule(counts, steps: int, quotas=None, stream=None):
+    _need_cuda(counts)
+    if counts.dtype != torch.int32 or counts.dim() != 1 or not counts.is_contiguous():
+        raise ValueError("counts must be a contiguous (B,) int32 tensor")
+    B = counts.numel()
+    if quotas is None:
+        quotas = torch.empty((B, max(int(steps), 0)), dtype=torch.int32, device=counts.device)
+    _check(_lib.dllm_transfer_schedule(_ptr(counts), B, int(steps), _ptr(quotas), _stream(stream)),
+           "dllm_transfer_schedule")
+    return quotas
+
+
+def block_ranges(P: int, gen_len: int, block_len: int, align: bool = False):
+    n = C.c_int64(0)
+    st = _lib.dllm_block_ranges(int(P), int(gen_len), int(block_len), int(bool(align)), None, 0, C.byref(n))
+    if st not in (DLLM_OK, 3):
+        _check(st, "dllm_block_ranges")
+    buf = (C.c_int64 * max(1, 2 * n.value))()
+    _check(_lib.dllm_block_ranges(int(P), int(gen_len), int(block_len), int(bool(align)), buf, n.value, C.byref(n)),
+           "dllm_block_ranges")
+    return [(buf[2 * i], buf[2 * i + 1]) for i in range(n.value)]
+
+
+def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, suppress_ids: Sequence[int] = (),
+                cand=None, mask_id: int = -1, tau: float = 0.0, strict: bool = False, k=None, factor: float = 0.0,
+                gamma: float = 0.0, edit: bool = False, tau_edit: float = 1.0, canvas=None, canvas_offset: int = 0,
+                out=None, counts=None, ws=None, stream=None):
+    """Fused statistics pass + commit rule (+ edit rule and canvas update) in one launch.
+
+    Returns (x0, prob, entropy, commit, edit_mask); commit/edit_mask are None
+    when not requested.
+    """
+    _need_cuda(logits, cand, canvas, k, counts)
+    B, L, V, stride = _logits_view(logits)
+    dt = _dtype_code(logits)
+    dev = logits.device
+    if out is None:
+        x0 = torch.empty((B, L), dtype=torch.int32, device=dev)
+        prob = torch.empty((B, L), dtype=torch.float32, device=dev)
+        ent = torch.empty((B, L), dtype=torch.float32, device=dev)
+        commit = torch.empty((B, L), dtype=torch.uint8, device=dev) if rule != RULE_NONE else None
+        edit_mask = torch.empty((B, L), dtype=torch.uint8, device=dev) if edit else None
+    else:
+        x0, prob, ent, commit, edit_mask = out
+    if rule == RULE_TOPK and not torch.is_tensor(k):
+        k = torch.full((B,), int(k), dtype=torch.int32, device=dev)
+    p = CommitParams()
+    p.rule, p.strict, p.tau, p.factor, p.gamma = int(rule), int(bool(strict)), float(tau), float(factor), float(gamma)
+    p.k = None if k is None else k.data_ptr()
+    p.cand = None if cand is None else cand.data_ptr()
+    p.mask_id = int(mask_id)
+    p.edit, p.tau_edit = int(bool(edit)), float(tau_edit)
+    p.commit = None if commit is None else commit.data_ptr()
+    p.edit_mask = None if edit_mask is None else edit_mask.data_ptr()
+    if canvas is not None:
+        if canvas.dim() != 2 or canvas.stride(1) != 1 or canvas.dtype != torch.int32:
+            raise ValueError("canvas must be a (B, N) int32 tensor with unit column stride")
+        p.canvas, p.canvas_stride, p.canvas_offset = canvas.data_ptr(), canvas.stride(0), int(canvas_offset)
+    p.counts = None if counts is None else counts.data_ptr()
+    sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
+    if ws is None:
+        ws = workspace(B, L, V, dt, dev, stream)
+    _check(_lib.dllm_commit_step(_ptr(logits), dt, B, L, V, stride, float(temperature), int(key) & (2**64 - 1),
+                                 sup, len(suppress_ids), _ptr(x0), _ptr(prob), _ptr(ent), C.byref(p), _ptr(ws),
+                                 ws.numel(), _stream(stream)), "dllm_commit_step")
+    return x0, prob, ent, commit, edit_mask
+
+
+def workspace_fault(ws: torch.Tensor, stream=None) -> int:
+    f = C.c_int32(0)
+    _check(_lib.dllm_workspace_fault(_ptr(ws), _stream(stream), C.byref(f)), "dllm_workspace_fault")
+    return f.value
+
+
+def lib_handle() -> C.CDLL:
+    return _lib

@@ -1,0 +1,427 @@
+// dllm_api.cu -- the C ABI of libdllmcommit (include/dllmcommit.h): argument
+// validation, launch planning, workspace layout and kernel launches.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/dllmcommit.h"
+#include "dllm_stats.cuh"
+
+namespace dllm {
+const void* stats_kernel_ptr(bool bf16, bool gumbel);
+const void* rules_kernel_ptr(int nt);
+const void* edit_kernel_ptr();
+const void* schedule_kernel_ptr();
+}  // namespace dllm
+
+namespace {
+
+using namespace dllm;
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kStatsSmemMax = static_cast<size_t>(kRingBytes) + kFusedSortCap * 9;
+
+struct DeviceInfo {
+  int sms = 0;
+  int occ[4] = {0, 0, 0, 0};  // CTAs per SM of stats_kernel<bf16, gumbel>, index 2*bf16+gumbel
+  cudaError_t err = cudaSuccess;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(g_once[dev], [dev]() {
+    DeviceInfo& d = g_dev[dev];
+    d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    for (int v = 0; v < 4 && d.err == cudaSuccess; ++v) {
+      const void* k = stats_kernel_ptr(v >= 2, (v & 1) != 0);
+      d.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmemMax));
+      if (d.err != cudaSuccess) break;
+      int n = 0;
+      d.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kThreads, kStatsSmemMax);
+      d.occ[v] = std::max(1, std::min(n, kMaxCtasPerSm));
+    }
+    for (int nt : {128, 256, 512, 1024}) {
+      if (d.err != cudaSuccess) break;
+      d.err = cudaFuncSetAttribute(rules_kernel_ptr(nt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   DLLM_MAX_SORT_L * 9);
+    }
+  });
+  const DeviceInfo* d = &g_dev[dev];
+  return d->err == cudaSuccess ? d : nullptr;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t fault = 0, row_count = 0, batch_count = 0, partials = 0, total = 0;
+};
+
+// Fault word, then the partials (a size fixed per device), then the counters.
+// Counters of every shape share one region that only ever holds counters, and
+// every successful call returns the counters it used to zero, so a workspace
+// serves calls of any shape in turn.
+WsLayout ws_layout(int64_t B, int64_t L, int sms) {
+  WsLayout w;
+  w.fault = 0;
+  w.partials = 256;
+  w.row_count = w.partials + static_cast<size_t>(2) * sms * kMaxCtasPerSm * sizeof(Partial);
+  w.batch_count = w.row_count + static_cast<size_t>(B * L) * 4;
+  w.total = align_up(w.batch_count + static_cast<size_t>(B) * 4, 256);
+  return w;
+}
+
+struct StatsPlan {
+  int64_t nvec, K, U;
+  int32_t tail, chunk_vec, P, stages;
+};
+
+StatsPlan plan_stats(int64_t T, int64_t V, int esize, int ctas) {
+  StatsPlan pl{};
+  pl.nvec = (V * esize) / 16;
+  pl.tail = static_cast<int32_t>(V - pl.nvec * (16 / esize));
+  const int64_t total_vec = T * std::max<int64_t>(pl.nvec, 1);
+  const int64_t per_cta = total_vec / std::max(ctas, 1);
+  int chunk = 1024;
+  while (chunk > 256 && static_cast<int64_t>(4) * chunk > per_cta) chunk >>= 1;
+  pl.chunk_vec = chunk;
+  pl.stages = std::min(kMaxStages, kRingBytes / (chunk * 16));
+  pl.K = pl.nvec > 0 ? (pl.nvec + chunk - 1) / chunk : 1;
+  pl.U = T * pl.K;
+  pl.P = static_cast<int32_t>(std::min<int64_t>(pl.U, ctas));
+  return pl;
+}
+
+dllm_status launch(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kernel, args) == cudaSuccess ? DLLM_OK : DLLM_ERR_CUDA;
+}
+
+int esize_of(dllm_dtype dt) { return dt == DLLM_BF16 ? 2 : 4; }
+
+// Shared validation of the statistics arguments; fills the suppress list.
+dllm_status check_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
+                        float temperature, const int32_t* sup, int32_t n_sup, const int32_t* x0, const float* prob,
+                        const float* entropy, std::vector<int32_t>& sorted_sup) {
+  if (B < 0 || L < 0 || V < 1 || V > INT32_MAX || row_stride < V) return DLLM_ERR_INVALID_ARGUMENT;
+  if (dt != DLLM_F32 && dt != DLLM_BF16) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!(temperature >= 0.0f) || std::isinf(temperature)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (n_sup < 0 || (n_sup > 0 && !sup)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (n_sup > DLLM_MAX_SUPPRESS) return DLLM_ERR_UNSUPPORTED;
+  sorted_sup.assign(sup, sup + n_sup);
+  for (int32_t id : sorted_sup)
+    if (id < 0 || id >= V) return DLLM_ERR_INVALID_ARGUMENT;
+  std::sort(sorted_sup.begin(), sorted_sup.end());
+  sorted_sup.erase(std::unique(sorted_sup.begin(), sorted_sup.end()), sorted_sup.end());
+  if (static_cast<int64_t>(sorted_sup.size()) >= V) return DLLM_ERR_INVALID_ARGUMENT;  // empty token set
+  if (B * L == 0) return DLLM_OK;
+  if (!logits || !x0 || !prob || !entropy) return DLLM_ERR_INVALID_ARGUMENT;
+  const int es = esize_of(dt);
+  if ((reinterpret_cast<uintptr_t>(logits) & 15u) != 0 || (row_stride * es) % 16 != 0) return DLLM_ERR_UNSUPPORTED;
+  return DLLM_OK;
+}
+
+dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
+                      float temperature, uint64_t key, const std::vector<int32_t>& sup, int32_t* x0, float* prob,
+                      float* entropy, const RuleArgs* rule, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const DeviceInfo* d = device_info();
+  if (!d) return DLLM_ERR_CUDA;
+  const bool bf16 = dt == DLLM_BF16, gumbel = temperature > 0.0f;
+  const int es = esize_of(dt);
+  const int64_t T = B * L;
+  const WsLayout lay = ws_layout(B, L, d->sms);
+  if (!ws || ws_bytes < lay.total) return DLLM_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0) return DLLM_ERR_INVALID_ARGUMENT;
+  const int occ = d->occ[(bf16 ? 2 : 0) + (gumbel ? 1 : 0)];
+  const StatsPlan pl = plan_stats(T, V, es, d->sms * occ);
+
+  StatsParams p{};
+  p.logits = static_cast<const uint8_t*>(logits);
+  p.row_bytes = row_stride * es;
+  p.T = T;
+  p.V = V;
+  p.L = L;
+  p.nvec = pl.nvec;
+  p.tail = pl.tail;
+  p.chunk_vec = pl.chunk_vec;
+  p.K = pl.K;
+  p.U = pl.U;
+  p.P = pl.P;
+  p.stages = pl.stages;
+  p.temperature = temperature;
+  p.key.k0 = static_cast<uint32_t>(key);
+  p.key.k1 = static_cast<uint32_t>(key >> 32);
+  p.n_sup = static_cast<int32_t>(sup.size());
+  for (size_t i = 0; i < sup.size(); ++i) p.sup[i] = sup[i];
+  p.ln_veff = static_cast<float>(std::log(static_cast<double>(V - static_cast<int64_t>(sup.size()))));
+  p.x0 = x0;
+  p.prob = prob;
+  p.entropy = entropy;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.fault = reinterpret_cast<int32_t*>(w + lay.fault);
+  p.row_count = reinterpret_cast<int32_t*>(w + lay.row_count);
+  p.batch_count = reinterpret_cast<int32_t*>(w + lay.batch_count);
+  p.partials = reinterpret_cast<Partial*>(w + lay.partials);
+  p.fused = rule ? 1 : 0;
+  if (rule) p.rule = *rule;
+  const size_t smem = static_cast<size_t>(pl.stages) * pl.chunk_vec * 16 + (rule ? kFusedSortCap * 9 : 0);
+  void* args[] = {&p};
+  return launch(stats_kernel_ptr(bf16, gumbel), dim3(pl.P), dim3(kThreads), smem, s, args);
+}
+
+int next_pow2(int64_t x) {
+  int n = 1;
+  while (n < x) n <<= 1;
+  return n;
+}
+
+dllm_status check_rule_tail(int64_t B, int64_t L, const int32_t* x0, const int32_t* canvas, int64_t canvas_stride,
+                            int64_t canvas_offset) {
+  if ((x0 == nullptr) != (canvas == nullptr)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (canvas) {
+    if (canvas_offset < 0 || canvas_stride < 0) return DLLM_ERR_INVALID_ARGUMENT;
+    if (B > 1 && canvas_stride < canvas_offset + L) return DLLM_ERR_INVALID_ARGUMENT;
+  }
+  return DLLM_OK;
+}
+
+dllm_status run_rule_kernel(const RuleArgs& a, int64_t B, int64_t L, cudaStream_t s) {
+  const DeviceInfo* d = device_info();
+  if (!d) return DLLM_ERR_CUDA;
+  const bool sorting = a.rule == kRuleTopk || a.rule == kRuleFactor || a.rule == kRuleEntropyBound;
+  int cap = 0, nt = 128;
+  if (sorting) {
+    if (L > DLLM_MAX_SORT_L) return DLLM_ERR_UNSUPPORTED;
+    cap = next_pow2(L);
+    nt = std::min(1024, std::max(128, cap / 2));
+  } else {
+    nt = L >= 1024 ? 1024 : (L >= 512 ? 512 : (L >= 256 ? 256 : 128));
+  }
+  RuleArgs args_copy = a;
+  int32_t cap_arg = cap;
+  void* args[] = {&args_copy, &cap_arg};
+  return launch(rules_kernel_ptr(nt), dim3(static_cast<unsigned>(B)), dim3(nt), static_cast<size_t>(cap) * 9, s, args);
+}
+
+dllm_status rule_entry(int32_t kind, const float* conf, const uint8_t* cand, int64_t B, int64_t L, float tau,
+                       int strict, const int32_t* k, float factor, float gamma, uint8_t* commit, const int32_t* x0,
+                       int32_t* canvas, int64_t canvas_stride, int64_t canvas_offset, cudaStream_t s) {
+  if (B < 0 || L < 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (B > INT32_MAX || L > INT32_MAX) return DLLM_ERR_UNSUPPORTED;
+  if (B * L == 0) return DLLM_OK;
+  if (!conf || !cand || !commit) return DLLM_ERR_INVALID_ARGUMENT;
+  if (kind == kRuleTopk && !k) return DLLM_ERR_INVALID_ARGUMENT;
+  if (std::isnan(tau) || std::isnan(factor) || std::isnan(gamma)) return DLLM_ERR_INVALID_ARGUMENT;
+  dllm_status st = check_rule_tail(B, L, x0, canvas, canvas_stride, canvas_offset);
+  if (st != DLLM_OK) return st;
+  RuleArgs a{};
+  a.rule = kind;
+  a.strict = strict ? 1 : 0;
+  a.tau = tau;
+  a.factor = factor;
+  a.gamma = gamma;
+  a.k = k;
+  a.conf = conf;
+  a.entropy = conf;
+  a.cand = cand;
+  a.commit = commit;
+  a.x0 = x0;
+  a.canvas = canvas;
+  a.canvas_stride = canvas_stride;
+  a.canvas_offset = canvas_offset;
+  a.L = L;
+  return run_rule_kernel(a, B, L, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dllm_status_string(dllm_status status) {
+  switch (status) {
+    case DLLM_OK: return "DLLM_OK";
+    case DLLM_ERR_INVALID_ARGUMENT: return "DLLM_ERR_INVALID_ARGUMENT: a shape, pointer, value or alignment is wrong";
+    case DLLM_ERR_UNSUPPORTED: return "DLLM_ERR_UNSUPPORTED: valid, but outside what this build handles";
+    case DLLM_ERR_WORKSPACE: return "DLLM_ERR_WORKSPACE: workspace missing or too small";
+    case DLLM_ERR_CUDA: return "DLLM_ERR_CUDA: a CUDA launch or query failed";
+    case DLLM_ERR_DEVICE: return "DLLM_ERR_DEVICE: a kernel reported a fault";
+  }
+  return "unknown dllm_status";
+}
+
+const char* dllm_version(void) { return "libdllmcommit 0.1.0 (sm_103a)"; }
+
+size_t dllm_token_stats_workspace_size(int64_t B, int64_t L, int64_t V, dllm_dtype dt) {
+  (void)V;
+  (void)dt;
+  if (B < 0 || L < 0) return 0;
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 160;  // no device: size for the largest part this build targets
+  return ws_layout(B, L, sms).total;
+}
+
+dllm_status dllm_token_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
+                             float temperature, uint64_t key, const int32_t* suppress_ids, int32_t n_suppress,
+                             int32_t* x0, float* prob, float* entropy, void* workspace, size_t workspace_bytes,
+                             dllm_stream_t stream) {
+  std::vector<int32_t> sup;
+  dllm_status st = check_stats(logits, dt, B, L, V, row_stride, temperature, suppress_ids, n_suppress, x0, prob,
+                               entropy, sup);
+  if (st != DLLM_OK || B * L == 0) return st;
+  return run_stats(logits, dt, B, L, V, row_stride, temperature, key, sup, x0, prob, entropy, nullptr, workspace,
+                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dllm_status dllm_threshold_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L, float tau,
+                                    int strict, uint8_t* commit, const int32_t* x0, int32_t* canvas,
+                                    int64_t canvas_stride, int64_t canvas_offset, dllm_stream_t stream) {
+  return rule_entry(kRuleThreshold, conf, cand, B, L, tau, strict, nullptr, 0.f, 0.f, commit, x0, canvas,
+                    canvas_stride, canvas_offset, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dllm_status dllm_topk_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L, const int32_t* k,
+                               uint8_t* commit, const int32_t* x0, int32_t* canvas, int64_t canvas_stride,
+                               int64_t canvas_offset, dllm_stream_t stream) {
+  return rule_entry(kRuleTopk, conf, cand, B, L, 0.f, 0, k, 0.f, 0.f, commit, x0, canvas, canvas_stride,
+                    canvas_offset, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dllm_status dllm_factor_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L, float factor,
+                                 uint8_t* commit, const int32_t* x0, int32_t* canvas, int64_t canvas_stride,
+                                 int64_t canvas_offset, dllm_stream_t stream) {
+  return rule_entry(kRuleFactor, conf, cand, B, L, 0.f, 0, nullptr, factor, 0.f, commit, x0, canvas, canvas_stride,
+                    canvas_offset, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dllm_status dllm_entropy_bound_transfer(const float* entropy, const uint8_t* cand, int64_t B, int64_t L, float gamma,
+                                        uint8_t* commit, const int32_t* x0, int32_t* canvas, int64_t canvas_stride,
+                                        int64_t canvas_offset, dllm_stream_t stream) {
+  return rule_entry(kRuleEntropyBound, entropy, cand, B, L, 0.f, 0, nullptr, 0.f, gamma, commit, x0, canvas,
+                    canvas_stride, canvas_offset, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dllm_status dllm_edit_transfer(const int32_t* x0, const float* prob, const int32_t* tokens, const uint8_t* editable,
+                               int64_t B, int64_t L, float tau_edit, uint8_t* edit, dllm_stream_t stream) {
+  if (B < 0 || L < 0 || std::isnan(tau_edit)) return DLLM_ERR_INVALID_ARGUMENT;
+  const int64_t n = B * L;
+  if (n == 0) return DLLM_OK;
+  if (!x0 || !prob || !tokens || !editable || !edit) return DLLM_ERR_INVALID_ARGUMENT;
+  const DeviceInfo* d = device_info();
+  if (!d) return DLLM_ERR_CUDA;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(d->sms) * 8);
+  void* args[] = {const_cast<int32_t**>(&x0), const_cast<float**>(&prob), const_cast<int32_t**>(&tokens),
+                  const_cast<uint8_t**>(&editable), const_cast<int64_t*>(&n), &tau_edit, &edit};
+  return launch(edit_kernel_ptr(), dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                reinterpret_cast<cudaStream_t>(stream), args);
+}
+
+dllm_status dllm_transfer_schedule(const int32_t* counts, int64_t B, int32_t steps, int32_t* quotas,
+                                   dllm_stream_t stream) {
+  if (B < 0 || steps <= 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (B == 0) return DLLM_OK;
+  if (!counts || !quotas) return DLLM_ERR_INVALID_ARGUMENT;
+  const DeviceInfo* d = device_info();
+  if (!d) return DLLM_ERR_CUDA;
+  const int64_t total = B * steps;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(d->sms) * 8);
+  void* args[] = {const_cast<int32_t**>(&counts), &B, &steps, &quotas};
+  return launch(schedule_kernel_ptr(), dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                reinterpret_cast<cudaStream_t>(stream), args);
+}
+
+dllm_status dllm_block_ranges(int64_t P, int64_t gen_len, int64_t block_len, int align, int64_t* ranges, int64_t cap,
+                              int64_t* n_out) {
+  if (P < 0 || gen_len < 0 || block_len <= 0 || cap < 0 || !n_out) return DLLM_ERR_INVALID_ARGUMENT;
+  if (cap > 0 && !ranges) return DLLM_ERR_INVALID_ARGUMENT;
+  if (P > INT64_MAX - gen_len) return DLLM_ERR_INVALID_ARGUMENT;
+  const int64_t first = align ? (P / block_len) * block_len : P;
+  const int64_t stop = P + gen_len;
+  const int64_t n = gen_len == 0 ? 0 : (stop - first + block_len - 1) / block_len;
+  for (int64_t i = 0; i < n && i < cap; ++i) {
+    const int64_t start = first + i * block_len;
+    ranges[2 * i] = start;
+    ranges[2 * i + 1] = std::min(start + block_len, stop);
+  }
+  *n_out = n;
+  return n > cap ? DLLM_ERR_WORKSPACE : DLLM_OK;
+}
+
+dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
+                             float temperature, uint64_t key, const int32_t* suppress_ids, int32_t n_suppress,
+                             int32_t* x0, float* prob, float* entropy, const dllm_commit_params* cp, void* workspace,
+                             size_t workspace_bytes, dllm_stream_t stream) {
+  std::vector<int32_t> sup;
+  dllm_status st = check_stats(logits, dt, B, L, V, row_stride, temperature, suppress_ids, n_suppress, x0, prob,
+                               entropy, sup);
+  if (st != DLLM_OK) return st;
+  if (!cp) return DLLM_ERR_INVALID_ARGUMENT;
+  if (cp->rule < DLLM_RULE_NONE || cp->rule > DLLM_RULE_ENTROPY_BOUND) return DLLM_ERR_INVALID_ARGUMENT;
+  if (B * L == 0) return DLLM_OK;
+  if (B > INT32_MAX || L > INT32_MAX) return DLLM_ERR_UNSUPPORTED;
+  if (cp->rule != DLLM_RULE_NONE && !cp->commit) return DLLM_ERR_INVALID_ARGUMENT;
+  if (cp->rule == DLLM_RULE_TOPK && !cp->k) return DLLM_ERR_INVALID_ARGUMENT;
+  if (cp->edit && !cp->edit_mask) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!cp->cand && !cp->canvas) return DLLM_ERR_INVALID_ARGUMENT;
+  if (std::isnan(cp->tau) || std::isnan(cp->factor) || std::isnan(cp->gamma) || std::isnan(cp->tau_edit))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  const bool sorting = cp->rule == DLLM_RULE_TOPK || cp->rule == DLLM_RULE_FACTOR || cp->rule == DLLM_RULE_ENTROPY_BOUND;
+  if (sorting && L > kFusedSortCap) return DLLM_ERR_UNSUPPORTED;
+  if (cp->canvas) {
+    if (cp->canvas_offset < 0 || cp->canvas_stride < 0) return DLLM_ERR_INVALID_ARGUMENT;
+    if (B > 1 && cp->canvas_stride < cp->canvas_offset + L) return DLLM_ERR_INVALID_ARGUMENT;
+  }
+  RuleArgs a{};
+  a.rule = cp->rule;
+  a.strict = cp->strict ? 1 : 0;
+  a.tau = cp->tau;
+  a.factor = cp->factor;
+  a.gamma = cp->gamma;
+  a.k = cp->k;
+  a.conf = prob;
+  a.entropy = entropy;
+  a.cand = cp->cand;
+  a.mask_id = cp->mask_id;
+  a.edit = cp->edit ? 1 : 0;
+  a.tau_edit = cp->tau_edit;
+  a.x0 = x0;
+  a.commit = cp->commit;
+  a.edit_mask = cp->edit ? cp->edit_mask : nullptr;
+  a.canvas = cp->canvas;
+  a.canvas_stride = cp->canvas_stride;
+  a.canvas_offset = cp->canvas_offset;
+  a.counts = cp->counts;
+  a.L = L;
+  return run_stats(logits, dt, B, L, V, row_stride, temperature, key, sup, x0, prob, entropy, &a, workspace,
+                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dllm_status dllm_workspace_fault(void* workspace, dllm_stream_t stream, int32_t* fault) {
+  if (!workspace || !fault) return DLLM_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return DLLM_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DLLM_ERR_CUDA;
+  if (v != 0 && cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess) return DLLM_ERR_CUDA;
+  *fault = v;
+  return DLLM_OK;
+}
+
+}  // extern "C"

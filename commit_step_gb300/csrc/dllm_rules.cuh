@@ -1,0 +1,283 @@
+// dllm_rules.cuh -- the commit rules of one batch row, run by NT threads.
+//
+// Sources (page, section):
+//   mlx-arsenal "dLLM block decoding": "What mlx-arsenal ships" (the
+//   threshold, top-k, factor, entropy-bound and edit rules), "Deviations from
+//   the references" (stable ranking, the forced token is the earliest maximal
+//   one, no factor off-by-one), "Token editing (LLaDA2.1)".
+//   mlxcel "Block Diffusion": "Samplers and Reveal Policies" (forced progress,
+//   at least one accepted under the entropy bound).
+//
+// Ranking keys are 64-bit: (order-preserving score bits << 32) | position, so
+// a plain ascending sort gives "best first, ties to the lower position".
+// Confidences rank descending with NaN as -inf; entropies rank ascending with
+// NaN as +inf.  The factor product and the entropy prefix sum are evaluated in
+// double with explicitly rounded operations, in ranking order.
+#pragma once
+
+#include <cstdint>
+
+#include "dllm_device.cuh"
+
+namespace dllm {
+
+enum RuleKind : int32_t { kRuleNone = 0, kRuleThreshold = 1, kRuleTopk = 2, kRuleFactor = 3, kRuleEntropyBound = 4 };
+
+struct RuleArgs {
+  int32_t rule;
+  int32_t strict;
+  float tau, factor, gamma;
+  const int32_t* k;        // (B,) top-k quotas
+  const float* conf;       // (B, L) confidence (threshold / top-k / factor)
+  const float* entropy;    // (B, L) entropy (entropy bound)
+  const uint8_t* cand;     // (B, L) or nullptr: cand = canvas token == mask_id
+  int32_t mask_id;
+  int32_t edit;            // also apply the edit rule with editable = !cand
+  float tau_edit;
+  const int32_t* x0;       // (B, L) proposals (canvas update / edit)
+  uint8_t* commit;         // (B, L)
+  uint8_t* edit_mask;      // (B, L) when edit
+  int32_t* canvas;         // nullable
+  int64_t canvas_stride, canvas_offset;
+  int32_t* counts;         // (B, 3) or nullptr
+  int64_t L;
+};
+
+constexpr uint64_t kNoKey = ~0ull;
+
+__device__ __forceinline__ float nan_to(float x, float v) { return x != x ? v : x; }
+
+__device__ __forceinline__ uint64_t desc_key(float c, int64_t l) {
+  const float cc = nan_to(c, -__int_as_float(0x7F800000));
+  return (static_cast<uint64_t>(~float_key(cc)) << 32) | static_cast<uint32_t>(l);
+}
+
+__device__ __forceinline__ uint64_t asc_key(float h, int64_t l) {
+  const float hh = nan_to(h, __int_as_float(0x7F800000));
+  return (static_cast<uint64_t>(float_key(hh)) << 32) | static_cast<uint32_t>(l);
+}
+
+// Synchronisation among the NT threads running a rule: a named barrier when
+// they are a subset of the CTA, __syncthreads when they are all of it.
+template <int NT, int BAR>
+__device__ __forceinline__ void rsync() {
+  if (BAR == 0)
+    __syncthreads();
+  else
+    named_sync(BAR, NT);
+}
+
+struct RuleScratch {
+  uint64_t* keys;     // capacity `cap` keys (power of two)
+  uint8_t* flags;     // capacity `cap` bytes
+  uint64_t* red64;    // NT/32 entries
+  int32_t* red32;     // 4 * NT/32 entries
+  int32_t cap;
+};
+
+template <int NT, int BAR>
+__device__ __forceinline__ uint64_t rule_min_u64(uint64_t v, const RuleScratch& s, int tid) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w < v ? w : v;
+  }
+  rsync<NT, BAR>();
+  if ((tid & 31) == 0) s.red64[tid >> 5] = v;
+  rsync<NT, BAR>();
+  v = s.red64[0];
+#pragma unroll
+  for (int w = 1; w < NT / 32; ++w) v = s.red64[w] < v ? s.red64[w] : v;
+  return v;
+}
+
+// Sums of up to four int32 counters over the NT threads.
+template <int NT, int BAR>
+__device__ __forceinline__ int4 rule_sum4(int4 v, const RuleScratch& s, int tid) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xFFFFFFFFu, v.x, o);
+    v.y += __shfl_xor_sync(0xFFFFFFFFu, v.y, o);
+    v.z += __shfl_xor_sync(0xFFFFFFFFu, v.z, o);
+    v.w += __shfl_xor_sync(0xFFFFFFFFu, v.w, o);
+  }
+  rsync<NT, BAR>();
+  if ((tid & 31) == 0) {
+    s.red32[4 * (tid >> 5) + 0] = v.x;
+    s.red32[4 * (tid >> 5) + 1] = v.y;
+    s.red32[4 * (tid >> 5) + 2] = v.z;
+    s.red32[4 * (tid >> 5) + 3] = v.w;
+  }
+  rsync<NT, BAR>();
+  int4 t = make_int4(0, 0, 0, 0);
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    t.x += s.red32[4 * w + 0];
+    t.y += s.red32[4 * w + 1];
+    t.z += s.red32[4 * w + 2];
+    t.w += s.red32[4 * w + 3];
+  }
+  return t;
+}
+
+// Ascending bitonic sort of n (a power of two) keys in shared memory.
+template <int NT, int BAR>
+__device__ __forceinline__ void bitonic_sort(uint64_t* keys, int n, int tid) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      rsync<NT, BAR>();
+      for (int i = tid; i < (n >> 1); i += NT) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const uint64_t a = keys[lo], b = keys[hi];
+        if ((a > b) == up) {
+          keys[lo] = b;
+          keys[hi] = a;
+        }
+      }
+    }
+  }
+  rsync<NT, BAR>();
+}
+
+__device__ __forceinline__ bool is_candidate(const RuleArgs& a, int64_t b, int64_t l, int32_t* tok_out) {
+  const int64_t i = b * a.L + l;
+  int32_t tok = 0;
+  if (a.canvas) tok = a.canvas[b * a.canvas_stride + a.canvas_offset + l];
+  *tok_out = tok;
+  if (a.cand) return __ldcg(a.cand + i) != 0;
+  return tok == a.mask_id;
+}
+
+// Runs the rule of batch row b.  All NT threads must call it.  Inputs written
+// by other CTAs of the same kernel are read through L2 (ld.global.cg).
+template <int NT, int BAR>
+__device__ void run_rule(const RuleArgs& a, int64_t b, const RuleScratch& s, int tid) {
+  const int64_t L = a.L;
+  const int64_t base = b * L;
+  int32_t n_commit_forced = 0;
+  uint64_t forced = kNoKey;
+  int64_t n_take = 0;      // sorting rules: commit the first n_take ranked keys
+  int n_cand_total = 0;
+
+  if (a.rule == kRuleThreshold || a.rule == kRuleNone) {
+    int any_pass = 0, n_cand = 0;
+    uint64_t best = kNoKey;
+    for (int64_t l = tid; l < L; l += NT) {
+      int32_t tok;
+      if (!is_candidate(a, b, l, &tok)) continue;
+      ++n_cand;
+      if (a.rule == kRuleThreshold) {
+        const float c = nan_to(__ldcg(a.conf + base + l), -__int_as_float(0x7F800000));
+        const bool pass = a.strict ? (c > a.tau) : (c >= a.tau);
+        any_pass |= pass ? 1 : 0;
+        const uint64_t key = desc_key(c, l);
+        best = key < best ? key : best;
+      }
+    }
+    const int4 t = rule_sum4<NT, BAR>(make_int4(n_cand, any_pass, 0, 0), s, tid);
+    n_cand_total = t.x;
+    if (a.rule == kRuleThreshold) {
+      best = rule_min_u64<NT, BAR>(best, s, tid);
+      if (t.x > 0 && t.y == 0) forced = best;
+    }
+  } else {
+    int n = 1;
+    while (n < L) n <<= 1;
+    // n <= s.cap is guaranteed by the host
+    int n_cand = 0;
+    for (int64_t l = tid; l < n; l += NT) {
+      uint64_t key = kNoKey;
+      if (l < L) {
+        int32_t tok;
+        if (is_candidate(a, b, l, &tok)) {
+          ++n_cand;
+          key = (a.rule == kRuleEntropyBound) ? asc_key(__ldcg(a.entropy + base + l), l)
+                                              : desc_key(__ldcg(a.conf + base + l), l);
+        }
+      }
+      s.keys[l] = key;
+    }
+    n_cand_total = rule_sum4<NT, BAR>(make_int4(n_cand, 0, 0, 0), s, tid).x;
+    bitonic_sort<NT, BAR>(s.keys, n, tid);
+    if (a.rule == kRuleTopk) {
+      const int32_t kb = __ldcg(a.k + b);
+      n_take = kb < 0 ? 0 : (kb > n_cand_total ? n_cand_total : kb);
+    } else if (a.rule == kRuleFactor) {
+      // first rank i whose (i+1)(1 - c_(i)) exceeds f, in double
+      uint64_t first_fail = static_cast<uint64_t>(n_cand_total);
+      for (int i = tid; i < n_cand_total; i += NT) {
+        const int64_t l = static_cast<int64_t>(s.keys[i] & 0xFFFFFFFFu);
+        const double c = nan_to(__ldcg(a.conf + base + l), -__int_as_float(0x7F800000));
+        const double lhs = __dmul_rn(static_cast<double>(i + 1), __dsub_rn(1.0, c));
+        if (!(lhs <= static_cast<double>(a.factor))) {
+          first_fail = static_cast<uint64_t>(i) < first_fail ? static_cast<uint64_t>(i) : first_fail;
+        }
+      }
+      n_take = static_cast<int64_t>(rule_min_u64<NT, BAR>(first_fail, s, tid));
+    } else {  // entropy bound: sequential double prefix in ranking order
+      if (tid == 0) {
+        double prefix = 0.0;
+        int64_t n_acc = 0;
+        while (n_acc < n_cand_total && prefix <= static_cast<double>(a.gamma)) {
+          const int64_t l = static_cast<int64_t>(s.keys[n_acc] & 0xFFFFFFFFu);
+          const float h = nan_to(__ldcg(a.entropy + base + l), __int_as_float(0x7F800000));
+          prefix = __dadd_rn(prefix, static_cast<double>(h));
+          ++n_acc;
+        }
+        s.red64[0] = static_cast<uint64_t>(n_acc);
+      }
+      rsync<NT, BAR>();
+      n_take = static_cast<int64_t>(s.red64[0]);
+      rsync<NT, BAR>();
+    }
+    if (a.rule != kRuleTopk && n_cand_total > 0 && n_take < 1) n_take = 1;
+    // flags[l] = 1 for the first n_take ranked candidates
+    for (int64_t l = tid; l < L; l += NT) s.flags[l] = 0;
+    rsync<NT, BAR>();
+    for (int64_t i = tid; i < n_take; i += NT) s.flags[s.keys[i] & 0xFFFFFFFFu] = 1;
+    rsync<NT, BAR>();
+  }
+
+  // Write the masks and update the canvas.
+  int n_commit = 0, n_edit = 0;
+  for (int64_t l = tid; l < L; l += NT) {
+    int32_t tok;
+    const bool cand = is_candidate(a, b, l, &tok);
+    bool commit = false;
+    if (a.rule == kRuleThreshold) {
+      if (cand) {
+        const float c = nan_to(__ldcg(a.conf + base + l), -__int_as_float(0x7F800000));
+        commit = a.strict ? (c > a.tau) : (c >= a.tau);
+        if (forced != kNoKey && static_cast<int64_t>(forced & 0xFFFFFFFFu) == l) commit = true;
+      }
+    } else if (a.rule != kRuleNone) {
+      commit = s.flags[l] != 0;
+    }
+    bool edit = false;
+    int32_t x0 = 0;
+    if (a.x0) x0 = __ldcg(a.x0 + base + l);
+    if (a.edit && !cand) {
+      const float p = nan_to(__ldcg(a.conf + base + l), -__int_as_float(0x7F800000));
+      edit = (x0 != tok) && (p > a.tau_edit);
+    }
+    if (a.commit) a.commit[base + l] = commit ? 1 : 0;
+    if (a.edit_mask) a.edit_mask[base + l] = edit ? 1 : 0;
+    if ((commit || edit) && a.canvas && a.x0) a.canvas[b * a.canvas_stride + a.canvas_offset + l] = x0;
+    n_commit += commit ? 1 : 0;
+    n_edit += edit ? 1 : 0;
+  }
+  (void)n_commit_forced;
+  if (a.counts) {
+    const int4 t = rule_sum4<NT, BAR>(make_int4(n_commit, n_edit, 0, 0), s, tid);
+    if (tid == 0) {
+      a.counts[3 * b + 0] = n_cand_total;
+      a.counts[3 * b + 1] = t.x;
+      a.counts[3 * b + 2] = t.y;
+    }
+  }
+  rsync<NT, BAR>();
+}
+
+}  // namespace dllm

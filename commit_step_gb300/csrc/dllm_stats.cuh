@@ -1,0 +1,58 @@
+// dllm_stats.cuh -- parameters shared by the statistics kernel and its host
+// launcher.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/dllmcommit.h"
+#include "dllm_gumbel.cuh"
+#include "dllm_rules.cuh"
+
+namespace dllm {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;  // threads that reduce the logits
+constexpr int kThreads = kConsumers + 32;        // plus one warp that issues the bulk copies
+constexpr int kMaxStages = 16;
+constexpr int kRingBytes = 64 * 1024;
+constexpr int kFusedSortCap = 1024;              // largest L the fused sorting rules take
+constexpr int kMaxCtasPerSm = 4;
+
+// Partial reduction of one row segment: max m, Z = sum 2^y and S2 = sum 2^y y
+// with y = (z - m) log2(e), the first index of m, and the best Gumbel score
+// with its id and logit.
+struct alignas(16) Partial {
+  float m, Z, S2;
+  int32_t idx;
+  float best_s, best_z;
+  int32_t best_v;
+  int32_t pad;
+};
+
+struct StatsParams {
+  const uint8_t* logits;
+  int64_t row_bytes;        // row stride in bytes (multiple of 16)
+  int64_t T, V, L;
+  int64_t nvec;             // full 16-byte vectors per row
+  int32_t tail;             // elements after the last full vector
+  int32_t chunk_vec;        // vectors per unit (256, 512 or 1024)
+  int64_t K, U;             // units per row, units in all
+  int32_t P;                // CTAs in the grid
+  int32_t stages;           // ring stages
+  float temperature;
+  PhiloxKey key;
+  int32_t n_sup;
+  int32_t sup[DLLM_MAX_SUPPRESS];  // sorted, distinct
+  float ln_veff;
+  int32_t* x0;
+  float* prob;
+  float* entropy;
+  int32_t* fault;
+  int32_t* row_count;       // (T) contributions that arrived, split rows only
+  int32_t* batch_count;     // (B) rows finished, fused rule only
+  Partial* partials;        // (2 P)
+  int32_t fused;
+  RuleArgs rule;
+};
+
+}  // namespace dllm

@@ -18,3 +18,18 @@ def golden():
 
     with open(os.path.join(ROOT, "tests", "golden", "worked_examples.json")) as f:
         return json.load(f)
+
+
+@pytest.fixture(scope="session")
+def cs():
+    """The built library (GPU tests only)."""
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import commit_step_gb300
+
+    return commit_step_gb300

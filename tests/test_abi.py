@@ -1,0 +1,82 @@
+"""The C-ABI library loads and exports every function include/dllmcommit.h
+declares; host-only entry points agree with the oracle.  CPU only (no kernel
+is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HDR = os.path.join(ROOT, "include", "dllmcommit.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location("_b", os.path.join(ROOT, "commit_step_gb300", "build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    path = b.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HDR).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dllm_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_and_version(lib):
+    lib.dllm_status_string.restype = ctypes.c_char_p
+    lib.dllm_version.restype = ctypes.c_char_p
+    assert lib.dllm_status_string(0) == b"DLLM_OK"
+    assert b"INVALID" in lib.dllm_status_string(1)
+    assert b"sm_103a" in lib.dllm_version()
+
+
+def _ranges(lib, P, gen, bl, align):
+    n = ctypes.c_int64(0)
+    lib.dllm_block_ranges.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                                                             ctypes.c_void_p]
+    st = lib.dllm_block_ranges(P, gen, bl, align, None, 0, ctypes.byref(n))
+    assert st in (0, 3)
+    buf = (ctypes.c_int64 * max(1, 2 * n.value))()
+    assert lib.dllm_block_ranges(P, gen, bl, align, buf, n.value, ctypes.byref(n)) == 0
+    return [(buf[2 * i], buf[2 * i + 1]) for i in range(n.value)]
+
+
+def test_block_ranges_matches_oracle(lib):
+    import numpy as np
+
+    rng = np.random.default_rng(41)
+    for _ in range(500):
+        P, gen, bl = int(rng.integers(0, 400)), int(rng.integers(0, 700)), int(rng.integers(1, 90))
+        for align in (0, 1):
+            assert _ranges(lib, P, gen, bl, align) == oracle.block_ranges(P, gen, bl, bool(align))
+
+
+def test_block_ranges_errors(lib):
+    n = ctypes.c_int64(0)
+    assert lib.dllm_block_ranges(5, 10, 0, 0, None, 0, ctypes.byref(n)) == 1     # block_len <= 0
+    assert lib.dllm_block_ranges(-1, 10, 4, 0, None, 0, ctypes.byref(n)) == 1    # P < 0
+    assert lib.dllm_block_ranges(5, 10, 4, 0, None, 0, None) == 1                # no n_out
+    assert lib.dllm_block_ranges(5, 10, 4, 0, None, 0, ctypes.byref(n)) == 3 and n.value == 3
+
+
+def test_workspace_size_without_device(lib):
+    lib.dllm_token_stats_workspace_size.restype = ctypes.c_size_t
+    lib.dllm_token_stats_workspace_size.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int]
+    a = lib.dllm_token_stats_workspace_size(1, 32, 126464, 1)
+    b = lib.dllm_token_stats_workspace_size(32, 512, 126464, 0)
+    assert 0 < a < b < (1 << 24)

@@ -1,0 +1,171 @@
+"""GPU parity of the fused commit step (statistics + rule + canvas update in
+one launch) against the oracle, on the five workloads: small cases in full,
+and the full-size workloads in the bench's launch configuration on sampled
+rows (plus properties that hold at any size)."""
+import numpy as np
+import pytest
+import torch
+
+import dllm_workloads as W
+import oracle
+from gpu_helpers import TOL, assert_stats_close, mask_mismatch_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+RULES = {"threshold": 1, "topk": 2, "factor": 3, "entropy_bound": 4}
+
+
+def fused(cs, w, logits_dev, rule, **kw):
+    cand = torch.from_numpy(w.candidates).cuda()
+    return cs.commit_step(logits_dev.view(w.B, w.L, w.V), rule=RULES[rule], temperature=w.temperature, key=w.key,
+                          suppress_ids=w.suppress_ids, cand=cand, **kw)
+
+
+def check_full(cs, w, rule, params, **kw):
+    dev = to_device(w.logits, w.dtype)
+    x0, prob, ent, commit, _ = fused(cs, w, dev, rule, **kw)
+    torch.cuda.synchronize()
+    ox0, op, oe = oracle.token_stats(w.logits, dtype=w.dtype, temperature=w.temperature, key=w.key,
+                                     suppress_ids=w.suppress_ids)
+    assert np.array_equal(x0.cpu().numpy().reshape(-1), ox0)
+    assert_stats_close(w.dtype, prob.cpu().numpy(), ent.cpu().numpy(), op, oe, w.name)
+    scores = (oe if rule == "entropy_bound" else op).reshape(w.B, w.L)
+    got = commit.cpu().numpy()
+    bad, amb = mask_mismatch_rows(rule, got, w.candidates, scores, params, w.dtype)
+    assert not bad, f"{w.name}/{rule}: commit masks differ in batch rows {bad}"
+    assert len(amb) <= max(1, w.B // 10)
+    return got
+
+
+def test_tiny_threshold(cs):
+    w = W.tiny()
+    got = check_full(cs, w, "threshold", w.params, tau=0.9, strict=False)
+    assert got.sum() >= 1
+
+
+def test_llada_threshold_strict(cs):
+    w = W.llada()
+    got = check_full(cs, w, "threshold", w.params, tau=0.95, strict=True)
+    assert 1 <= got.sum() <= 19 and np.all(got <= w.candidates)
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_small_rules_all_kinds(cs, seed):
+    """Every rule on a reduced LLaDA-like shape (B=3, L=40, V=3000, ragged)."""
+    rng = np.random.default_rng(seed)
+    B, L, V = 3, 40, 3000
+    z = (rng.standard_normal((B * L, V)) * 2).astype(np.float32)
+    for r in range(B * L):
+        z[r, rng.integers(0, V)] += rng.uniform(0, 14)
+    cand = (rng.random((B, L)) < 0.6).astype(np.uint8)
+    w = W.Workload("small", B, L, V, "f32", z, None, [7], 0.0, 0, "", cand, {})
+    k = np.array([3, 0, 50], dtype=np.int32)
+    check_full(cs, w, "threshold", {"tau": 0.6, "strict": False}, tau=0.6)
+    check_full(cs, w, "topk", {"k": k}, k=torch.from_numpy(k).cuda())
+    check_full(cs, w, "factor", {"factor": 1.0}, factor=1.0)
+    check_full(cs, w, "entropy_bound", {"gamma": 0.3}, gamma=0.3)
+
+
+def test_fused_canvas_candidates_edit_counts(cs):
+    """Candidates from the canvas (token == mask id), edit rule, canvas update
+    and per-row counts, as the block-decode loop uses them."""
+    rng = np.random.default_rng(3)
+    B, L, V, N, off, MASK = 2, 32, 2048, 96, 40, 2047
+    z = (rng.standard_normal((B * L, V))).astype(np.float32)
+    tgt = rng.integers(0, 2000, (B, L))
+    for b in range(B):
+        for l in range(L):
+            z[b * L + l, tgt[b, l]] += 18.0 if l % 3 else 5.0
+    canvas0 = rng.integers(0, 2000, (B, N)).astype(np.int32)
+    masked = rng.random((B, L)) < 0.5
+    canvas0[:, off:off + L][masked] = MASK
+    canvas = torch.from_numpy(canvas0.copy()).cuda()
+    counts = torch.zeros((B, 3), dtype=torch.int32, device="cuda")
+    dev = torch.from_numpy(z).cuda().view(B, L, V)
+    x0, prob, ent, commit, edit = cs.commit_step(dev, rule=1, tau=0.95, strict=True, suppress_ids=[MASK],
+                                                 mask_id=MASK, edit=True, tau_edit=0.9, canvas=canvas,
+                                                 canvas_offset=off, counts=counts)
+    ox0, op, _ = oracle.token_stats(z, suppress_ids=[MASK])
+    assert np.array_equal(x0.cpu().numpy().reshape(-1), ox0)
+    p32 = op.astype(np.float32).reshape(B, L)
+    window = canvas0[:, off:off + L]
+    want_c = oracle.threshold_transfer(p32, masked.astype(np.uint8), 0.95, True)
+    want_e = oracle.edit_transfer(ox0.reshape(B, L), p32, window, (~masked).astype(np.uint8), 0.9)
+    assert np.array_equal(commit.cpu().numpy(), want_c)
+    assert np.array_equal(edit.cpu().numpy(), want_e)
+    exp = canvas0.copy()
+    exp[:, off:off + L] = np.where((want_c | want_e).astype(bool), ox0.reshape(B, L), window)
+    assert np.array_equal(canvas.cpu().numpy(), exp)
+    assert counts.cpu().numpy().tolist() == [[int(masked[b].sum()), int(want_c[b].sum()), int(want_e[b].sum())]
+                                             for b in range(B)]
+
+
+def test_repeated_fused_calls_leave_workspace_clean(cs):
+    w = W.tiny()
+    dev = to_device(w.logits, w.dtype)
+    first = None
+    for _ in range(5):
+        x0, prob, ent, commit, _ = fused(cs, w, dev, "threshold", tau=0.9)
+        cur = (x0.cpu().numpy(), commit.cpu().numpy())
+        if first is None:
+            first = cur
+        assert np.array_equal(cur[0], first[0]) and np.array_equal(cur[1], first[1])
+
+
+# ---------------- full-size workloads, bench launch configuration ----------------
+
+def sampled_rows_check(w, x0, prob, ent, rows):
+    s = W.build(w.name, rows=rows)
+    ox0, op, oe = oracle.token_stats(s.logits, dtype=w.dtype, temperature=w.temperature, key=w.key,
+                                     suppress_ids=w.suppress_ids, row_ids=rows)
+    gx0 = x0.reshape(-1)[rows]
+    assert np.array_equal(gx0, ox0), f"{w.name}: x0 differs on sampled rows"
+    assert_stats_close(w.dtype, prob.reshape(-1)[rows], ent.reshape(-1)[rows], op, oe, w.name)
+
+
+def invariants(w, x0, prob, ent, commit):
+    veff = w.V - len(set(w.suppress_ids))
+    assert np.all(prob > 0) and np.all(prob <= 1 + 1e-6)
+    assert np.all(ent >= 0) and np.all(ent <= np.log(veff) + 1e-4)
+    assert not np.isin(x0, w.suppress_ids).any()
+    assert np.all(commit <= w.candidates)
+
+
+def test_full_dream_topk(cs):
+    w = W.dream()
+    dev = to_device(w.logits, w.dtype)
+    k = torch.full((w.B,), 8, dtype=torch.int32, device="cuda")
+    x0, prob, ent, commit, _ = fused(cs, w, dev, "topk", k=k)
+    x0, prob, ent, commit = (t.cpu().numpy() for t in (x0, prob, ent, commit))
+    invariants(w, x0, prob, ent, commit)
+    assert np.all(commit.sum(axis=1) == 8)
+    rows = np.random.default_rng(0).choice(w.T, 48, replace=False)
+    sampled_rows_check(w, x0, prob, ent, np.sort(rows))
+    # one whole batch row through the oracle rule
+    b = 3
+    s = W.build("dream", rows=np.arange(b * w.L, (b + 1) * w.L))
+    _, op, _ = oracle.token_stats(s.logits, dtype="bf16", temperature=w.temperature, key=w.key,
+                                  row_ids=np.arange(b * w.L, (b + 1) * w.L))
+    bad, _ = mask_mismatch_rows("topk", commit[b:b + 1], w.candidates[b:b + 1], op[None], {"k": 8}, "bf16")
+    assert not bad
+
+
+def test_full_large_factor_and_entropy_bound(cs):
+    w = W.large()
+    dev = to_device(w.logits, w.dtype)
+    x0, prob, ent, commit, _ = fused(cs, w, dev, "factor", factor=1.0)
+    cand = torch.from_numpy(w.candidates).cuda()
+    eb = cs.entropy_bound_transfer(ent, cand, 0.1).cpu().numpy()
+    x0, prob, ent, commit = (t.cpu().numpy() for t in (x0, prob, ent, commit))
+    invariants(w, x0, prob, ent, commit)
+    assert np.all(commit.sum(axis=1) >= 1) and np.all(eb.sum(axis=1) >= 1) and np.all(eb <= w.candidates)
+    rows = np.sort(np.random.default_rng(1).choice(w.T, 32, replace=False))
+    sampled_rows_check(w, x0, prob, ent, rows)
+    b = 17
+    idx = np.arange(b * w.L, (b + 1) * w.L)
+    s = W.build("large", rows=idx)
+    _, op, oe = oracle.token_stats(s.logits, suppress_ids=w.suppress_ids)
+    bad, _ = mask_mismatch_rows("factor", commit[b:b + 1], w.candidates[b:b + 1], op[None], {"factor": 1.0}, "f32")
+    assert not bad
+    bad, _ = mask_mismatch_rows("entropy_bound", eb[b:b + 1], w.candidates[b:b + 1], oe[None], {"gamma": 0.1}, "f32")
+    assert not bad

@@ -32,7 +32,7 @@ EXPORTS = (
     "dllm_status_string", "dllm_version", "dllm_token_stats_workspace_size", "dllm_token_stats",
     "dllm_threshold_transfer", "dllm_topk_transfer", "dllm_factor_transfer", "dllm_entropy_bound_transfer",
     "dllm_edit_transfer", "dllm_transfer_schedule", "dllm_block_ranges", "dllm_commit_step",
-    "dllm_workspace_fault",
+    "dllm_workspace_fault", "dllm_token_stats_noalloc",
 )
 
 
@@ -76,6 +76,7 @@ def _load() -> C.CDLL:
     lib.dllm_transfer_schedule.argtypes = [P, i64, i32, P, P]
     lib.dllm_block_ranges.argtypes = [i64, i64, i64, C.c_int, P, i64, P]
     lib.dllm_workspace_fault.argtypes = [P, P, C.POINTER(C.c_int32)]
+    lib.dllm_token_stats_noalloc.argtypes = stats_args + [P]
     for name in EXPORTS[3:]:
         if name != "dllm_token_stats_workspace_size":
             getattr(lib, name).restype = C.c_int
@@ -313,6 +314,26 @@ def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, su
                                  sup, len(suppress_ids), _ptr(x0), _ptr(prob), _ptr(ent), C.byref(p), _ptr(ws),
                                  ws.numel(), _stream(stream)), "dllm_commit_step")
     return x0, prob, ent, commit, edit_mask
+
+
+def token_stats_noalloc(logits: torch.Tensor, temperature: float = 0.0, key: int = 0,
+                        suppress_ids: Sequence[int] = (), out=None, stream=None):
+    """token_stats without a workspace: the library's fixed scratch array is
+    used instead (see dllm_token_stats_noalloc); calls must not overlap."""
+    _need_cuda(logits)
+    B, L, V, stride = _logits_view(logits)
+    dt = _dtype_code(logits)
+    shape = logits.shape[:-1]
+    if out is None:
+        out = (torch.empty(shape, dtype=torch.int32, device=logits.device),
+               torch.empty(shape, dtype=torch.float32, device=logits.device),
+               torch.empty(shape, dtype=torch.float32, device=logits.device))
+    x0, prob, ent = out
+    sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
+    _check(_lib.dllm_token_stats_noalloc(_ptr(logits), dt, B, L, V, stride, float(temperature),
+                                         int(key) & (2**64 - 1), sup, len(suppress_ids), _ptr(x0), _ptr(prob),
+                                         _ptr(ent), _stream(stream)), "dllm_token_stats_noalloc")
+    return x0, prob, ent
 
 
 def workspace_fault(ws: torch.Tensor, stream=None) -> int:

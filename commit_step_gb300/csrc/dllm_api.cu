@@ -250,6 +250,36 @@ dllm_status rule_entry(int32_t kind, const float* conf, const uint8_t* cand, int
   return run_rule_kernel(a, B, L, s);
 }
 
+// Scratch of dllm_token_stats_noalloc: one fixed array per GPU that loads the
+// library.  Host code must not use `g_noalloc_scratch` as an address (it is a
+// host-side stand-in); the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[DLLM_NOALLOC_SCRATCH_BYTES];
+
+struct NoallocSlot {
+  void* ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+NoallocSlot g_noalloc[kMaxDevices];
+std::once_flag g_noalloc_once[kMaxDevices];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current).
+void* noalloc_scratch(cudaError_t* err) {
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::call_once(g_noalloc_once[dev], [dev]() {
+    void* p = nullptr;
+    g_noalloc[dev].err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    g_noalloc[dev].ptr = g_noalloc[dev].err == cudaSuccess ? p : nullptr;
+  });
+  *err = g_noalloc[dev].err;
+  return g_noalloc[dev].ptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -411,6 +441,29 @@ dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64
   a.L = L;
   return run_stats(logits, dt, B, L, V, row_stride, temperature, key, sup, x0, prob, entropy, &a, workspace,
                    workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dllm_status dllm_token_stats_noalloc(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,
+                                     int64_t row_stride, float temperature, uint64_t key, const int32_t* suppress_ids,
+                                     int32_t n_suppress, int32_t* x0, float* prob, float* entropy,
+                                     dllm_stream_t stream) {
+  std::vector<int32_t> sup;
+  dllm_status st = check_stats(logits, dt, B, L, V, row_stride, temperature, suppress_ids, n_suppress, x0, prob,
+                               entropy, sup);
+  if (st != DLLM_OK || B * L == 0) return st;
+  const DeviceInfo* d = device_info();
+  if (!d) return DLLM_ERR_CUDA;
+  const size_t need = ws_layout(B, L, d->sms).total;
+  if (need > DLLM_NOALLOC_SCRATCH_BYTES) return DLLM_ERR_UNSUPPORTED;  // shape too large for the fixed scratch
+  cudaError_t err = cudaSuccess;
+  void* scratch = noalloc_scratch(&err);
+  if (!scratch) return DLLM_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: clear the fault word and
+  // the counters this call relies on starting at zero.
+  if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) return DLLM_ERR_CUDA;
+  return run_stats(logits, dt, B, L, V, row_stride, temperature, key, sup, x0, prob, entropy, nullptr, scratch,
+                   DLLM_NOALLOC_SCRATCH_BYTES, s);
 }
 
 dllm_status dllm_workspace_fault(void* workspace, dllm_stream_t stream, int32_t* fault) {

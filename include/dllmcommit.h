@@ -98,6 +98,40 @@ dllm_status dllm_token_stats(const void* logits, dllm_dtype dt, int64_t B, int64
                              void* workspace, size_t workspace_bytes, dllm_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Statistics pass that allocates nothing.  The pages have no counterpart:
+ * this entry point is an addition of this library.
+ *
+ * For callers that may not allocate device memory at all: code whose memory
+ * is wholly owned by another allocator (a framework's caching pool, where a
+ * cudaMalloc outside the pool can fail or fragment it), inference-server and
+ * plugin hosts that hand a kernel only its input and output buffers, and
+ * latency-critical loops that forbid allocation after warm-up because
+ * cudaMalloc and cudaFree synchronise the device.
+ *
+ * Arguments, results and errors are those of dllm_token_stats without the
+ * workspace.  The scratch memory is one fixed device array inside the
+ * library, DLLM_NOALLOC_SCRATCH_BYTES per GPU, held by every GPU that loads
+ * the library until the process exits.  A shape whose scratch does not fit
+ * (about (B*L + B) * 4 bytes plus a fixed part, so B*L up to roughly 250,000
+ * rows) returns DLLM_ERR_UNSUPPORTED without launching anything.
+ *   - The first call on each device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call first clears the part of the array it uses
+ *     (cudaMemsetAsync on the stream), then launches the kernel; nothing is
+ *     allocated or freed.
+ *   - All calls share the one array and it keeps the last call's contents:
+ *     calls that can overlap on the GPU (other streams, other host threads)
+ *     race with each other and give wrong results.  Serialise them.
+ * ------------------------------------------------------------------------ */
+#define DLLM_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+dllm_status dllm_token_stats_noalloc(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,
+                                     int64_t row_stride, float temperature, uint64_t key,
+                                     const int32_t* suppress_ids, int32_t n_suppress,
+                                     int32_t* x0, float* prob, float* entropy, dllm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Commit rules.  One batch row b of L positions; cand (device, (B, L)) marks
  * the masked candidates; commit (device, (B, L)) is written for every
  * position (0 for non-candidates).  Ranking: higher confidence first (NaN

@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="eager steps only (no graph, e2e or CPU leg): the command the ncu captures use")
     return ap.parse_args()
 
 
@@ -269,9 +271,13 @@ def run_ours(args, rank, world):
                            cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws)
             cs.entropy_bound_transfer(ent, cand, w.params["gamma"], commit=commit2)
 
-    # correctness guard on the very inputs being timed (cheap, sampled rows)
     step(0)
     torch.cuda.synchronize()
+    if args.profile:
+        for i in range(warmup + steps):
+            step(i)
+        torch.cuda.synchronize()
+        return {"profile": w.name, "steps": warmup + steps, "workspace_fault": cs.workspace_fault(ws)}, w
 
     # graph of G steps over the rotating buffers
     G = R if R > 1 else min(50, steps)
@@ -436,7 +442,7 @@ def main():
         dist.init_process_group("nccl")
     res, w = run_ours(args, rank, world)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and not args.profile:
             res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
         print(json.dumps(res))
     if world > 1:

@@ -27,6 +27,7 @@ RULE_NONE, RULE_THRESHOLD, RULE_TOPK, RULE_FACTOR, RULE_ENTROPY_BOUND = 0, 1, 2,
 MAX_SUPPRESS = 64
 MAX_SORT_L = 16384
 FUSED_SORT_CAP = 1024
+FLAG_INPUTS_READY = 1
 
 EXPORTS = (
     "dllm_status_string", "dllm_version", "dllm_token_stats_workspace_size", "dllm_token_stats",
@@ -50,7 +51,7 @@ class CommitParams(C.Structure):
         ("gamma", C.c_float), ("k", C.c_void_p), ("cand", C.c_void_p), ("mask_id", C.c_int32),
         ("edit", C.c_int32), ("tau_edit", C.c_float), ("commit", C.c_void_p), ("edit_mask", C.c_void_p),
         ("canvas", C.c_void_p), ("canvas_stride", C.c_int64), ("canvas_offset", C.c_int64),
-        ("counts", C.c_void_p),
+        ("counts", C.c_void_p), ("flags", C.c_int32),
     ]
 
 
@@ -274,8 +275,11 @@ def block_ranges(P: int, gen_len: int, block_len: int, align: bool = False):
 def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, suppress_ids: Sequence[int] = (),
                 cand=None, mask_id: int = -1, tau: float = 0.0, strict: bool = False, k=None, factor: float = 0.0,
                 gamma: float = 0.0, edit: bool = False, tau_edit: float = 1.0, canvas=None, canvas_offset: int = 0,
-                out=None, counts=None, ws=None, stream=None):
+                out=None, counts=None, ws=None, stream=None, inputs_ready: bool = False):
     """Fused statistics pass + commit rule (+ edit rule and canvas update) in one launch.
+
+    ``inputs_ready`` sets DLLM_FLAG_INPUTS_READY: only when the logits were not
+    written by the kernel that precedes this call in the stream.
 
     Returns (x0, prob, entropy, commit, edit_mask); commit/edit_mask are None
     when not requested.
@@ -307,6 +311,7 @@ def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, su
             raise ValueError("canvas must be a (B, N) int32 tensor with unit column stride")
         p.canvas, p.canvas_stride, p.canvas_offset = canvas.data_ptr(), canvas.stride(0), int(canvas_offset)
     p.counts = None if counts is None else counts.data_ptr()
+    p.flags = FLAG_INPUTS_READY if inputs_ready else 0
     sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
     if ws is None:
         ws = workspace(B, L, V, dt, dev, stream)

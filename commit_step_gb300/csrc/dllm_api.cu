@@ -14,6 +14,7 @@
 
 namespace dllm {
 const void* stats_kernel_ptr(bool bf16, bool gumbel);
+const void* stats_cluster_kernel_ptr(bool bf16, bool gumbel);
 const void* rules_kernel_ptr(int nt);
 const void* edit_kernel_ptr();
 const void* schedule_kernel_ptr();
@@ -29,6 +30,7 @@ constexpr size_t kStatsSmemMax = static_cast<size_t>(kRingBytes) + kFusedSortCap
 struct DeviceInfo {
   int sms = 0;
   int occ[4] = {0, 0, 0, 0};  // CTAs per SM of stats_kernel<bf16, gumbel>, index 2*bf16+gumbel
+  int clusters[4][5] = {};    // co-resident clusters of stats_cluster_kernel per cluster size 1,2,4,8,16
   cudaError_t err = cudaSuccess;
 };
 
@@ -49,6 +51,31 @@ const DeviceInfo* device_info() {
       d.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kThreads, kStatsSmemMax);
       d.occ[v] = std::max(1, std::min(n, kMaxCtasPerSm));
     }
+    for (int v = 0; v < 4 && d.err == cudaSuccess; ++v) {
+      const void* k = stats_cluster_kernel_ptr(v >= 2, (v & 1) != 0);
+      d.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmemMax));
+      if (d.err == cudaSuccess) d.err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      for (int e = 0; e < 5 && d.err == cudaSuccess; ++e) {
+        const int S = 1 << e;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(S * 64);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kStatsSmemMax;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+          (void)cudaGetLastError();  // an unsupported size only rules that size out
+          n = 0;
+        }
+        d.clusters[v][e] = n;
+      }
+    }
     for (int nt : {128, 256, 512, 1024}) {
       if (d.err != cudaSuccess) break;
       d.err = cudaFuncSetAttribute(rules_kernel_ptr(nt), cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -62,7 +89,8 @@ const DeviceInfo* device_info() {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t fault = 0, row_count = 0, batch_count = 0, partials = 0, total = 0;
+  size_t fault = 0, partials = 0, row_count = 0, batch_count = 0, batch_cand = 0, batch_commit = 0, batch_edit = 0,
+         batch_forced = 0, total = 0;
 };
 
 // Fault word, then the partials (a size fixed per device), then the counters.
@@ -74,43 +102,77 @@ WsLayout ws_layout(int64_t B, int64_t L, int sms) {
   w.fault = 0;
   w.partials = 256;
   w.row_count = w.partials + static_cast<size_t>(2) * sms * kMaxCtasPerSm * sizeof(Partial);
-  w.batch_count = w.row_count + static_cast<size_t>(B * L) * 4;
-  w.total = align_up(w.batch_count + static_cast<size_t>(B) * 4, 256);
+  w.batch_forced = align_up(w.row_count + static_cast<size_t>(B * L) * 4, 8);
+  w.batch_count = w.batch_forced + static_cast<size_t>(B) * 8;
+  w.batch_cand = w.batch_count + static_cast<size_t>(B) * 4;
+  w.batch_commit = w.batch_cand + static_cast<size_t>(B) * 4;
+  w.batch_edit = w.batch_commit + static_cast<size_t>(B) * 4;
+  w.total = align_up(w.batch_edit + static_cast<size_t>(B) * 4, 256);
   return w;
 }
 
 struct StatsPlan {
   int64_t nvec, K, U;
-  int32_t tail, chunk_vec, P, stages;
+  int32_t tail, chunk_vec, P, stages, cluster;
 };
 
-StatsPlan plan_stats(int64_t T, int64_t V, int esize, int ctas) {
+int chunk_for(int64_t vectors_per_cta) {
+  int chunk = 1024;
+  while (chunk > 256 && static_cast<int64_t>(4) * chunk > vectors_per_cta) chunk >>= 1;
+  return chunk;
+}
+
+// Few rows: one cluster of S CTAs per row, the largest S whose whole grid is
+// co-resident (one wave) and leaves each CTA at least 128 vectors.  Many
+// rows: the persistent grid over equal unit ranges.
+StatsPlan plan_stats(const DeviceInfo& d, int variant, int64_t T, int64_t V, int esize) {
   StatsPlan pl{};
   pl.nvec = (V * esize) / 16;
   pl.tail = static_cast<int32_t>(V - pl.nvec * (16 / esize));
+  const int ctas = d.sms * d.occ[variant];
+  for (int e = 4; e >= 1; --e) {
+    const int S = 1 << e;
+    if (T <= d.clusters[variant][e] && T * S <= ctas && pl.nvec >= static_cast<int64_t>(S) * 128) {
+      pl.cluster = S;
+      // slices are equal by construction: favour few, large copies
+      const int64_t slice = pl.nvec / S;
+      pl.chunk_vec = slice >= 2048 ? 1024 : (slice >= 1024 ? 512 : 256);
+      pl.stages = std::min(kMaxStages, kRingBytes / (pl.chunk_vec * 16));
+      pl.P = static_cast<int32_t>(T * S);
+      pl.K = 0;
+      pl.U = 0;
+      return pl;
+    }
+  }
   const int64_t total_vec = T * std::max<int64_t>(pl.nvec, 1);
-  const int64_t per_cta = total_vec / std::max(ctas, 1);
-  int chunk = 1024;
-  while (chunk > 256 && static_cast<int64_t>(4) * chunk > per_cta) chunk >>= 1;
-  pl.chunk_vec = chunk;
-  pl.stages = std::min(kMaxStages, kRingBytes / (chunk * 16));
-  pl.K = pl.nvec > 0 ? (pl.nvec + chunk - 1) / chunk : 1;
+  pl.cluster = 0;
+  pl.chunk_vec = chunk_for(total_vec / std::max(ctas, 1));
+  pl.stages = std::min(kMaxStages, kRingBytes / (pl.chunk_vec * 16));
+  pl.K = pl.nvec > 0 ? (pl.nvec + pl.chunk_vec - 1) / pl.chunk_vec : 1;
   pl.U = T * pl.K;
   pl.P = static_cast<int32_t>(std::min<int64_t>(pl.U, ctas));
   return pl;
 }
 
-dllm_status launch(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
+dllm_status launch(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
+                   int cluster = 0) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attr;
   return cudaLaunchKernelExC(&cfg, kernel, args) == cudaSuccess ? DLLM_OK : DLLM_ERR_CUDA;
 }
 
@@ -140,7 +202,8 @@ dllm_status check_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L,
 
 dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
                       float temperature, uint64_t key, const std::vector<int32_t>& sup, int32_t* x0, float* prob,
-                      float* entropy, const RuleArgs* rule, void* ws, size_t ws_bytes, cudaStream_t s) {
+                      float* entropy, const RuleArgs* rule, void* ws, size_t ws_bytes, cudaStream_t s,
+                      bool early = false) {
   const DeviceInfo* d = device_info();
   if (!d) return DLLM_ERR_CUDA;
   const bool bf16 = dt == DLLM_BF16, gumbel = temperature > 0.0f;
@@ -149,11 +212,13 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   const WsLayout lay = ws_layout(B, L, d->sms);
   if (!ws || ws_bytes < lay.total) return DLLM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0) return DLLM_ERR_INVALID_ARGUMENT;
-  const int occ = d->occ[(bf16 ? 2 : 0) + (gumbel ? 1 : 0)];
-  const StatsPlan pl = plan_stats(T, V, es, d->sms * occ);
+  const int variant = (bf16 ? 2 : 0) + (gumbel ? 1 : 0);
+  const StatsPlan pl = plan_stats(*d, variant, T, V, es);
 
   StatsParams p{};
   p.logits = static_cast<const uint8_t*>(logits);
+  p.cluster = pl.cluster;
+  p.early = early ? 1 : 0;
   p.row_bytes = row_stride * es;
   p.T = T;
   p.V = V;
@@ -178,11 +243,17 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   p.fault = reinterpret_cast<int32_t*>(w + lay.fault);
   p.row_count = reinterpret_cast<int32_t*>(w + lay.row_count);
   p.batch_count = reinterpret_cast<int32_t*>(w + lay.batch_count);
+  p.batch_cand = reinterpret_cast<int32_t*>(w + lay.batch_cand);
+  p.batch_commit = reinterpret_cast<int32_t*>(w + lay.batch_commit);
+  p.batch_edit = reinterpret_cast<int32_t*>(w + lay.batch_edit);
+  p.batch_forced = reinterpret_cast<unsigned long long*>(w + lay.batch_forced);
   p.partials = reinterpret_cast<Partial*>(w + lay.partials);
   p.fused = rule ? 1 : 0;
   if (rule) p.rule = *rule;
   const size_t smem = static_cast<size_t>(pl.stages) * pl.chunk_vec * 16 + (rule ? kFusedSortCap * 9 : 0);
   void* args[] = {&p};
+  if (pl.cluster > 0)
+    return launch(stats_cluster_kernel_ptr(bf16, gumbel), dim3(pl.P), dim3(kThreads), smem, s, args, pl.cluster);
   return launch(stats_kernel_ptr(bf16, gumbel), dim3(pl.P), dim3(kThreads), smem, s, args);
 }
 
@@ -439,8 +510,9 @@ dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64
   a.canvas_offset = cp->canvas_offset;
   a.counts = cp->counts;
   a.L = L;
+  if (cp->flags & ~static_cast<int32_t>(DLLM_FLAG_INPUTS_READY)) return DLLM_ERR_INVALID_ARGUMENT;
   return run_stats(logits, dt, B, L, V, row_stride, temperature, key, sup, x0, prob, entropy, &a, workspace,
-                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream), (cp->flags & DLLM_FLAG_INPUTS_READY) != 0);
 }
 
 dllm_status dllm_token_stats_noalloc(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,

@@ -16,9 +16,11 @@ enum : int32_t {
   kFaultDrainWait = 3,  // the final drain of in-flight copies gave up
 };
 
-// A bulk-copy wait that has not completed after this long is treated as a
-// fault: the kernel records it and stops instead of spinning forever.
-constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// A bulk-copy wait that has not completed after this many SM clock cycles
+// (about 1 s at 2 GHz) is treated as a fault: the kernel records it and stops
+// instead of waiting forever.  The SM-local cycle counter is cheap to read,
+// unlike the global timer.
+constexpr long long kWaitLimitCycles = 2000ll * 1000ll * 1000ll;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -59,15 +61,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread sleeps in hardware until the phase
+// completes or about `hint_ns` pass, instead of spinning and taking issue
+// slots from the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kSleepHintNs = 20000;  // one hardware sleep before the deadline is checked again
+
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs and returns false; the caller records the fault and stops.
+// kWaitLimitCycles and returns false; the caller records the fault and stops.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
 

@@ -5,13 +5,11 @@
 // every logit row, the proposal x0 (first argmax, or Gumbel-max), its
 // probability and the entropy of the softmax over the non-suppressed ids.
 //
-// How (one pass over HBM, persistent grid):
-//   * The T rows are cut into units of chunk_vec 16-byte vectors; the U units
-//     are dealt to the P CTAs in contiguous, equal ranges, so every CTA reads
-//     the same number of bytes whatever the shape (few long rows or many).
-//   * In each CTA one producer thread streams its units into a shared-memory
-//     ring with cp.async.bulk (TMA bulk copies), one mbarrier per stage; eight
-//     consumer warps read each unit from shared memory.
+// How (one pass over HBM):
+//   * Rows are cut into units of chunk_vec 16-byte vectors.  In each CTA one
+//     producer thread streams its units into a shared-memory ring with
+//     cp.async.bulk (TMA bulk copies), one mbarrier per stage; eight consumer
+//     warps read each unit from shared memory.
 //   * Each consumer thread keeps an online softmax state: running max m,
 //     Z = sum 2^y and S2 = sum 2^y y with y = (z - m) log2 e (packed fp32x2
 //     accumulators), rescaled when the max grows; entropy = ln Z - S2 ln 2 / Z.
@@ -19,9 +17,17 @@
 //   * Gumbel-max: one Philox4x32-10 call per four ids; a bound on the noise
 //     from the largest uniform of each 16-byte vector lets most vectors skip
 //     the two logarithms; the warp shares its best score to tighten the bound.
-//   * A row that spans CTAs is combined by whichever CTA contributes last
-//     (atomic arrival count, no waiting); in the fused commit step the CTA that
-//     finishes the last row of a batch row then runs that row's commit rule.
+//   * Many rows (persistent kernel): the units are dealt to the CTAs in equal
+//     contiguous ranges; a row shared by several CTAs is combined by the one
+//     that contributes last (atomic arrival count, no waiting), its warp 0
+//     loading the partials in parallel.
+//   * Few rows (cluster kernel): one thread-block cluster per row, each CTA a
+//     contiguous slice; the CTAs' partials are combined through distributed
+//     shared memory by rank 0.
+//   * Fused commit step: the thread that finalizes a row also makes the row's
+//     threshold / edit decision and canvas update; the last row of a batch row
+//     applies the forced commit when nothing passed (or, for the sorting rules,
+//     its CTA runs the whole rule).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -35,7 +41,10 @@ struct Acc {
   uint64_t Z2;      // two partial sums of 2^y
   uint64_t S2;      // two partial sums of 2^y y
   float negm;
-  int32_t idx;
+  int32_t idx;      // first index of m among the tail elements (greedy)
+  float vm;         // max over the thread's full vectors (greedy)
+  int32_t vv;       // first id of the first vector holding vm, -1 if none
+  float vm_tail;    // the thread's tail element, if any (greedy)
   float best_s;
   int32_t best_v;
   float best_z;
@@ -50,6 +59,7 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
 constexpr float kMInit = -0x1p+121f;  // below every sanitized value
 constexpr float kTopClamp = 0x1p+100f;
 constexpr uint32_t kTopBf16x2 = 0x71807180u;  // two bf16 2^100
+constexpr float kNegInf = -__builtin_huge_valf();
 
 __device__ __forceinline__ void acc_init(Acc& a) {
   a.m = kMInit;
@@ -57,7 +67,10 @@ __device__ __forceinline__ void acc_init(Acc& a) {
   a.S2 = 0;
   a.negm = -kMInit;
   a.idx = 0x7FFFFFFF;
-  a.best_s = -__int_as_float(0x7F800000);
+  a.vm = kMInit;
+  a.vv = -1;
+  a.vm_tail = kMInit;
+  a.best_s = kNegInf;
   a.best_v = 0x7FFFFFFF;
   a.best_z = 0.0f;
 }
@@ -89,6 +102,30 @@ __device__ __forceinline__ float sanitize(float z) {
   return fminf(fmaxf(z, kSentinel), kTopClamp);  // fmaxf drops a NaN operand
 }
 
+// fp32 bits: NaN and values <= -2^100 -> -2^100 (fmaxf drops a NaN operand).
+__device__ __forceinline__ uint32_t sanitize_low_bits(uint32_t b) {
+  return __float_as_uint(fmaxf(__uint_as_float(b), kSentinel));
+}
+__device__ __forceinline__ uint32_t clamp_top_bits(uint32_t b) {
+  return __float_as_uint(fminf(__uint_as_float(b), kTopClamp));
+}
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Adds two sanitized logits (<= the running max) to the sums (Z2, S2).
+__device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, float z1, uint64_t negm2) {
+  const uint64_t d2 = add2(pack2(z0, z1), negm2);
+  const uint64_t y2 = mul2(d2, pack2(kLog2e, kLog2e));
+  float y0, y1;
+  unpack2(y2, y0, y1);
+  const uint64_t e2 = pack2(ex2_approx(y0), ex2_approx(y1));
+  Z2 = add2(Z2, e2);
+  S2 = fma2(e2, y2, S2);
+}
+
 // Combines b into a (a and b may cover any id sets).
 template <bool GUMBEL>
 __device__ __forceinline__ void part_combine(Partial& a, const Partial& b) {
@@ -110,6 +147,19 @@ __device__ __forceinline__ void part_combine(Partial& a, const Partial& b) {
       a.best_z = b.best_z;
     }
   }
+}
+
+__device__ __forceinline__ Partial empty_partial() {
+  Partial p;
+  p.m = kMInit;
+  p.Z = 0.0f;
+  p.S2 = 0.0f;
+  p.idx = 0x7FFFFFFF;
+  p.best_s = kNegInf;
+  p.best_z = 0.0f;
+  p.best_v = 0x7FFFFFFF;
+  p.pad = 0;
+  return p;
 }
 
 __device__ __forceinline__ Partial acc_to_partial(const Acc& a) {
@@ -148,6 +198,16 @@ __device__ __forceinline__ Partial shfl_partial(const Partial& p, int o) {
   return q;
 }
 
+template <bool GUMBEL>
+__device__ __forceinline__ Partial warp_combine(Partial part) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const Partial q = shfl_partial<GUMBEL>(part, o);
+    part_combine<GUMBEL>(part, q);
+  }
+  return part;
+}
+
 __device__ __forceinline__ void store_partial(Partial* dst, const Partial& p) {
   const int4* s = reinterpret_cast<const int4*>(&p);
   int4* d = reinterpret_cast<int4*>(dst);
@@ -164,9 +224,38 @@ __device__ __forceinline__ Partial load_partial(const Partial* src) {
   return p;
 }
 
-// Writes x0, prob and entropy of one row from its full reduction.
+// Reads a Partial held in the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ Partial load_partial_dsmem(const Partial* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+  Partial p;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&p);
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(remote)
+               : "memory");
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "r"(remote + 16u)
+               : "memory");
+  return p;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Writes x0, prob and entropy of one row from its full reduction and, in the
+// fused step, makes the row's own commit / edit decisions.  Run by one thread.
+// Returns the batch row whose sorting rule this CTA must now run, or -1.
 template <bool GUMBEL>
-__device__ __forceinline__ void finalize_row(const StatsParams& p, int64_t row, const Partial& r) {
+__device__ int32_t finish_row(const StatsParams& p, int64_t row, const Partial& r) {
   const int32_t x0 = GUMBEL ? r.best_v : r.idx;
   const float zx = GUMBEL ? r.best_z : r.m;
   const float prob = ex2_approx((zx - r.m) * kLog2e) / r.Z;
@@ -175,6 +264,55 @@ __device__ __forceinline__ void finalize_row(const StatsParams& p, int64_t row, 
   p.x0[row] = x0;
   p.prob[row] = prob;
   p.entropy[row] = H;
+  if (!p.fused) return -1;
+
+  const RuleArgs& a = p.rule;
+  const int64_t b = row / p.L, l = row - b * p.L;
+  const bool per_row = a.rule == kRuleThreshold || a.rule == kRuleNone;
+  if (per_row) {
+    int32_t tok;
+    const bool cand = is_candidate(a, b, l, &tok);
+    const float c = nan_to(prob, kNegInf);
+    bool commit = false, edit = false;
+    if (a.rule == kRuleThreshold && cand) commit = a.strict ? (c > a.tau) : (c >= a.tau);
+    if (a.edit && !cand) edit = (x0 != tok) && (c > a.tau_edit);
+    if (a.commit) a.commit[row] = commit ? 1 : 0;
+    if (a.edit_mask) a.edit_mask[row] = edit ? 1 : 0;
+    if ((commit || edit) && a.canvas) a.canvas[b * a.canvas_stride + a.canvas_offset + l] = x0;
+    if (cand) {
+      atomicAdd(p.batch_cand + b, 1);
+      if (a.rule == kRuleThreshold) atomicMax(p.batch_forced + b, ~desc_key(c, l));
+    }
+    if (commit) atomicAdd(p.batch_commit + b, 1);
+    if (edit) atomicAdd(p.batch_edit + b, 1);
+  }
+  __threadfence();
+  const int32_t old = atomicAdd(p.batch_count + b, 1);
+  if (old != p.L - 1) return -1;
+  __threadfence();
+  if (!per_row) return static_cast<int32_t>(b);
+  // Last row of the batch row: force one commit if candidates exist and none passed.
+  const int32_t n_cand = __ldcg(p.batch_cand + b);
+  int32_t n_commit = __ldcg(p.batch_commit + b);
+  const int32_t n_edit = __ldcg(p.batch_edit + b);
+  if (a.rule == kRuleThreshold && n_cand > 0 && n_commit == 0) {
+    const unsigned long long key = ~__ldcg(p.batch_forced + b);
+    const int64_t lf = static_cast<int64_t>(key & 0xFFFFFFFFull);
+    if (a.commit) a.commit[b * p.L + lf] = 1;
+    if (a.canvas) a.canvas[b * a.canvas_stride + a.canvas_offset + lf] = __ldcg(p.x0 + b * p.L + lf);
+    n_commit = 1;
+  }
+  if (a.counts) {
+    a.counts[3 * b + 0] = n_cand;
+    a.counts[3 * b + 1] = n_commit;
+    a.counts[3 * b + 2] = n_edit;
+  }
+  p.batch_cand[b] = 0;
+  p.batch_commit[b] = 0;
+  p.batch_edit[b] = 0;
+  p.batch_forced[b] = 0ull;
+  p.batch_count[b] = 0;
+  return -1;
 }
 
 __device__ __forceinline__ int64_t unit_start(int64_t c, int64_t U, int64_t P) { return (c * U) / P; }
@@ -190,277 +328,158 @@ struct SharedCtl {
   Partial result;
   uint64_t rule_red64[kConsumerWarps];
   int32_t rule_red32[4 * kConsumerWarps];
-  float warp_best[kConsumerWarps];
   int32_t abort_flag;
-  int32_t flag;            // broadcast of per-segment decisions
+  int32_t flag;
+  int32_t flag2;
 };
 
-// Bounded wait used by the consumers: gives up when the CTA has aborted.
+// Bounded wait used by the consumers: sleeps in hardware until the copy
+// lands; gives up when the CTA has aborted or the deadline passes.
 __device__ __forceinline__ bool consumer_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
 
+// Consumer-side state of one CTA.
 template <bool BF16, bool GUMBEL>
-__global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constant__ StatsParams p) {
-  extern __shared__ __align__(128) uint8_t dsmem[];
-  __shared__ SharedCtl ctl;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int64_t c = blockIdx.x;
-  const int64_t u_begin = unit_start(c, p.U, p.P);
-  const int64_t u_end = unit_start(c + 1, p.U, p.P);
-  const int64_t n_units = u_end - u_begin;
-  const int stages = p.stages;
-  const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
-  const uint32_t ring = smem_addr(dsmem);
-
-  if (tid == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(smem_addr(&ctl.full[s]), 1);
-      mbar_init(smem_addr(&ctl.empty[s]), kConsumerWarps);
-    }
-    ctl.abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  // Inputs may be written by the previous kernel in the stream.
-  pdl_wait();
-  pdl_launch_dependents();
-
-  volatile int32_t* abort_flag = &ctl.abort_flag;
-
-  if (warp == kConsumerWarps) {
-    // ---------------- producer: one thread issues the bulk copies ----------------
-    if (lane == 0) {
-      int64_t issued = 0;
-      for (int64_t i = 0; i < n_units; ++i) {
-        const int slot = static_cast<int>(i % stages);
-        if (i >= stages) {
-          const uint32_t par = static_cast<uint32_t>((i / stages - 1) & 1);
-          if (!mbar_wait_bounded(smem_addr(&ctl.empty[slot]), par) || *abort_flag) {
-            if (!*abort_flag) {
-              atomicExch(p.fault, kFaultEmptyWait);
-              *abort_flag = 1;
-            }
-            break;
-          }
-        }
-        const int64_t u = u_begin + i;
-        const int64_t row = u / p.K, uk = u - row * p.K;
-        const int64_t v0 = uk * p.chunk_vec;
-        int64_t nv = p.nvec - v0;
-        nv = nv < p.chunk_vec ? nv : p.chunk_vec;
-        nv = nv > 0 ? nv : 0;
-        const uint32_t bar = smem_addr(&ctl.full[slot]);
-        if (nv > 0) {
-          const uint32_t bytes = static_cast<uint32_t>(nv) * 16u;
-          mbar_arrive_expect_tx(bar, bytes);
-          bulk_copy_g2s(ring + slot * chunk_bytes, p.logits + row * p.row_bytes + v0 * 16, bytes, bar);
-        } else {
-          mbar_arrive(bar);
-        }
-        issued = i + 1;
-      }
-      // Drain: every issued copy must land before the CTA may exit.
-      const uint64_t t0 = global_timer_ns();
-      for (int64_t i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
-        const int slot = static_cast<int>(i % stages);
-        const uint32_t par = static_cast<uint32_t>((i / stages) & 1);
-        while (!mbar_try_wait(smem_addr(&ctl.full[slot]), par)) {
-          if (global_timer_ns() - t0 > kWaitLimitNs) {
-            atomicExch(p.fault, kFaultDrainWait);
-            i = issued;
-            break;
-          }
-        }
-      }
-    }
-    return;
-  }
-
-  // ---------------- consumers ----------------
-  constexpr int EPV = BF16 ? 8 : 4;  // elements per 16-byte vector
-  const float t = p.temperature;
-  const float t_ln2 = t * kLn2;
-
-  RuleScratch rs;
-  rs.keys = reinterpret_cast<uint64_t*>(dsmem + static_cast<size_t>(stages) * chunk_bytes);
-  rs.flags = reinterpret_cast<uint8_t*>(rs.keys + kFusedSortCap);
-  rs.red64 = ctl.rule_red64;
-  rs.red32 = ctl.rule_red32;
-  rs.cap = kFusedSortCap;
-
+struct Consumer {
+  static constexpr int EPV = BF16 ? 8 : 4;  // elements per 16-byte vector
+  const StatsParams& p;
+  SharedCtl& ctl;
+  uint32_t ring, chunk_bytes;
+  int tid, warp, lane;
+  float t, t_ln2;
   Acc acc;
-  acc_init(acc);
-  float warp_best = -__int_as_float(0x7F800000);
-  int64_t cur_row = -1, seg_uk0 = 0;
-  bool first_segment = true;
+  float warp_best;
 
-  // Reduces the consumers' states of the current segment and publishes it:
-  // finalize directly, or as a partial for a row shared with other CTAs.
-  auto flush = [&](int64_t row, int64_t uk0, int64_t uk1) {
-    Partial part = acc_to_partial(acc);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      Partial q = shfl_partial<GUMBEL>(part, o);
-      part_combine<GUMBEL>(part, q);
-    }
-    if (lane == 0) ctl.warp_part[warp] = part;
-    named_sync(1, kConsumers);
-    int32_t run_rule_b = -1;
-    if (tid == 0) {
-      Partial r = ctl.warp_part[0];
-      for (int w = 1; w < kConsumerWarps; ++w) part_combine<GUMBEL>(r, ctl.warp_part[w]);
-      bool done = false;
-      if (!*abort_flag) {
-        if (uk0 == 0 && uk1 == p.K - 1) {
-          finalize_row<GUMBEL>(p, row, r);
-          done = true;
-        } else {
-          const int64_t slot = 2 * c + (first_segment ? 0 : 1);
-          store_partial(p.partials + slot, r);
-          __threadfence();
-          const int32_t add = static_cast<int32_t>(uk1 - uk0 + 1);
-          const int32_t old = atomicAdd(p.row_count + row, add);
-          if (old + add == p.K) {
-            // last contributor: combine every partial of the row, in CTA order
-            __threadfence();
-            const int64_t c0 = cta_of_unit(row * p.K, p.U, p.P);
-            const int64_t c1 = cta_of_unit(row * p.K + p.K - 1, p.U, p.P);
-            Partial tot = load_partial(
-                p.partials + 2 * c0 + ((unit_start(c0, p.U, p.P) < row * p.K) ? 1 : 0));
-            for (int64_t cc = c0 + 1; cc <= c1; ++cc) {
-              const Partial q = load_partial(p.partials + 2 * cc);
-              part_combine<GUMBEL>(tot, q);
-            }
-            p.row_count[row] = 0;
-            finalize_row<GUMBEL>(p, row, tot);
-            done = true;
-          }
-        }
-        if (done && p.fused) {
-          __threadfence();
-          const int64_t b = row / p.L;
-          const int32_t old = atomicAdd(p.batch_count + b, 1);
-          if (old == p.L - 1) run_rule_b = static_cast<int32_t>(b);
-        }
-      }
-      ctl.flag = run_rule_b;
-    }
-    named_sync(1, kConsumers);
-    run_rule_b = ctl.flag;
-    if (run_rule_b >= 0) {
-      __threadfence();
-      run_rule<kConsumers, 1>(p.rule, run_rule_b, rs, tid);
-      if (tid == 0) p.batch_count[run_rule_b] = 0;
-    }
-    first_segment = false;
-  };
+  __device__ Consumer(const StatsParams& p_, SharedCtl& ctl_, uint32_t ring_, uint32_t chunk_bytes_)
+      : p(p_), ctl(ctl_), ring(ring_), chunk_bytes(chunk_bytes_) {
+    tid = threadIdx.x;
+    warp = tid >> 5;
+    lane = tid & 31;
+    t = p.temperature;
+    t_ln2 = t * kLn2;
+    reset();
+  }
 
-  for (int64_t i = 0; i < n_units; ++i) {
-    const int slot = static_cast<int>(i % stages);
-    const uint32_t par = static_cast<uint32_t>((i / stages) & 1);
-    const int64_t u = u_begin + i;
-    const int64_t row = u / p.K, uk = u - row * p.K;
-    if (row != cur_row) {
-      if (cur_row >= 0) flush(cur_row, seg_uk0, p.K - 1);
-      acc_init(acc);
-      warp_best = -__int_as_float(0x7F800000);
-      cur_row = row;
-      seg_uk0 = uk;
-    }
-    const int64_t v_unit = uk * p.chunk_vec;  // first vector of the unit
-    int64_t nv = p.nvec - v_unit;
-    nv = nv < p.chunk_vec ? nv : p.chunk_vec;
-    // suppressed ids inside this unit (CTA-uniform)
-    const int64_t id_lo = v_unit * EPV;
-    const int64_t id_hi = (uk == p.K - 1) ? p.V : (v_unit + nv) * EPV;
-    bool unit_has_sup = false;
-    for (int s = 0; s < p.n_sup; ++s) unit_has_sup |= (p.sup[s] >= id_lo && p.sup[s] < id_hi);
+  __device__ void reset() {
+    acc_init(acc);
+    warp_best = kNegInf;
+  }
 
-    if (!*abort_flag && !consumer_wait(smem_addr(&ctl.full[slot]), par, abort_flag)) {
-      if (!*abort_flag) {
-        atomicExch(p.fault, kFaultFullWait);
-        *abort_flag = 1;
-      }
+  static constexpr int kVPT = 1024 / kConsumers;  // vectors per thread in the largest unit
+  static constexpr uint32_t kAbsentWord = BF16 ? 0xFB80FB80u : 0xFB800000u;  // -2^120 in every lane
+
+  // Reduces one unit: nv (<= 1024) vectors in the ring stage at shared
+  // address `base`, the first being vector v_unit of global row `row`.
+  // Thread tid holds vectors tid, tid + 256, ...: all its loads are issued
+  // first, the unit's max comes from one max tree (bf16x2 for bf16), the
+  // running state is rescaled at most once, and the sums run on two
+  // independent accumulator pairs.
+  __device__ void unit(uint32_t base, int64_t row, int64_t v_unit, int64_t nv, bool unit_has_sup) {
+    uint32_t w[kVPT][4];
+    bool valid[kVPT];
+#pragma unroll
+    for (int j = 0; j < kVPT; ++j) {
+      const int64_t vi = static_cast<int64_t>(j) * kConsumers + tid;
+      valid[j] = vi < nv;
+      const uint4 q = valid[j] ? lds128(base + static_cast<uint32_t>(vi) * 16u)
+                               : make_uint4(kAbsentWord, kAbsentWord, kAbsentWord, kAbsentWord);
+      w[j][0] = q.x;
+      w[j][1] = q.y;
+      w[j][2] = q.z;
+      w[j][3] = q.w;
     }
-    const uint32_t base = ring + slot * chunk_bytes;
-    // The trip count is the same for every consumer thread (warp-collective
-    // operations below need all 32 lanes); lanes past the unit's end idle.
-    for (int64_t vb = 0; vb < nv; vb += kConsumers) {
-      const int64_t vi = vb + tid;
-      const bool valid = vi < nv;
-      const uint4 q = valid ? lds128(base + static_cast<uint32_t>(vi) * 16u) : make_uint4(0, 0, 0, 0);
-      const int64_t v0 = (v_unit + vi) * EPV;
-      float z[EPV];
-      if (BF16) {
-        uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    // NaN and values <= -2^100 -> -2^100 (the top clamp is applied below,
+    // only when the unit holds a value above 2^100).
 #pragma unroll
-        for (int j = 0; j < 4; ++j) w[j] = bmax2(w[j], kSentinelBf16x2);
-        // clamp the top at 2^100 (min of bf16 pairs)
+    for (int j = 0; j < kVPT; ++j)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t r;
-          asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w[j]), "r"(kTopBf16x2));
-          w[j] = r;
-        }
-        if (unit_has_sup) {
-          for (int s = 0; s < p.n_sup; ++s) {
-            const int64_t off = p.sup[s] - v0;
+      for (int k = 0; k < 4; ++k) w[j][k] = BF16 ? bmax2(w[j][k], kSentinelBf16x2) : sanitize_low_bits(w[j][k]);
+    if (unit_has_sup) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (off == 2 * j) w[j] = (w[j] & 0xFFFF0000u) | kAbsentBf16;
-              if (off == 2 * j + 1) w[j] = (w[j] & 0x0000FFFFu) | (kAbsentBf16 << 16);
+      for (int j = 0; j < kVPT; ++j) {
+        const int64_t v0 = (v_unit + static_cast<int64_t>(j) * kConsumers + tid) * EPV;
+        for (int s = 0; s < p.n_sup; ++s) {
+          const int64_t off = p.sup[s] - v0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (BF16) {
+              if (off == 2 * k) w[j][k] = (w[j][k] & 0xFFFF0000u) | kAbsentBf16;
+              if (off == 2 * k + 1) w[j][k] = (w[j][k] & 0x0000FFFFu) | (kAbsentBf16 << 16);
+            } else if (off == k) {
+              w[j][k] = __float_as_uint(kAbsent);
             }
           }
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          z[2 * j] = bf16lo(w[j]);
-          z[2 * j + 1] = bf16hi(w[j]);
-        }
-      } else {
-        z[0] = sanitize(__uint_as_float(q.x));
-        z[1] = sanitize(__uint_as_float(q.y));
-        z[2] = sanitize(__uint_as_float(q.z));
-        z[3] = sanitize(__uint_as_float(q.w));
-        if (unit_has_sup) {
-          for (int s = 0; s < p.n_sup; ++s) {
-            const int64_t off = p.sup[s] - v0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (off == j) z[j] = kAbsent;
-          }
-        }
       }
-      float vmax = z[0];
+    }
+    // per-vector and unit maxima
+    float vmax[kVPT];
 #pragma unroll
-      for (int j = 1; j < EPV; ++j) vmax = fmaxf(vmax, z[j]);
-      if (valid) {
-        if (vmax > acc.m) {
-          acc_rescale(acc, vmax);
-          if (!GUMBEL) {
+    for (int j = 0; j < kVPT; ++j) vmax[j] = valid[j] ? vector_max(w[j]) : kMInit;
+    float umax = vmax[0];
 #pragma unroll
-            for (int j = EPV - 1; j >= 0; --j)
-              if (z[j] == vmax) acc.idx = static_cast<int32_t>(v0 + j);
-          }
-        }
+    for (int j = 1; j < kVPT; ++j) umax = fmaxf(umax, vmax[j]);
+    if (umax > kTopClamp) {  // rare: +inf or huge logits count as 2^100
 #pragma unroll
-        for (int j = 0; j < EPV; j += 2) acc_pair(acc, z[j], z[j + 1]);
+      for (int j = 0; j < kVPT; ++j) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[j][k] = BF16 ? bmin2(w[j][k], kTopBf16x2) : clamp_top_bits(w[j][k]);
+        vmax[j] = fminf(vmax[j], kTopClamp);
       }
+      umax = kTopClamp;
+    }
+    if (!GUMBEL) {
+      // The first vector holding this thread's max (ids increase with j and
+      // from unit to unit, so a strict > keeps the earliest).  The element
+      // inside it is located once per row, in resolve_index().
+#pragma unroll
+      for (int j = 0; j < kVPT; ++j) {
+        const bool better = vmax[j] > acc.vm;
+        acc.vm = better ? vmax[j] : acc.vm;
+        acc.vv = better ? static_cast<int32_t>((v_unit + static_cast<int64_t>(j) * kConsumers + tid) * EPV) : acc.vv;
+      }
+    }
+    // Branch-free rescale to the new running max (factor 1 when it did not grow).
+    {
+      const float mnew = fmaxf(acc.m, umax);
+      const float d = (acc.m - mnew) * kLog2e;
+      const float c = ex2_approx(d);
+      const uint64_t d2 = pack2(d, d), c2 = pack2(c, c);
+      acc.S2 = mul2(c2, fma2(d2, acc.Z2, acc.S2));
+      acc.Z2 = mul2(acc.Z2, c2);
+      acc.m = mnew;
+      acc.negm = -mnew;
+    }
+    const uint64_t negm2 = pack2(acc.negm, acc.negm);
+    uint64_t Zb = 0, Sb = 0;
+#pragma unroll
+    for (int j = 0; j < kVPT; ++j) {
+      if (!valid[j]) continue;
+#pragma unroll
+      for (int e = 0; e < EPV; e += 4) {
+        acc_pair2(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), negm2);
+        acc_pair2(Zb, Sb, elem(w[j], e + 2), elem(w[j], e + 3), negm2);
+      }
+    }
+    acc.Z2 = add2(acc.Z2, Zb);
+    acc.S2 = add2(acc.S2, Sb);
 
-      if (GUMBEL) {
+    if (GUMBEL) {
+      bool updated = false;
+#pragma unroll
+      for (int j = 0; j < kVPT; ++j) {
+        const int64_t v0 = (v_unit + static_cast<int64_t>(j) * kConsumers + tid) * EPV;
         // Philox words of ids v0 .. v0 + EPV - 1 (v0 is a multiple of 4)
         uint32_t r[EPV];
-        const uint32_t row_lo = static_cast<uint32_t>(row), row_hi = static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32);
+        const uint32_t row_lo = static_cast<uint32_t>(row);
+        const uint32_t row_hi = static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32);
 #pragma unroll
         for (int h = 0; h < EPV / 4; ++h) {
           const uint4 o = philox4x32_10(static_cast<uint32_t>((v0 >> 2) + h), row_lo, row_hi, 0u, p.key);
@@ -471,79 +490,445 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
         }
         uint32_t rmax = r[0];
 #pragma unroll
-        for (int j = 1; j < EPV; ++j) rmax = max(rmax, r[j]);
+        for (int e = 1; e < EPV; ++e) rmax = max(rmax, r[e]);
         // g = -ln(-ln u) <= -ln(1 - u) for every id of the vector; the margin
         // covers the fp32 rounding of ln_p, lg2.approx and the final fmaf.
         const float w1 = __fsub_rn(1.0f, uniform_from_bits(rmax));
         const float gbound = -lg2_approx(w1);
-        const float bound = fmaf(t_ln2, gbound, vmax + fmaf(fabsf(vmax), 1e-6f, 1e-3f));
-        const bool survive = valid && !(bound < warp_best);
-        bool updated = false;
-        if (survive) {
+        const float bound = fmaf(t_ln2, gbound, vmax[j] + fmaf(fabsf(vmax[j]), 1e-6f, 1e-3f));
+        if (valid[j] && !(bound < warp_best)) {
 #pragma unroll
-          for (int j = 0; j < EPV; ++j) {
-            const float s = gumbel_score(z[j], t, r[j]);
-            if (s > acc.best_s) {
-              acc.best_s = s;
-              acc.best_v = static_cast<int32_t>(v0 + j);
-              acc.best_z = z[j];
+          for (int e = 0; e < EPV; ++e) {
+            const float z = elem(w[j], e);
+            const float sc = gumbel_score(z, t, r[e]);
+            if (sc > acc.best_s) {
+              acc.best_s = sc;
+              acc.best_v = static_cast<int32_t>(v0 + e);
+              acc.best_z = z;
               updated = true;
             }
           }
         }
-        if (__any_sync(0xFFFFFFFFu, updated)) {
-          float wb = acc.best_s;
+      }
+      if (__any_sync(0xFFFFFFFFu, updated)) {
+        float wb = acc.best_s;
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, o));
-          warp_best = fmaxf(warp_best, wb);
-        }
-      }
-    }
-    // Release the stage: one arrival per consumer warp.
-    __syncwarp();
-    if (lane == 0 && !*abort_flag) mbar_arrive(smem_addr(&ctl.empty[slot]));
-
-    // Elements after the last full vector of the row (V * size % 16 != 0).
-    if (uk == p.K - 1 && p.tail > 0 && tid < p.tail && !*abort_flag) {
-      const int64_t v = p.nvec * EPV + tid;
-      const uint8_t* rowp = p.logits + row * p.row_bytes;
-      float z;
-      if (BF16) {
-        const uint16_t bits = __ldg(reinterpret_cast<const uint16_t*>(rowp) + v);
-        z = __uint_as_float(static_cast<uint32_t>(bits) << 16);
-      } else {
-        z = __ldg(reinterpret_cast<const float*>(rowp) + v);
-      }
-      z = sanitize(z);
-      for (int s = 0; s < p.n_sup; ++s)
-        if (p.sup[s] == v) z = kAbsent;
-      if (z > acc.m) {
-        acc_rescale(acc, z);
-        acc.idx = static_cast<int32_t>(v);
-      }
-      {
-        const float y = (z - acc.m) * kLog2e;
-        const float e = ex2_approx(y);
-        acc.Z2 = add2(acc.Z2, pack2(e, 0.0f));
-        acc.S2 = fma2(pack2(e, 0.0f), pack2(y, 0.0f), acc.S2);
-      }
-      if (GUMBEL) {
-        const uint4 o = philox4x32_10(static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(row),
-                                      static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32), 0u, p.key);
-        const int w = static_cast<int>(v & 3);
-        const uint32_t word = w == 0 ? o.x : (w == 1 ? o.y : (w == 2 ? o.z : o.w));
-        const float s = gumbel_score(z, t, word);
-        if (s > acc.best_s) {
-          acc.best_s = s;
-          acc.best_v = static_cast<int32_t>(v);
-          acc.best_z = z;
-        }
+        for (int o = 16; o > 0; o >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, o));
+        warp_best = fmaxf(warp_best, wb);
       }
     }
   }
-  if (cur_row >= 0) {
-    const int64_t last_u = u_end - 1;
-    flush(cur_row, seg_uk0, last_u - cur_row * p.K);
+
+  // Element e of a 16-byte vector held as four 32-bit words.
+  __device__ __forceinline__ static float elem(const uint32_t (&v)[4], int e) {
+    if (BF16) return (e & 1) ? bf16hi(v[e >> 1]) : bf16lo(v[e >> 1]);
+    return __uint_as_float(v[e]);
+  }
+
+  __device__ __forceinline__ static float vector_max(const uint32_t (&v)[4]) {
+    if (BF16) {
+      const uint32_t m = bmax2(bmax2(v[0], v[1]), bmax2(v[2], v[3]));
+      return fmaxf(bf16lo(m), bf16hi(m));
+    }
+    return fmaxf(fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                 fmaxf(__uint_as_float(v[2]), __uint_as_float(v[3])));
+  }
+
+  // Elements after the last full vector of `row` (V * size % 16 != 0); one
+  // element per thread tid < p.tail.
+  __device__ void tail(int64_t row) {
+    if (p.tail <= 0 || tid >= p.tail) return;
+    const int64_t v = p.nvec * EPV + tid;
+    const uint8_t* rowp = p.logits + row * p.row_bytes;
+    float z;
+    if (BF16) {
+      const uint16_t bits = __ldg(reinterpret_cast<const uint16_t*>(rowp) + v);
+      z = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+    } else {
+      z = __ldg(reinterpret_cast<const float*>(rowp) + v);
+    }
+    z = sanitize(z);
+    for (int s = 0; s < p.n_sup; ++s)
+      if (p.sup[s] == v) z = kAbsent;
+    if (z > acc.m) acc_rescale(acc, z);
+    acc.idx = static_cast<int32_t>(v);  // one tail element per thread
+    acc.vm_tail = z;
+    const float y = (z - acc.m) * kLog2e;
+    const float e = ex2_approx(y);
+    acc.Z2 = add2(acc.Z2, pack2(e, 0.0f));
+    acc.S2 = fma2(pack2(e, 0.0f), pack2(y, 0.0f), acc.S2);
+    if (GUMBEL) {
+      const uint4 o = philox4x32_10(static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(row),
+                                    static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32), 0u, p.key);
+      const int w = static_cast<int>(v & 3);
+      const uint32_t word = w == 0 ? o.x : (w == 1 ? o.y : (w == 2 ? o.z : o.w));
+      const float s = gumbel_score(z, t, word);
+      if (s > acc.best_s) {
+        acc.best_s = s;
+        acc.best_v = static_cast<int32_t>(v);
+        acc.best_z = z;
+      }
+    }
+  }
+
+  // Greedy x0 bookkeeping: the first id holding this thread's max acc.m.  It
+  // is in the best full vector (ids below every tail element) unless the tail
+  // element is larger; the vector is read once more from global memory (an
+  // L2 hit) and sanitized exactly as when it was streamed.
+  __device__ void resolve_index(int64_t row) {
+    if (GUMBEL) return;
+    int32_t idx = 0x7FFFFFFF;
+    if (acc.vv >= 0 && acc.vm == acc.m) {
+      const uint8_t* rowp = p.logits + row * p.row_bytes;
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(rowp + static_cast<int64_t>(acc.vv) * (BF16 ? 2 : 4)));
+      uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        w[k] = BF16 ? bmin2(bmax2(w[k], kSentinelBf16x2), kTopBf16x2) : clamp_top_bits(sanitize_low_bits(w[k]));
+      for (int s = 0; s < p.n_sup; ++s) {
+        const int64_t off = p.sup[s] - acc.vv;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (BF16) {
+            if (off == 2 * k) w[k] = (w[k] & 0xFFFF0000u) | kAbsentBf16;
+            if (off == 2 * k + 1) w[k] = (w[k] & 0x0000FFFFu) | (kAbsentBf16 << 16);
+          } else if (off == k) {
+            w[k] = __float_as_uint(kAbsent);
+          }
+        }
+      }
+#pragma unroll
+      for (int e = EPV - 1; e >= 0; --e)
+        if (elem(w, e) == acc.vm) idx = acc.vv + e;
+    } else if (acc.vm_tail == acc.m && acc.m > kMInit) {
+      idx = acc.idx;
+    }
+    acc.idx = idx;
+  }
+
+  // Whether suppressed ids fall in [lo, hi) (the same answer in every thread).
+  __device__ bool has_sup(int64_t lo, int64_t hi) const {
+    bool any = false;
+    for (int s = 0; s < p.n_sup; ++s) any |= (p.sup[s] >= lo && p.sup[s] < hi);
+    return any;
+  }
+
+  // The CTA's reduction of all consumer states; valid in thread 0.
+  __device__ Partial cta_reduce() {
+    Partial part = warp_combine<GUMBEL>(acc_to_partial(acc));
+    if (lane == 0) ctl.warp_part[warp] = part;
+    named_sync(1, kConsumers);
+    Partial r = ctl.warp_part[0];
+    if (tid == 0)
+      for (int w = 1; w < kConsumerWarps; ++w) part_combine<GUMBEL>(r, ctl.warp_part[w]);
+    return r;
+  }
+
+  // Runs the sorting rule of batch row b in this CTA's consumer warps.
+  __device__ void rule_if_needed(int32_t b, uint8_t* rule_smem) {
+    if (b < 0) return;
+    RuleScratch rs;
+    rs.keys = reinterpret_cast<uint64_t*>(rule_smem);
+    rs.flags = rule_smem + static_cast<size_t>(kFusedSortCap) * 8;
+    rs.red64 = ctl.rule_red64;
+    rs.red32 = ctl.rule_red32;
+    rs.cap = kFusedSortCap;
+    __threadfence();
+    run_rule<kConsumers, 1>(p.rule, b, rs, tid);
+    if (tid == 0) p.batch_count[b] = 0;
+  }
+};
+
+// Position in the shared-memory ring: stage index and mbarrier phase parity.
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void advance(int stages) {
+    if (++slot == stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Producer: issues the bulk copies of this CTA's n units in order; next(src,
+// bytes) yields each unit's global address and size.  Returns when every
+// issued copy has landed (or, after a fault, when the drain deadline passes).
+template <typename Next>
+__device__ void produce(const StatsParams& p, SharedCtl& ctl, uint32_t ring, uint32_t chunk_bytes, int64_t n,
+                        Next next) {
+  volatile int32_t* abort_flag = &ctl.abort_flag;
+  const int stages = p.stages;
+  RingPos r;
+  int64_t issued = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    if (i >= stages) {  // wait until the consumers released this stage's previous unit
+      if (!mbar_wait_bounded(smem_addr(&ctl.empty[r.slot]), r.phase ^ 1u) || *abort_flag) {
+        if (!*abort_flag) {
+          atomicExch(p.fault, kFaultEmptyWait);
+          *abort_flag = 1;
+        }
+        break;
+      }
+    }
+    const uint8_t* src;
+    uint32_t bytes;
+    next(src, bytes);
+    const uint32_t bar = smem_addr(&ctl.full[r.slot]);
+    if (bytes > 0) {
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_copy_g2s(ring + r.slot * chunk_bytes, src, bytes, bar);
+    } else {
+      mbar_arrive(bar);
+    }
+    issued = i + 1;
+    r.advance(stages);
+  }
+  // Drain: the last (up to `stages`) issued copies must land before exit.
+  const long long t0 = clock64();
+  for (int64_t i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+    const int slot = static_cast<int>(i % stages);
+    const uint32_t par = static_cast<uint32_t>((i / stages) & 1);
+    while (!mbar_try_wait_sleep(smem_addr(&ctl.full[slot]), par, kSleepHintNs)) {
+      if (clock64() - t0 > kWaitLimitCycles) {
+        atomicExch(p.fault, kFaultDrainWait);
+        return;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void init_barriers(SharedCtl& ctl, int stages) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(smem_addr(&ctl.full[s]), 1);
+      mbar_init(smem_addr(&ctl.empty[s]), kConsumerWarps);
+    }
+    ctl.abort_flag = 0;
+    fence_mbar_init();
+  }
+}
+
+// Consumer wait for the unit at ring position r; records a fault and aborts
+// the CTA on timeout.
+__device__ __forceinline__ void wait_unit(const StatsParams& p, SharedCtl& ctl, const RingPos& r) {
+  volatile int32_t* abort_flag = &ctl.abort_flag;
+  if (!*abort_flag && !consumer_wait(smem_addr(&ctl.full[r.slot]), r.phase, abort_flag)) {
+    if (!*abort_flag) {
+      atomicExch(p.fault, kFaultFullWait);
+      *abort_flag = 1;
+    }
+  }
+}
+
+__device__ __forceinline__ void release_unit(SharedCtl& ctl, const RingPos& r, int lane) {
+  __syncwarp();
+  if (lane == 0 && !ctl.abort_flag) mbar_arrive(smem_addr(&ctl.empty[r.slot]));
+}
+
+// ---------------------------------------------------------------------------
+// Persistent kernel: many rows.  CTA c owns units [c U / P, (c+1) U / P).
+// ---------------------------------------------------------------------------
+template <bool BF16, bool GUMBEL>
+__global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constant__ StatsParams p) {
+  extern __shared__ __align__(128) uint8_t dsmem[];
+  __shared__ SharedCtl ctl;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int64_t c = blockIdx.x;
+  const int64_t u_begin = unit_start(c, p.U, p.P);
+  const int64_t u_end = unit_start(c + 1, p.U, p.P);
+  const int64_t n_units = u_end - u_begin;
+  const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
+  const uint32_t ring = smem_addr(dsmem);
+
+  init_barriers(ctl, p.stages);
+  __syncthreads();
+  if (!p.early) pdl_wait();   // inputs may come from the previous kernel in the stream
+  pdl_launch_dependents();
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      int64_t prow = u_begin / p.K, puk = u_begin - prow * p.K;
+      produce(p, ctl, ring, chunk_bytes, n_units, [&](const uint8_t*& src, uint32_t& bytes) {
+        const int64_t v0 = puk * p.chunk_vec;
+        int64_t nv = p.nvec - v0;
+        nv = nv < p.chunk_vec ? nv : p.chunk_vec;
+        nv = nv > 0 ? nv : 0;
+        src = p.logits + prow * p.row_bytes + v0 * 16;
+        bytes = static_cast<uint32_t>(nv) * 16u;
+        if (++puk == p.K) {
+          puk = 0;
+          ++prow;
+        }
+      });
+    }
+    return;
+  }
+
+  Consumer<BF16, GUMBEL> con(p, ctl, ring, chunk_bytes);
+  uint8_t* rule_smem = dsmem + static_cast<size_t>(p.stages) * chunk_bytes;
+  volatile int32_t* abort_flag = &ctl.abort_flag;
+  int64_t cur_row = -1, seg_uk0 = 0;
+  bool first_segment = true;
+  bool waited = !p.early;
+
+  auto flush = [&](int64_t row, int64_t uk0, int64_t uk1) {
+    if (!waited) {
+      pdl_wait();  // nothing is written before the previous kernel has finished
+      waited = true;
+    }
+    con.resolve_index(row);
+    const Partial r = con.cta_reduce();
+    if (tid == 0) {
+      int32_t action = 0;  // 0 nothing, 1 finish r, 2 combine the row's partials
+      if (!*abort_flag) {
+        if (uk0 == 0 && uk1 == p.K - 1) {
+          ctl.result = r;
+          action = 1;
+        } else {
+          const int64_t slot = 2 * c + (first_segment ? 0 : 1);
+          store_partial(p.partials + slot, r);
+          __threadfence();
+          const int32_t add = static_cast<int32_t>(uk1 - uk0 + 1);
+          if (atomicAdd(p.row_count + row, add) + add == p.K) {
+            __threadfence();
+            action = 2;
+          }
+        }
+      }
+      ctl.flag = action;
+    }
+    named_sync(1, kConsumers);
+    const int32_t action = ctl.flag;
+    if (action == 2 && warp == 0) {
+      // last contributor: warp 0 loads the row's partials in parallel
+      const int64_t c0 = cta_of_unit(row * p.K, p.U, p.P);
+      const int64_t c1 = cta_of_unit(row * p.K + p.K - 1, p.U, p.P);
+      const bool c0_tail = unit_start(c0, p.U, p.P) < row * p.K;
+      Partial tot = empty_partial();
+      for (int64_t cb = c0; cb <= c1; cb += 32) {
+        const int64_t cc = cb + lane;
+        Partial q = empty_partial();
+        if (cc <= c1) q = load_partial(p.partials + 2 * cc + ((cc == c0 && c0_tail) ? 1 : 0));
+        part_combine<GUMBEL>(tot, q);
+      }
+      tot = warp_combine<GUMBEL>(tot);
+      if (lane == 0) {
+        p.row_count[row] = 0;
+        ctl.result = tot;
+      }
+    }
+    if (tid == 0) ctl.flag2 = action != 0 ? finish_row<GUMBEL>(p, row, ctl.result) : -1;
+    named_sync(1, kConsumers);
+    con.rule_if_needed(ctl.flag2, rule_smem);
+    first_segment = false;
+  };
+
+  RingPos rc;
+  int64_t row = u_begin / p.K, uk = u_begin - row * p.K;
+  for (int64_t i = 0; i < n_units; ++i) {
+    if (row != cur_row) {
+      if (cur_row >= 0) flush(cur_row, seg_uk0, p.K - 1);
+      con.reset();
+      cur_row = row;
+      seg_uk0 = uk;
+    }
+    const int64_t v_unit = uk * p.chunk_vec;
+    int64_t nv = p.nvec - v_unit;
+    nv = nv < p.chunk_vec ? nv : p.chunk_vec;
+    const bool sup = con.has_sup(v_unit * con.EPV, (uk == p.K - 1) ? p.V : (v_unit + nv) * con.EPV);
+    wait_unit(p, ctl, rc);
+    con.unit(ring + rc.slot * chunk_bytes, row, v_unit, nv, sup);
+    release_unit(ctl, rc, lane);
+    rc.advance(p.stages);
+    if (uk == p.K - 1 && !*abort_flag) con.tail(row);
+    if (++uk == p.K) {
+      uk = 0;
+      ++row;
+    }
+  }
+  if (cur_row >= 0) flush(cur_row, seg_uk0, (u_end - 1) - cur_row * p.K);
+}
+
+// ---------------------------------------------------------------------------
+// Cluster kernel: few rows.  Cluster `row` of p.cluster CTAs reduces one row;
+// CTA rank k owns vectors [k nvec / S, (k+1) nvec / S) (and rank S-1 the
+// tail).  Rank 0 combines the CTAs' partials through distributed shared
+// memory and finishes the row.
+// ---------------------------------------------------------------------------
+template <bool BF16, bool GUMBEL>
+__global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid_constant__ StatsParams p) {
+  extern __shared__ __align__(128) uint8_t dsmem[];
+  __shared__ SharedCtl ctl;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int S = p.cluster;
+  const uint32_t rank = cluster_rank();
+  const int64_t row = blockIdx.x / S;
+  const int64_t vb = (static_cast<int64_t>(rank) * p.nvec) / S;
+  const int64_t ve = (static_cast<int64_t>(rank + 1) * p.nvec) / S;
+  const int64_t n_units = (ve - vb + p.chunk_vec - 1) / p.chunk_vec;
+  const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
+  const uint32_t ring = smem_addr(dsmem);
+
+  init_barriers(ctl, p.stages);
+  __syncthreads();
+  if (!p.early) pdl_wait();
+  pdl_launch_dependents();
+
+  int32_t rule_b = -1;
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      int64_t pv = vb;
+      produce(p, ctl, ring, chunk_bytes, n_units, [&](const uint8_t*& src, uint32_t& bytes) {
+        int64_t nv = ve - pv;
+        nv = nv < p.chunk_vec ? nv : p.chunk_vec;
+        src = p.logits + row * p.row_bytes + pv * 16;
+        bytes = static_cast<uint32_t>(nv) * 16u;
+        pv += p.chunk_vec;
+      });
+    }
+    __syncwarp();
+    cluster_sync_all();  // partials published
+    cluster_sync_all();  // rank 0 has read them
+    return;
+  }
+
+  Consumer<BF16, GUMBEL> con(p, ctl, ring, chunk_bytes);
+  RingPos rc;
+  for (int64_t i = 0; i < n_units; ++i) {
+    const int64_t v_unit = vb + i * p.chunk_vec;
+    int64_t nv = ve - v_unit;
+    nv = nv < p.chunk_vec ? nv : p.chunk_vec;
+    const bool last_unit = rank == static_cast<uint32_t>(S - 1) && i == n_units - 1;
+    const bool sup = con.has_sup(v_unit * con.EPV, last_unit ? p.V : (v_unit + nv) * con.EPV);
+    wait_unit(p, ctl, rc);
+    con.unit(ring + rc.slot * chunk_bytes, row, v_unit, nv, sup);
+    release_unit(ctl, rc, lane);
+    rc.advance(p.stages);
+  }
+  if (rank == static_cast<uint32_t>(S - 1) && !ctl.abort_flag) con.tail(row);
+  con.resolve_index(row);
+  const Partial r = con.cta_reduce();
+  if (tid == 0) ctl.result = r;
+  __syncwarp();
+  cluster_sync_all();
+  if (rank == 0) {
+    if (p.early) pdl_wait();
+    if (warp == 0) {
+      Partial tot = empty_partial();
+      for (int k = lane; k < S; k += 32) part_combine<GUMBEL>(tot, load_partial_dsmem(&ctl.result, k));
+      tot = warp_combine<GUMBEL>(tot);
+      if (lane == 0) rule_b = ctl.abort_flag ? -1 : finish_row<GUMBEL>(p, row, tot);
+    }
+  }
+  __syncwarp();
+  cluster_sync_all();
+  if (rank == 0) {
+    if (tid == 0) ctl.flag2 = rule_b;
+    named_sync(1, kConsumers);
+    con.rule_if_needed(ctl.flag2, dsmem + static_cast<size_t>(p.stages) * chunk_bytes);
   }
 }
 
@@ -552,12 +937,23 @@ template __global__ void stats_kernel<false, false>(const __grid_constant__ Stat
 template __global__ void stats_kernel<true, false>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<false, true>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<true, true>(const __grid_constant__ StatsParams);
+template __global__ void stats_cluster_kernel<false, false>(const __grid_constant__ StatsParams);
+template __global__ void stats_cluster_kernel<true, false>(const __grid_constant__ StatsParams);
+template __global__ void stats_cluster_kernel<false, true>(const __grid_constant__ StatsParams);
+template __global__ void stats_cluster_kernel<true, true>(const __grid_constant__ StatsParams);
 
 const void* stats_kernel_ptr(bool bf16, bool gumbel) {
   if (bf16) return gumbel ? reinterpret_cast<const void*>(&stats_kernel<true, true>)
                           : reinterpret_cast<const void*>(&stats_kernel<true, false>);
   return gumbel ? reinterpret_cast<const void*>(&stats_kernel<false, true>)
                 : reinterpret_cast<const void*>(&stats_kernel<false, false>);
+}
+
+const void* stats_cluster_kernel_ptr(bool bf16, bool gumbel) {
+  if (bf16) return gumbel ? reinterpret_cast<const void*>(&stats_cluster_kernel<true, true>)
+                          : reinterpret_cast<const void*>(&stats_cluster_kernel<true, false>);
+  return gumbel ? reinterpret_cast<const void*>(&stats_cluster_kernel<false, true>)
+                : reinterpret_cast<const void*>(&stats_cluster_kernel<false, false>);
 }
 
 }  // namespace dllm

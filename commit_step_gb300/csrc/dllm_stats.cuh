@@ -31,6 +31,8 @@ struct alignas(16) Partial {
 
 struct StatsParams {
   const uint8_t* logits;
+  int32_t cluster;          // CTAs per row in the cluster kernel (0: persistent kernel)
+  int32_t early;            // logits are ready before the previous kernel ends: load before the grid dependency
   int64_t row_bytes;        // row stride in bytes (multiple of 16)
   int64_t T, V, L;
   int64_t nvec;             // full 16-byte vectors per row
@@ -50,6 +52,10 @@ struct StatsParams {
   int32_t* fault;
   int32_t* row_count;       // (T) contributions that arrived, split rows only
   int32_t* batch_count;     // (B) rows finished, fused rule only
+  int32_t* batch_cand;      // (B) candidates seen (per-row threshold decisions)
+  int32_t* batch_commit;    // (B) commits made
+  int32_t* batch_edit;      // (B) edits made
+  unsigned long long* batch_forced;  // (B) max of ~ranking key over candidates: the forced commit
   Partial* partials;        // (2 P)
   int32_t fused;
   RuleArgs rule;

@@ -232,7 +232,15 @@ typedef struct {
   int64_t canvas_stride;    /* elements between batch rows of the canvas */
   int64_t canvas_offset;    /* canvas column of position l = 0 */
   int32_t* counts;          /* device (B, 3) or NULL: per batch row [candidates, commits, edits] */
+  int32_t flags;            /* 0, or DLLM_FLAG_INPUTS_READY */
 } dllm_commit_params;
+
+/* The logits were complete before the previous kernel in the stream began
+ * (they are not that kernel's output): the call may start reading them while
+ * that kernel still runs, and writes nothing until it has finished.  Lets
+ * back-to-back steps over independent inputs overlap.  Never set it when the
+ * previous kernel produces the logits (an LM-head GEMM, say). */
+#define DLLM_FLAG_INPUTS_READY 1
 
 dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,
                              int64_t row_stride, float temperature, uint64_t key,

@@ -61,6 +61,7 @@ def test_small_rules_all_kinds(cs, seed):
     w = W.Workload("small", B, L, V, "f32", z, None, [7], 0.0, 0, "", cand, {})
     k = np.array([3, 0, 50], dtype=np.int32)
     check_full(cs, w, "threshold", {"tau": 0.6, "strict": False}, tau=0.6)
+    check_full(cs, w, "threshold", {"tau": 0.999, "strict": True}, tau=0.999, strict=True)   # forced commits
     check_full(cs, w, "topk", {"k": k}, k=torch.from_numpy(k).cuda())
     check_full(cs, w, "factor", {"factor": 1.0}, factor=1.0)
     check_full(cs, w, "entropy_bound", {"gamma": 0.3}, gamma=0.3)
@@ -98,6 +99,31 @@ def test_fused_canvas_candidates_edit_counts(cs):
     assert np.array_equal(canvas.cpu().numpy(), exp)
     assert counts.cpu().numpy().tolist() == [[int(masked[b].sum()), int(want_c[b].sum()), int(want_e[b].sum())]
                                              for b in range(B)]
+
+
+def test_inputs_ready_pipelining_matches_plain_calls(cs):
+    """Back-to-back fused steps over independent buffers with
+    DLLM_FLAG_INPUTS_READY give the same results as plain calls."""
+    rng = np.random.default_rng(12)
+    B, L, V = 2, 32, 50_000
+    bufs, outs_plain = [], []
+    cand = torch.from_numpy((rng.random((B, L)) < 0.6).astype(np.uint8)).cuda()
+    for j in range(4):
+        z = (rng.standard_normal((B * L, V)) * (1 + j)).astype(np.float32)
+        bufs.append(torch.from_numpy(z).cuda().view(B, L, V))
+    for j in range(4):
+        x0, prob, ent, commit, _ = cs.commit_step(bufs[j], rule=1, tau=0.5, cand=cand, suppress_ids=[0])
+        outs_plain.append((x0.clone(), prob.clone(), commit.clone()))
+    res = []
+    for rep in range(3):
+        for j in range(4):
+            x0, prob, ent, commit, _ = cs.commit_step(bufs[j], rule=1, tau=0.5, cand=cand, suppress_ids=[0],
+                                                      inputs_ready=True)
+            res.append((j, x0, prob, commit))
+    torch.cuda.synchronize()
+    for j, x0, prob, commit in res:
+        assert torch.equal(x0, outs_plain[j][0]) and torch.equal(commit, outs_plain[j][2])
+        assert torch.equal(prob, outs_plain[j][1])
 
 
 def test_repeated_fused_calls_leave_workspace_clean(cs):

@@ -55,6 +55,19 @@ def test_few_long_rows_split_across_ctas(cs, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_persistent_path_rows_split_across_ctas(cs, dtype):
+    """Too many rows for one cluster per row: the persistent grid, with rows
+    shared by two or three CTAs and combined through the workspace."""
+    rng = np.random.default_rng(71)
+    V = 200_003 if dtype == "bf16" else 100_001
+    z = gen(rng, 200, V, scale=1.5)
+    host = z if dtype == "f32" else f32_to_bf16_bits(z)
+    per16 = 4 if dtype == "f32" else 8
+    run_case(cs, host, dtype, suppress=[3, V - 1], stride=-(-V // per16) * per16)
+    run_case(cs, host, dtype, temperature=0.9, key=99, stride=-(-V // per16) * per16)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_suppress_nan_inf_and_ties(cs, dtype):
     rng = np.random.default_rng(8)
     V = 5000

@@ -258,17 +258,22 @@ def run_ours(args, rank, world):
     out = (x0, prob, ent, commit, None)
     launches_per_step = 2 if w.rule == "factor+entropy_bound" else 1
 
-    def step(i):
+    def step(i, ready=False):
+        # ready: this step's logits do not come from the kernel before it (the
+        # rotating buffers were filled before timing), so it may start loading
+        # them while that kernel finishes (DLLM_FLAG_INPUTS_READY).
         lg = bufs[i % R]
         if w.rule == "threshold":
             cs.commit_step(lg, rule=cs.RULE_THRESHOLD, tau=w.params["tau"], strict=w.params["strict"],
-                           suppress_ids=w.suppress_ids, cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws)
+                           suppress_ids=w.suppress_ids, cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws,
+                           inputs_ready=ready)
         elif w.rule == "topk":
             cs.commit_step(lg, rule=cs.RULE_TOPK, k=kq, temperature=w.temperature, key=w.key + i,
-                           suppress_ids=w.suppress_ids, cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws)
+                           suppress_ids=w.suppress_ids, cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws,
+                           inputs_ready=ready)
         else:
             cs.commit_step(lg, rule=cs.RULE_FACTOR, factor=w.params["factor"], suppress_ids=w.suppress_ids,
-                           cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws)
+                           cand=cand, canvas=canvas, canvas_offset=128, out=out, ws=ws, inputs_ready=ready)
             cs.entropy_bound_transfer(ent, cand, w.params["gamma"], commit=commit2)
 
     step(0)
@@ -279,18 +284,25 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         return {"profile": w.name, "steps": warmup + steps, "workspace_fault": cs.workspace_fault(ws)}, w
 
-    # graph of G steps over the rotating buffers
+    # graphs of G steps over the rotating buffers: independent steps (the
+    # timed figure) and the same steps as a dependent chain (no early loads)
     G = R if R > 1 else min(50, steps)
     stream = torch.cuda.Stream(dev)
     stream.wait_stream(torch.cuda.current_stream(dev))
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        for i in range(G):   # eager warm-up on the capture stream
-            step(i)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(G):
-            step(i)
+
+    def capture(ready):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(G):   # eager warm-up on the capture stream
+                step(i, ready)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                step(i, ready)
+        return g
+
+    g = capture(True)
+    g_dep = capture(False)
     reps_w = max(1, math.ceil(warmup / G))
     reps = max(1, math.ceil(steps / G))
     steps_done = reps * G
@@ -320,6 +332,20 @@ def run_ours(args, rank, world):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     ms_per_step = ms / steps_done
+
+    # the same steps as a dependent chain (each waits for the previous kernel)
+    reps_dep = max(1, min(reps, math.ceil(20000 / G)))
+    with torch.cuda.stream(stream):
+        g_dep.replay()
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps_dep):
+            g_dep.replay()
+    d1.record(stream)
+    d1.synchronize()
+    dep_ms_per_step = d0.elapsed_time(d1) / (reps_dep * G)
 
     # single-launch latency: one step at a time, synchronised on both sides
     lat = []
@@ -379,8 +405,12 @@ def run_ours(args, rank, world):
                    "parallelism": f"replicas x{world} (batch rows shard, no collective)",
                    "l2": f"{R} rotating logit buffers, {R * nbytes / 1e6:.0f} MB total vs L2 {l2 / 1e6:.0f} MB"
                          if R > 1 else f"one {nbytes / 1e6:.0f} MB buffer, larger than L2 {l2 / 1e6:.0f} MB",
-                   "launch": f"CUDA graph of {G} steps with programmatic dependent launch"},
+                   "launch": f"CUDA graph of {G} independent steps, programmatic dependent launch, "
+                             "DLLM_FLAG_INPUTS_READY (logits resident before timing)"},
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
+        "dependent_steps": {"ms_per_step": dep_ms_per_step,
+                            "value": round(alg / (dep_ms_per_step / 1e3) / 1e9, 2), "unit": "GB/s",
+                            "note": "each step waits for the previous kernel before reading its logits"},
         "single_launch_us": round(single_us, 2),
         "positions_per_s": round(w.B * w.L * steps_done * world / (ms / 1e3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

@@ -89,8 +89,7 @@ const DeviceInfo* device_info() {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t fault = 0, partials = 0, row_count = 0, batch_count = 0, batch_cand = 0, batch_commit = 0, batch_edit = 0,
-         batch_forced = 0, total = 0;
+  size_t fault = 0, partials = 0, row_count = 0, batch_packed = 0, batch_forced = 0, total = 0;
 };
 
 // Fault word, then the partials (a size fixed per device), then the counters.
@@ -102,12 +101,9 @@ WsLayout ws_layout(int64_t B, int64_t L, int sms) {
   w.fault = 0;
   w.partials = 256;
   w.row_count = w.partials + static_cast<size_t>(2) * sms * kMaxCtasPerSm * sizeof(Partial);
-  w.batch_forced = align_up(w.row_count + static_cast<size_t>(B * L) * 4, 8);
-  w.batch_count = w.batch_forced + static_cast<size_t>(B) * 8;
-  w.batch_cand = w.batch_count + static_cast<size_t>(B) * 4;
-  w.batch_commit = w.batch_cand + static_cast<size_t>(B) * 4;
-  w.batch_edit = w.batch_commit + static_cast<size_t>(B) * 4;
-  w.total = align_up(w.batch_edit + static_cast<size_t>(B) * 4, 256);
+  w.batch_packed = align_up(w.row_count + static_cast<size_t>(B * L) * 4, 8);
+  w.batch_forced = w.batch_packed + static_cast<size_t>(B) * 8;
+  w.total = align_up(w.batch_forced + static_cast<size_t>(B) * 8, 256);
   return w;
 }
 
@@ -242,10 +238,7 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.fault = reinterpret_cast<int32_t*>(w + lay.fault);
   p.row_count = reinterpret_cast<int32_t*>(w + lay.row_count);
-  p.batch_count = reinterpret_cast<int32_t*>(w + lay.batch_count);
-  p.batch_cand = reinterpret_cast<int32_t*>(w + lay.batch_cand);
-  p.batch_commit = reinterpret_cast<int32_t*>(w + lay.batch_commit);
-  p.batch_edit = reinterpret_cast<int32_t*>(w + lay.batch_edit);
+  p.batch_packed = reinterpret_cast<unsigned long long*>(w + lay.batch_packed);
   p.batch_forced = reinterpret_cast<unsigned long long*>(w + lay.batch_forced);
   p.partials = reinterpret_cast<Partial*>(w + lay.partials);
   p.fused = rule ? 1 : 0;
@@ -476,7 +469,7 @@ dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64
   if (!cp) return DLLM_ERR_INVALID_ARGUMENT;
   if (cp->rule < DLLM_RULE_NONE || cp->rule > DLLM_RULE_ENTROPY_BOUND) return DLLM_ERR_INVALID_ARGUMENT;
   if (B * L == 0) return DLLM_OK;
-  if (B > INT32_MAX || L > INT32_MAX) return DLLM_ERR_UNSUPPORTED;
+  if (B > INT32_MAX || L > 65535) return DLLM_ERR_UNSUPPORTED;  // per-batch-row counters are 16-bit
   if (cp->rule != DLLM_RULE_NONE && !cp->commit) return DLLM_ERR_INVALID_ARGUMENT;
   if (cp->rule == DLLM_RULE_TOPK && !cp->k) return DLLM_ERR_INVALID_ARGUMENT;
   if (cp->edit && !cp->edit_mask) return DLLM_ERR_INVALID_ARGUMENT;

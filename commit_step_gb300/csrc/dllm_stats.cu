@@ -44,6 +44,7 @@ struct Acc {
   int32_t idx;      // first index of m among the tail elements (greedy)
   float vm;         // max over the thread's full vectors (greedy)
   int32_t vv;       // first id of the first vector holding vm, -1 if none
+  uint32_t bw[4];   // that vector's sanitized words
   float vm_tail;    // the thread's tail element, if any (greedy)
   float best_s;
   int32_t best_v;
@@ -69,6 +70,7 @@ __device__ __forceinline__ void acc_init(Acc& a) {
   a.idx = 0x7FFFFFFF;
   a.vm = kMInit;
   a.vv = -1;
+  a.bw[0] = a.bw[1] = a.bw[2] = a.bw[3] = 0u;
   a.vm_tail = kMInit;
   a.best_s = kNegInf;
   a.best_v = 0x7FFFFFFF;
@@ -245,17 +247,43 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
 
+// The row's candidate flag and current canvas token, when already loaded.
+struct RowPre {
+  bool have = false;
+  bool cand = false;
+  int32_t tok = 0;
+};
+
+__device__ __forceinline__ RowPre load_row_pre(const StatsParams& p, int64_t row) {
+  RowPre pre;
+  if (!p.fused) return pre;
+  const int64_t b = row / p.L, l = row - b * p.L;
+  pre.cand = is_candidate(p.rule, b, l, &pre.tok);
+  pre.have = true;
+  return pre;
+}
+
+__device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long long* a, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(a), "l"(v) : "memory");
+  return old;
+}
+
 // Writes x0, prob and entropy of one row from its full reduction and, in the
 // fused step, makes the row's own commit / edit decisions.  Run by one thread.
 // Returns the batch row whose sorting rule this CTA must now run, or -1.
 template <bool GUMBEL>
-__device__ int32_t finish_row(const StatsParams& p, int64_t row, const Partial& r) {
+__device__ int32_t finish_row(const StatsParams& p, int64_t row, const Partial& r, RowPre pre) {
   const int32_t x0 = GUMBEL ? r.best_v : r.idx;
   const float zx = GUMBEL ? r.best_z : r.m;
   const float prob = ex2_approx((zx - r.m) * kLog2e) / r.Z;
@@ -269,9 +297,11 @@ __device__ int32_t finish_row(const StatsParams& p, int64_t row, const Partial& 
   const RuleArgs& a = p.rule;
   const int64_t b = row / p.L, l = row - b * p.L;
   const bool per_row = a.rule == kRuleThreshold || a.rule == kRuleNone;
+  unsigned long long inc = 1ull;
   if (per_row) {
-    int32_t tok;
-    const bool cand = is_candidate(a, b, l, &tok);
+    if (!pre.have) pre = load_row_pre(p, row);
+    const bool cand = pre.cand;
+    const int32_t tok = pre.tok;
     const float c = nan_to(prob, kNegInf);
     bool commit = false, edit = false;
     if (a.rule == kRuleThreshold && cand) commit = a.strict ? (c > a.tau) : (c >= a.tau);
@@ -279,22 +309,19 @@ __device__ int32_t finish_row(const StatsParams& p, int64_t row, const Partial& 
     if (a.commit) a.commit[row] = commit ? 1 : 0;
     if (a.edit_mask) a.edit_mask[row] = edit ? 1 : 0;
     if ((commit || edit) && a.canvas) a.canvas[b * a.canvas_stride + a.canvas_offset + l] = x0;
-    if (cand) {
-      atomicAdd(p.batch_cand + b, 1);
-      if (a.rule == kRuleThreshold) atomicMax(p.batch_forced + b, ~desc_key(c, l));
-    }
-    if (commit) atomicAdd(p.batch_commit + b, 1);
-    if (edit) atomicAdd(p.batch_edit + b, 1);
+    if (cand && a.rule == kRuleThreshold) atomicMax(p.batch_forced + b, ~desc_key(c, l));
+    inc |= (cand ? 1ull << 16 : 0ull) | (commit ? 1ull << 32 : 0ull) | (edit ? 1ull << 48 : 0ull);
   }
-  __threadfence();
-  const int32_t old = atomicAdd(p.batch_count + b, 1);
-  if (old != p.L - 1) return -1;
-  __threadfence();
+  // One release-acquire arrival per row: this row's writes become visible to
+  // whichever thread sees the batch row complete.
+  const unsigned long long tot = atom_add_acq_rel(p.batch_packed + b, inc) + inc;
+  if (static_cast<int64_t>(tot & 0xFFFFull) != p.L) return -1;
+  p.batch_packed[b] = 0ull;
   if (!per_row) return static_cast<int32_t>(b);
   // Last row of the batch row: force one commit if candidates exist and none passed.
-  const int32_t n_cand = __ldcg(p.batch_cand + b);
-  int32_t n_commit = __ldcg(p.batch_commit + b);
-  const int32_t n_edit = __ldcg(p.batch_edit + b);
+  const int32_t n_cand = static_cast<int32_t>((tot >> 16) & 0xFFFFull);
+  int32_t n_commit = static_cast<int32_t>((tot >> 32) & 0xFFFFull);
+  const int32_t n_edit = static_cast<int32_t>((tot >> 48) & 0xFFFFull);
   if (a.rule == kRuleThreshold && n_cand > 0 && n_commit == 0) {
     const unsigned long long key = ~__ldcg(p.batch_forced + b);
     const int64_t lf = static_cast<int64_t>(key & 0xFFFFFFFFull);
@@ -302,16 +329,12 @@ __device__ int32_t finish_row(const StatsParams& p, int64_t row, const Partial& 
     if (a.canvas) a.canvas[b * a.canvas_stride + a.canvas_offset + lf] = __ldcg(p.x0 + b * p.L + lf);
     n_commit = 1;
   }
+  if (a.rule == kRuleThreshold) p.batch_forced[b] = 0ull;
   if (a.counts) {
     a.counts[3 * b + 0] = n_cand;
     a.counts[3 * b + 1] = n_commit;
     a.counts[3 * b + 2] = n_edit;
   }
-  p.batch_cand[b] = 0;
-  p.batch_commit[b] = 0;
-  p.batch_edit[b] = 0;
-  p.batch_forced[b] = 0ull;
-  p.batch_count[b] = 0;
   return -1;
 }
 
@@ -343,6 +366,45 @@ __device__ __forceinline__ bool consumer_wait(uint32_t bar, uint32_t parity, vol
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitLimitCycles) return false;
   }
+}
+
+struct VecWords {
+  uint32_t w[4];
+};
+struct GumbelWords {
+  uint32_t w[8];
+};
+
+struct GumbelBest {
+  float s;
+  int32_t v;
+  float z;
+};
+
+// Exact Gumbel scores of the elements of one vector that can still beat
+// max(floor, best.s): each element's own bound z + t (-ln(1 - u)) (plus
+// margin) gates the two logarithms.  Out of line: it runs for few vectors, and
+// keeping it out of the streaming loop keeps that loop small.
+template <bool BF16>
+__device__ __noinline__ GumbelBest gumbel_exact(GumbelBest best, VecWords vw, GumbelWords r, int32_t v0, float t,
+                                                float t_ln2, float floor) {
+  constexpr int EPV = BF16 ? 8 : 4;
+#pragma unroll 1
+  for (int e = 0; e < EPV; ++e) {
+    const uint32_t word = vw.w[BF16 ? (e >> 1) : e];
+    const float z = BF16 ? ((e & 1) ? bf16hi(word) : bf16lo(word)) : __uint_as_float(word);
+    const uint32_t re = r.w[e];
+    const float w1 = __fsub_rn(1.0f, uniform_from_bits(re));
+    const float bound = fmaf(t_ln2, -lg2_approx(w1), z + fmaf(fabsf(z), 1e-6f, 1e-3f));
+    if (bound < floor || bound < best.s) continue;
+    const float sc = gumbel_score(z, t, re);
+    if (sc > best.s) {
+      best.s = sc;
+      best.v = v0 + e;
+      best.z = z;
+    }
+  }
+  return best;
 }
 
 // Consumer-side state of one CTA.
@@ -377,17 +439,30 @@ struct Consumer {
 
   // Reduces one unit: nv (<= 1024) vectors in the ring stage at shared
   // address `base`, the first being vector v_unit of global row `row`.
-  // Thread tid holds vectors tid, tid + 256, ...: all its loads are issued
-  // first, the unit's max comes from one max tree (bf16x2 for bf16), the
-  // running state is rescaled at most once, and the sums run on two
-  // independent accumulator pairs.
-  __device__ void unit(uint32_t base, int64_t row, int64_t v_unit, int64_t nv, bool unit_has_sup) {
-    uint32_t w[kVPT][4];
-    bool valid[kVPT];
+  // Dispatches to a version specialised on the vectors each thread holds.
+  __device__ __forceinline__ void unit(uint32_t base, int64_t row, int64_t v_unit, int64_t nv, bool unit_has_sup) {
+    const int32_t vu = static_cast<int32_t>(v_unit);
+    if (nv == p.chunk_vec) {
+      if (p.chunk_vec == 1024) return unit_t<4, true>(base, row, vu, static_cast<int32_t>(nv), unit_has_sup);
+      if (p.chunk_vec == 512) return unit_t<2, true>(base, row, vu, static_cast<int32_t>(nv), unit_has_sup);
+      return unit_t<1, true>(base, row, vu, static_cast<int32_t>(nv), unit_has_sup);
+    }
+    unit_t<kVPT, false>(base, row, vu, static_cast<int32_t>(nv), unit_has_sup);
+  }
+
+  // Thread tid holds vectors tid, tid + 256, ... (NPT of them; FULL: all of
+  // them exist).  All loads are issued first, the unit's max comes from one
+  // max tree (bf16x2 for bf16), the running state is rescaled once without
+  // branching, and the sums run on two independent accumulator pairs.
+  template <int NPT, bool FULL>
+  __device__ __forceinline__ void unit_t(uint32_t base, int64_t row, int32_t v_unit, int32_t nv,
+                                         bool unit_has_sup) {
+    uint32_t w[NPT][4];
+    bool valid[NPT];
 #pragma unroll
-    for (int j = 0; j < kVPT; ++j) {
-      const int64_t vi = static_cast<int64_t>(j) * kConsumers + tid;
-      valid[j] = vi < nv;
+    for (int j = 0; j < NPT; ++j) {
+      const int32_t vi = j * kConsumers + tid;
+      valid[j] = FULL || vi < nv;
       const uint4 q = valid[j] ? lds128(base + static_cast<uint32_t>(vi) * 16u)
                                : make_uint4(kAbsentWord, kAbsentWord, kAbsentWord, kAbsentWord);
       w[j][0] = q.x;
@@ -398,15 +473,16 @@ struct Consumer {
     // NaN and values <= -2^100 -> -2^100 (the top clamp is applied below,
     // only when the unit holds a value above 2^100).
 #pragma unroll
-    for (int j = 0; j < kVPT; ++j)
+    for (int j = 0; j < NPT; ++j)
 #pragma unroll
       for (int k = 0; k < 4; ++k) w[j][k] = BF16 ? bmax2(w[j][k], kSentinelBf16x2) : sanitize_low_bits(w[j][k]);
+    const int32_t id0 = (v_unit + tid) * EPV;  // first id of vector j = 0; vector j adds j * 256 * EPV
     if (unit_has_sup) {
 #pragma unroll
-      for (int j = 0; j < kVPT; ++j) {
-        const int64_t v0 = (v_unit + static_cast<int64_t>(j) * kConsumers + tid) * EPV;
+      for (int j = 0; j < NPT; ++j) {
+        const int32_t v0 = id0 + j * kConsumers * EPV;
         for (int s = 0; s < p.n_sup; ++s) {
-          const int64_t off = p.sup[s] - v0;
+          const int32_t off = p.sup[s] - v0;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (BF16) {
@@ -419,16 +495,15 @@ struct Consumer {
         }
       }
     }
-    // per-vector and unit maxima
-    float vmax[kVPT];
+    float vmax[NPT];
 #pragma unroll
-    for (int j = 0; j < kVPT; ++j) vmax[j] = valid[j] ? vector_max(w[j]) : kMInit;
+    for (int j = 0; j < NPT; ++j) vmax[j] = valid[j] ? vector_max(w[j]) : kMInit;
     float umax = vmax[0];
 #pragma unroll
-    for (int j = 1; j < kVPT; ++j) umax = fmaxf(umax, vmax[j]);
+    for (int j = 1; j < NPT; ++j) umax = fmaxf(umax, vmax[j]);
     if (umax > kTopClamp) {  // rare: +inf or huge logits count as 2^100
 #pragma unroll
-      for (int j = 0; j < kVPT; ++j) {
+      for (int j = 0; j < NPT; ++j) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) w[j][k] = BF16 ? bmin2(w[j][k], kTopBf16x2) : clamp_top_bits(w[j][k]);
         vmax[j] = fminf(vmax[j], kTopClamp);
@@ -437,13 +512,15 @@ struct Consumer {
     }
     if (!GUMBEL) {
       // The first vector holding this thread's max (ids increase with j and
-      // from unit to unit, so a strict > keeps the earliest).  The element
-      // inside it is located once per row, in resolve_index().
+      // from unit to unit, so a strict > keeps the earliest), kept with its
+      // words; the element inside it is located once per row.
 #pragma unroll
-      for (int j = 0; j < kVPT; ++j) {
+      for (int j = 0; j < NPT; ++j) {
         const bool better = vmax[j] > acc.vm;
         acc.vm = better ? vmax[j] : acc.vm;
-        acc.vv = better ? static_cast<int32_t>((v_unit + static_cast<int64_t>(j) * kConsumers + tid) * EPV) : acc.vv;
+        acc.vv = better ? id0 + j * kConsumers * EPV : acc.vv;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc.bw[k] = better ? w[j][k] : acc.bw[k];
       }
     }
     // Branch-free rescale to the new running max (factor 1 when it did not grow).
@@ -460,8 +537,8 @@ struct Consumer {
     const uint64_t negm2 = pack2(acc.negm, acc.negm);
     uint64_t Zb = 0, Sb = 0;
 #pragma unroll
-    for (int j = 0; j < kVPT; ++j) {
-      if (!valid[j]) continue;
+    for (int j = 0; j < NPT; ++j) {
+      if (!FULL && !valid[j]) continue;
 #pragma unroll
       for (int e = 0; e < EPV; e += 4) {
         acc_pair2(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), negm2);
@@ -472,49 +549,49 @@ struct Consumer {
     acc.S2 = add2(acc.S2, Sb);
 
     if (GUMBEL) {
-      bool updated = false;
+      const uint32_t row_lo = static_cast<uint32_t>(row);
+      const uint32_t row_hi = static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32);
 #pragma unroll
-      for (int j = 0; j < kVPT; ++j) {
-        const int64_t v0 = (v_unit + static_cast<int64_t>(j) * kConsumers + tid) * EPV;
+      for (int j = 0; j < NPT; ++j) {
+        const int32_t v0 = id0 + j * kConsumers * EPV;
         // Philox words of ids v0 .. v0 + EPV - 1 (v0 is a multiple of 4)
-        uint32_t r[EPV];
-        const uint32_t row_lo = static_cast<uint32_t>(row);
-        const uint32_t row_hi = static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32);
+        GumbelWords r;
 #pragma unroll
         for (int h = 0; h < EPV / 4; ++h) {
-          const uint4 o = philox4x32_10(static_cast<uint32_t>((v0 >> 2) + h), row_lo, row_hi, 0u, p.key);
-          r[4 * h + 0] = o.x;
-          r[4 * h + 1] = o.y;
-          r[4 * h + 2] = o.z;
-          r[4 * h + 3] = o.w;
+          const uint4 o = philox4x32_10(static_cast<uint32_t>(v0 >> 2) + h, row_lo, row_hi, 0u, p.key);
+          r.w[4 * h + 0] = o.x;
+          r.w[4 * h + 1] = o.y;
+          r.w[4 * h + 2] = o.z;
+          r.w[4 * h + 3] = o.w;
         }
-        uint32_t rmax = r[0];
+        uint32_t rmax = r.w[0];
 #pragma unroll
-        for (int e = 1; e < EPV; ++e) rmax = max(rmax, r[e]);
+        for (int e = 1; e < EPV; ++e) rmax = max(rmax, r.w[e]);
         // g = -ln(-ln u) <= -ln(1 - u) for every id of the vector; the margin
         // covers the fp32 rounding of ln_p, lg2.approx and the final fmaf.
         const float w1 = __fsub_rn(1.0f, uniform_from_bits(rmax));
-        const float gbound = -lg2_approx(w1);
-        const float bound = fmaf(t_ln2, gbound, vmax[j] + fmaf(fabsf(vmax[j]), 1e-6f, 1e-3f));
-        if (valid[j] && !(bound < warp_best)) {
+        const float bound = fmaf(t_ln2, -lg2_approx(w1), vmax[j] + fmaf(fabsf(vmax[j]), 1e-6f, 1e-3f));
+        const bool survive = (FULL || valid[j]) && !(bound < warp_best);
+        if (__any_sync(0xFFFFFFFFu, survive)) {
+          bool updated = false;
+          if (survive) {
+            VecWords vw;
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const float z = elem(w[j], e);
-            const float sc = gumbel_score(z, t, r[e]);
-            if (sc > acc.best_s) {
-              acc.best_s = sc;
-              acc.best_v = static_cast<int32_t>(v0 + e);
-              acc.best_z = z;
-              updated = true;
-            }
+            for (int k = 0; k < 4; ++k) vw.w[k] = w[j][k];
+            GumbelBest b{acc.best_s, acc.best_v, acc.best_z};
+            b = gumbel_exact<BF16>(b, vw, r, v0, t, t_ln2, warp_best);
+            updated = b.s > acc.best_s;
+            acc.best_s = b.s;
+            acc.best_v = b.v;
+            acc.best_z = b.z;
+          }
+          if (__any_sync(0xFFFFFFFFu, updated)) {
+            float wb = acc.best_s;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, o));
+            warp_best = fmaxf(warp_best, wb);
           }
         }
-      }
-      if (__any_sync(0xFFFFFFFFu, updated)) {
-        float wb = acc.best_s;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, o));
-        warp_best = fmaxf(warp_best, wb);
       }
     }
   }
@@ -572,34 +649,15 @@ struct Consumer {
   }
 
   // Greedy x0 bookkeeping: the first id holding this thread's max acc.m.  It
-  // is in the best full vector (ids below every tail element) unless the tail
-  // element is larger; the vector is read once more from global memory (an
-  // L2 hit) and sanitized exactly as when it was streamed.
-  __device__ void resolve_index(int64_t row) {
+  // is in the best full vector (whose sanitized words the thread kept; its
+  // ids are below every tail element) unless the tail element is larger.
+  __device__ void resolve_index() {
     if (GUMBEL) return;
     int32_t idx = 0x7FFFFFFF;
     if (acc.vv >= 0 && acc.vm == acc.m) {
-      const uint8_t* rowp = p.logits + row * p.row_bytes;
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(rowp + static_cast<int64_t>(acc.vv) * (BF16 ? 2 : 4)));
-      uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        w[k] = BF16 ? bmin2(bmax2(w[k], kSentinelBf16x2), kTopBf16x2) : clamp_top_bits(sanitize_low_bits(w[k]));
-      for (int s = 0; s < p.n_sup; ++s) {
-        const int64_t off = p.sup[s] - acc.vv;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (BF16) {
-            if (off == 2 * k) w[k] = (w[k] & 0xFFFF0000u) | kAbsentBf16;
-            if (off == 2 * k + 1) w[k] = (w[k] & 0x0000FFFFu) | (kAbsentBf16 << 16);
-          } else if (off == k) {
-            w[k] = __float_as_uint(kAbsent);
-          }
-        }
-      }
 #pragma unroll
       for (int e = EPV - 1; e >= 0; --e)
-        if (elem(w, e) == acc.vm) idx = acc.vv + e;
+        if (elem(acc.bw, e) == acc.vm) idx = acc.vv + e;
     } else if (acc.vm_tail == acc.m && acc.m > kMInit) {
       idx = acc.idx;
     }
@@ -618,9 +676,15 @@ struct Consumer {
     Partial part = warp_combine<GUMBEL>(acc_to_partial(acc));
     if (lane == 0) ctl.warp_part[warp] = part;
     named_sync(1, kConsumers);
-    Partial r = ctl.warp_part[0];
-    if (tid == 0)
-      for (int w = 1; w < kConsumerWarps; ++w) part_combine<GUMBEL>(r, ctl.warp_part[w]);
+    Partial r = empty_partial();
+    if (warp == 0) {
+      if (lane < kConsumerWarps) r = ctl.warp_part[lane];
+#pragma unroll
+      for (int o = kConsumerWarps / 2; o > 0; o >>= 1) {
+        const Partial q = shfl_partial<GUMBEL>(r, o);
+        part_combine<GUMBEL>(r, q);
+      }
+    }
     return r;
   }
 
@@ -635,7 +699,6 @@ struct Consumer {
     rs.cap = kFusedSortCap;
     __threadfence();
     run_rule<kConsumers, 1>(p.rule, b, rs, tid);
-    if (tid == 0) p.batch_count[b] = 0;
   }
 };
 
@@ -778,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
       pdl_wait();  // nothing is written before the previous kernel has finished
       waited = true;
     }
-    con.resolve_index(row);
+    con.resolve_index();
     const Partial r = con.cta_reduce();
     if (tid == 0) {
       int32_t action = 0;  // 0 nothing, 1 finish r, 2 combine the row's partials
@@ -819,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
         ctl.result = tot;
       }
     }
-    if (tid == 0) ctl.flag2 = action != 0 ? finish_row<GUMBEL>(p, row, ctl.result) : -1;
+    if (tid == 0) ctl.flag2 = action != 0 ? finish_row<GUMBEL>(p, row, ctl.result, RowPre()) : -1;
     named_sync(1, kConsumers);
     con.rule_if_needed(ctl.flag2, rule_smem);
     first_segment = false;
@@ -891,11 +954,19 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
     }
     __syncwarp();
     cluster_sync_all();  // partials published
-    cluster_sync_all();  // rank 0 has read them
+    // second barrier: rank 0 has read them (rank 0 itself only arrives)
+    if (rank == 0)
+      cluster_arrive();
+    else
+      cluster_sync_all();
     return;
   }
 
   Consumer<BF16, GUMBEL> con(p, ctl, ring, chunk_bytes);
+  // Rank 0 finishes the row; its candidate flag and canvas token are loaded
+  // now so they are at hand then (after the grid dependency in early mode).
+  RowPre pre;
+  if (rank == 0 && tid == 0 && !p.early) pre = load_row_pre(p, row);
   RingPos rc;
   for (int64_t i = 0; i < n_units; ++i) {
     const int64_t v_unit = vb + i * p.chunk_vec;
@@ -909,23 +980,33 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
     rc.advance(p.stages);
   }
   if (rank == static_cast<uint32_t>(S - 1) && !ctl.abort_flag) con.tail(row);
-  con.resolve_index(row);
+  con.resolve_index();
+  if (rank == 0 && p.early) {
+    pdl_wait();  // nothing is written, nor the canvas read, before the previous kernel ends
+    if (tid == 0) pre = load_row_pre(p, row);
+  }
   const Partial r = con.cta_reduce();
   if (tid == 0) ctl.result = r;
   __syncwarp();
   cluster_sync_all();
   if (rank == 0) {
-    if (p.early) pdl_wait();
-    if (warp == 0) {
-      Partial tot = empty_partial();
+    // Read the cluster's partials, then release the other CTAs at once (they
+    // exit and free their SM slots while rank 0 finishes the row).
+    Partial tot = empty_partial();
+    if (warp == 0)
       for (int k = lane; k < S; k += 32) part_combine<GUMBEL>(tot, load_partial_dsmem(&ctl.result, k));
+    __syncwarp();
+    cluster_arrive();
+    if (warp == 0) {
       tot = warp_combine<GUMBEL>(tot);
-      if (lane == 0) rule_b = ctl.abort_flag ? -1 : finish_row<GUMBEL>(p, row, tot);
+      if (lane == 0) rule_b = ctl.abort_flag ? -1 : finish_row<GUMBEL>(p, row, tot, pre);
     }
+  } else {
+    __syncwarp();
+    cluster_sync_all();
+    return;
   }
-  __syncwarp();
-  cluster_sync_all();
-  if (rank == 0) {
+  {
     if (tid == 0) ctl.flag2 = rule_b;
     named_sync(1, kConsumers);
     con.rule_if_needed(ctl.flag2, dsmem + static_cast<size_t>(p.stages) * chunk_bytes);

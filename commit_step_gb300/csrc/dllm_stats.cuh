@@ -51,10 +51,8 @@ struct StatsParams {
   float* entropy;
   int32_t* fault;
   int32_t* row_count;       // (T) contributions that arrived, split rows only
-  int32_t* batch_count;     // (B) rows finished, fused rule only
-  int32_t* batch_cand;      // (B) candidates seen (per-row threshold decisions)
-  int32_t* batch_commit;    // (B) commits made
-  int32_t* batch_edit;      // (B) edits made
+  // (B) per batch row, four 16-bit fields: rows finished | candidates | commits | edits
+  unsigned long long* batch_packed;
   unsigned long long* batch_forced;  // (B) max of ~ranking key over candidates: the forced commit
   Partial* partials;        // (2 P)
   int32_t fused;

@@ -204,8 +204,8 @@ dllm_status dllm_block_ranges(int64_t P, int64_t gen_len, int64_t block_len, int
  * optional edit rule and canvas update) in one launch.  The rule of batch
  * row b runs as soon as its L rows' statistics are complete, inside the same
  * kernel ([MOJO] spec "possible future fused kernel": softmax, entropy and
- * confidence, top-k, sample, scatter).  Requires L <= 1024 for the sorting
- * rules.
+ * confidence, top-k, sample, scatter).  Requires L <= 65535, and L <= 1024
+ * for the sorting rules (else DLLM_ERR_UNSUPPORTED).
  * ------------------------------------------------------------------------ */
 typedef enum {
   DLLM_RULE_NONE = 0,

@@ -227,8 +227,15 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   p.P = pl.P;
   p.stages = pl.stages;
   p.temperature = temperature;
-  p.key.k0 = static_cast<uint32_t>(key);
-  p.key.k1 = static_cast<uint32_t>(key >> 32);
+  {
+    uint32_t k0 = static_cast<uint32_t>(key), k1 = static_cast<uint32_t>(key >> 32);
+    for (int r = 0; r < 10; ++r) {
+      p.keys.k[r][0] = k0;
+      p.keys.k[r][1] = k1;
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+  }
   p.n_sup = static_cast<int32_t>(sup.size());
   for (size_t i = 0; i < sup.size(); ++i) p.sup[i] = sup[i];
   p.ln_veff = static_cast<float>(std::log(static_cast<double>(V - static_cast<int64_t>(sup.size()))));

@@ -25,6 +25,12 @@ struct PhiloxKey {
   uint32_t k0, k1;
 };
 
+// The key of each of the ten rounds: round i uses (k0 + i 0x9E3779B9,
+// k1 + i 0xBB67AE85) mod 2^32.  Computed once per launch on the host.
+struct PhiloxSchedule {
+  uint32_t k[10][2];
+};
+
 __device__ __forceinline__ void mulhilo(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo) {
   uint64_t p;
   asm("mul.wide.u32 %0, %1, %2;" : "=l"(p) : "r"(a), "r"(b));
@@ -32,23 +38,20 @@ __device__ __forceinline__ void mulhilo(uint32_t a, uint32_t b, uint32_t& hi, ui
   hi = static_cast<uint32_t>(p >> 32);
 }
 
-// Ten Philox rounds on (c0, c1, c2, c3); the key advances by the Weyl
-// increments (0x9E3779B9, 0xBB67AE85) between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, PhiloxKey key) {
-  uint32_t k0 = key.k0, k1 = key.k1;
+// Ten Philox rounds on (c0, c1, c2, c3) with a precomputed key schedule.
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                               const PhiloxSchedule& ks) {
 #pragma unroll
   for (int round = 0; round < 10; ++round) {
     uint32_t hi0, lo0, hi1, lo1;
     mulhilo(0xD2511F53u, c0, hi0, lo0);
     mulhilo(0xCD9E8D57u, c2, hi1, lo1);
-    const uint32_t n0 = hi1 ^ c1 ^ k0;
-    const uint32_t n2 = hi0 ^ c3 ^ k1;
+    const uint32_t n0 = hi1 ^ c1 ^ ks.k[round][0];
+    const uint32_t n2 = hi0 ^ c3 ^ ks.k[round][1];
     c0 = n0;
     c1 = lo1;
     c2 = n2;
     c3 = lo0;
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
   }
   return make_uint4(c0, c1, c2, c3);
 }

@@ -354,6 +354,7 @@ struct SharedCtl {
   int32_t abort_flag;
   int32_t flag;
   int32_t flag2;
+  uint32_t cta_best;   // running best Gumbel score of the CTA's current row (order-preserving bits)
 };
 
 // Bounded wait used by the consumers: sleeps in hardware until the copy
@@ -429,6 +430,8 @@ struct Consumer {
     reset();
   }
 
+  // Per-row reset of the thread's state (the CTA-wide best is cleared at the
+  // start of the kernel and at the end of every flush, before a barrier).
   __device__ void reset() {
     acc_init(acc);
     warp_best = kNegInf;
@@ -551,49 +554,73 @@ struct Consumer {
     if (GUMBEL) {
       const uint32_t row_lo = static_cast<uint32_t>(row);
       const uint32_t row_hi = static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32);
+      // The pruning floor: the best score any warp of the CTA has seen in
+      // this row (a lower bound of the row's winning score).
+      warp_best = fmaxf(warp_best, key_float(*reinterpret_cast<volatile uint32_t*>(&ctl.cta_best)));
+      constexpr int PAIR = NPT >= 2 ? 2 : 1;
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        const int32_t v0 = id0 + j * kConsumers * EPV;
-        // Philox words of ids v0 .. v0 + EPV - 1 (v0 is a multiple of 4)
-        GumbelWords r;
+      for (int j0 = 0; j0 < NPT; j0 += PAIR) {
+        GumbelWords r[PAIR];
+        bool survive[PAIR];
+        // Philox words of the vectors j0 .. j0 + PAIR - 1, generated together
 #pragma unroll
-        for (int h = 0; h < EPV / 4; ++h) {
-          const uint4 o = philox4x32_10(static_cast<uint32_t>(v0 >> 2) + h, row_lo, row_hi, 0u, p.key);
-          r.w[4 * h + 0] = o.x;
-          r.w[4 * h + 1] = o.y;
-          r.w[4 * h + 2] = o.z;
-          r.w[4 * h + 3] = o.w;
-        }
-        uint32_t rmax = r.w[0];
+        for (int q = 0; q < PAIR; ++q) {
+          const int32_t v0 = id0 + (j0 + q) * kConsumers * EPV;
 #pragma unroll
-        for (int e = 1; e < EPV; ++e) rmax = max(rmax, r.w[e]);
-        // g = -ln(-ln u) <= -ln(1 - u) for every id of the vector; the margin
-        // covers the fp32 rounding of ln_p, lg2.approx and the final fmaf.
-        const float w1 = __fsub_rn(1.0f, uniform_from_bits(rmax));
-        const float bound = fmaf(t_ln2, -lg2_approx(w1), vmax[j] + fmaf(fabsf(vmax[j]), 1e-6f, 1e-3f));
-        const bool survive = (FULL || valid[j]) && !(bound < warp_best);
-        if (__any_sync(0xFFFFFFFFu, survive)) {
-          bool updated = false;
-          if (survive) {
-            VecWords vw;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) vw.w[k] = w[j][k];
-            GumbelBest b{acc.best_s, acc.best_v, acc.best_z};
-            b = gumbel_exact<BF16>(b, vw, r, v0, t, t_ln2, warp_best);
-            updated = b.s > acc.best_s;
-            acc.best_s = b.s;
-            acc.best_v = b.v;
-            acc.best_z = b.z;
+          for (int h = 0; h < EPV / 4; ++h) {
+            const uint4 o = philox4x32_10(static_cast<uint32_t>(v0 >> 2) + h, row_lo, row_hi, 0u, p.keys);
+            r[q].w[4 * h + 0] = o.x;
+            r[q].w[4 * h + 1] = o.y;
+            r[q].w[4 * h + 2] = o.z;
+            r[q].w[4 * h + 3] = o.w;
           }
-          if (__any_sync(0xFFFFFFFFu, updated)) {
-            float wb = acc.best_s;
+        }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, o));
-            warp_best = fmaxf(warp_best, wb);
+        for (int q = 0; q < PAIR; ++q) {
+          const int j = j0 + q;
+          uint32_t rmax = r[q].w[0];
+#pragma unroll
+          for (int e = 1; e < EPV; ++e) rmax = max(rmax, r[q].w[e]);
+          // g = -ln(-ln u) <= -ln(1 - u) for every id of the vector; the
+          // margin covers the fp32 rounding of ln_p, lg2.approx and the fmaf.
+          const float w1 = __fsub_rn(1.0f, uniform_from_bits(rmax));
+          const float bound = fmaf(t_ln2, -lg2_approx(w1), vmax[j] + fmaf(fabsf(vmax[j]), 1e-6f, 1e-3f));
+          survive[q] = (FULL || valid[j]) && !(bound < warp_best);
+        }
+#pragma unroll
+        for (int q = 0; q < PAIR; ++q) {
+          const int j = j0 + q;
+          if (__any_sync(0xFFFFFFFFu, survive[q])) {
+            bool updated = false;
+            if (survive[q]) {
+              VecWords vw;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) vw.w[k] = w[j][k];
+              GumbelBest b{acc.best_s, acc.best_v, acc.best_z};
+              b = gumbel_exact<BF16>(b, vw, r[q], id0 + j * kConsumers * EPV, t, t_ln2, warp_best);
+              updated = b.s > acc.best_s;
+              acc.best_s = b.s;
+              acc.best_v = b.v;
+              acc.best_z = b.z;
+            }
+            if (__any_sync(0xFFFFFFFFu, updated)) {
+              float wb = acc.best_s;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, o));
+              if (wb > warp_best) {
+                warp_best = wb;
+                if (lane == 0) atomicMax(&ctl.cta_best, float_key(wb));
+              }
+            }
           }
         }
       }
     }
+  }
+
+  __device__ __forceinline__ static float key_float(uint32_t k) {
+    // inverse of float_key
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
   }
 
   // Element e of a 16-byte vector held as four 32-bit words.
@@ -636,7 +663,7 @@ struct Consumer {
     acc.S2 = fma2(pack2(e, 0.0f), pack2(y, 0.0f), acc.S2);
     if (GUMBEL) {
       const uint4 o = philox4x32_10(static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(row),
-                                    static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32), 0u, p.key);
+                                    static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32), 0u, p.keys);
       const int w = static_cast<int>(v & 3);
       const uint32_t word = w == 0 ? o.x : (w == 1 ? o.y : (w == 2 ? o.z : o.w));
       const float s = gumbel_score(z, t, word);
@@ -768,6 +795,7 @@ __device__ __forceinline__ void init_barriers(SharedCtl& ctl, int stages) {
       mbar_init(smem_addr(&ctl.empty[s]), kConsumerWarps);
     }
     ctl.abort_flag = 0;
+    ctl.cta_best = float_key(-__int_as_float(0x7F800000));
     fence_mbar_init();
   }
 }
@@ -882,7 +910,10 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
         ctl.result = tot;
       }
     }
-    if (tid == 0) ctl.flag2 = action != 0 ? finish_row<GUMBEL>(p, row, ctl.result, RowPre()) : -1;
+    if (tid == 0) {
+      ctl.flag2 = action != 0 ? finish_row<GUMBEL>(p, row, ctl.result, RowPre()) : -1;
+      ctl.cta_best = float_key(kNegInf);  // the next row starts with no pruning floor
+    }
     named_sync(1, kConsumers);
     con.rule_if_needed(ctl.flag2, rule_smem);
     first_segment = false;

@@ -42,7 +42,7 @@ struct StatsParams {
   int32_t P;                // CTAs in the grid
   int32_t stages;           // ring stages
   float temperature;
-  PhiloxKey key;
+  PhiloxSchedule keys;      // Philox round keys of the caller's key
   int32_t n_sup;
   int32_t sup[DLLM_MAX_SUPPRESS];  // sorted, distinct
   float ln_veff;

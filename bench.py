@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="llada", choices=["llada", "tiny", "dream", "large"])
+    ap.add_argument("--workload", default="llada", choices=["llada", "tiny", "dream", "large", "loop"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -428,6 +428,54 @@ def run_ours(args, rank, world):
     return res, w
 
 
+def run_loop(args, rank, world):
+    """The block-decode loop workload: B=4, P=128, gen_len=1024, block_len=32,
+    V=126464 bf16, strict threshold 0.95 then editing 0.9, max_post_steps=4;
+    a seeded generator emits each step's block rows.  Reports the commit
+    steps' GB/s and canvas positions per second (B * gen_len / the summed GPU
+    time of the commit steps)."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import commit_step_gb300 as cs
+    from commit_step_gb300.decode import decode_with_editing
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    spec = W.loop_spec()
+    gen = W.LoopGenerator(spec)
+    prompt = torch.from_numpy(gen.prompt).to(dev)
+    model = lambda bi, st, c0, n: gen.device_logits(bi, st, c0, n)
+    kw = dict(gen_len=spec.gen_len, block_len=spec.block_len, mask_id=spec.mask_id, threshold=spec.tau,
+              editing_threshold=spec.tau_edit, max_post_steps=spec.max_post_steps, suppress_ids=[spec.mask_id])
+    decode_with_editing(model, prompt, **kw)               # warm-up pass
+    times, trace = [], []
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_query_id(torch.cuda.get_device_properties(dev), dev.index)) as clk:
+        out, forwards = decode_with_editing(model, prompt, step_times=times, trace=trace, **kw)
+    total_ms = float(sum(times))
+    rows_per_step = spec.B * spec.block_len
+    bytes_per_step = rows_per_step * (spec.V * 2 + 18)
+    peak, peak_kind = measured_peaks()
+    value = bytes_per_step * forwards / (total_ms / 1e3) / 1e9 * world
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": forwards, "warmup": 1,
+        "ms_per_step": total_ms / forwards, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded generator, dllm_workloads.py)",
+        "config": {"workload": "loop: B=4, P=128, gen_len=1024, block_len=32 (aligned), V=126464 bf16, strict "
+                               "threshold 0.95 then edit 0.9, max_post_steps=4",
+                   "global_batch": spec.B * world, "seq_len": spec.block_len, "vocab": spec.V,
+                   "parallelism": f"replicas x{world}", "l2": "per-step rows are written by the generator just before"
+                                                              " the step (L2-warm, as in a real loop)"},
+        "positions_per_s": round(spec.B * spec.gen_len * world / (total_ms / 1e3), 1),
+        "forwards": forwards, "commits": int(sum(t[2] for t in trace)), "edits": int(sum(t[3] for t in trace)),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 1),
+        "gpu_launches": forwards, "clocks": clk.summary(),
+    }
+
+
 def run_reference(args, rank, world):
     w = W.build(args.workload)
     steps = args.steps if args.steps is not None else 3
@@ -470,6 +518,11 @@ def main():
 
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
+    if args.workload == "loop":
+        res = run_loop(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res))
+        return 0
     res, w = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline and not args.profile:

@@ -1,0 +1,73 @@
+"""Block decoding with token editing on the GPU, built on the fused commit step.
+
+Follows the loop of the mlx-arsenal "dLLM block decoding" notes, section
+"Token editing (LLaDA2.1)": whole blocks aligned on absolute positions; at
+each step the block's masked positions are the candidates of a strict
+threshold commit and its other generated positions may be edited; a block
+ends after a step with no mask and no edit, or once more than
+``max_post_steps`` extra passes ran on a full block; batch rows share the
+termination.  Each step is one fused launch (statistics, threshold, edit and
+canvas update) plus one read of three counters per batch row.
+
+The caller's ``model(block_index, step_in_block, col0, n_cols)`` returns the
+(B * n_cols, V) logits of canvas columns [col0, col0 + n_cols) on the device.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import RULE_THRESHOLD, block_ranges, commit_step
+
+
+def decode_with_editing(model, prompt: torch.Tensor, *, gen_len: int, block_len: int, mask_id: int,
+                        threshold: float = 0.95, editing_threshold: float = 0.9, max_post_steps: int = 16,
+                        suppress_ids=(), step_times=None, trace=None):
+    """Returns (generated tokens (B, gen_len), number of forwards).
+
+    ``step_times``: optional list receiving the GPU time (ms) of each fused
+    commit step, measured with CUDA events on the current stream.
+    """
+    dev = prompt.device
+    B, P = prompt.shape
+    total = -(-(P + gen_len) // block_len) * block_len
+    x = torch.full((B, total), mask_id, dtype=torch.int32, device=dev)
+    x[:, :P] = prompt.to(torch.int32)
+    counts = torch.zeros((B, 3), dtype=torch.int32, device=dev)
+    counts_host = torch.zeros((B, 3), dtype=torch.int32).pin_memory()
+    forwards = 0
+    for bi, (start, end) in enumerate(block_ranges(P, total - P, block_len, align=True)):
+        lo = max(start, P)
+        n = end - lo
+        if n <= 0:
+            continue
+        has_mask = bool((x[:, lo:end] == mask_id).any().item())
+        post_steps = 0
+        step = 0
+        while True:
+            if not has_mask:
+                post_steps += 1
+                if post_steps > max_post_steps:
+                    break
+            logits = model(bi, step, lo, n).view(B, n, -1)
+            if step_times is not None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            commit_step(logits, rule=RULE_THRESHOLD, tau=threshold, strict=True, suppress_ids=suppress_ids,
+                        mask_id=mask_id, edit=True, tau_edit=editing_threshold, canvas=x, canvas_offset=lo,
+                        counts=counts)
+            if step_times is not None:
+                e1.record()
+            forwards += 1
+            counts_host.copy_(counts)          # the one host read of the step
+            c = counts_host.numpy()
+            if step_times is not None:
+                step_times.append(e0.elapsed_time(e1))
+            n_commit, n_edit = int(c[:, 1].sum()), int(c[:, 2].sum())
+            if trace is not None:
+                trace.append((bi, step, n_commit, n_edit))
+            masked_after = int((c[:, 0] - c[:, 1]).sum())
+            step += 1
+            if not has_mask and n_edit == 0:
+                break
+            has_mask = masked_after > 0
+    return x[:, P:P + gen_len], forwards

@@ -174,6 +174,25 @@ def recorded_traffic(workload: str):
 
 
 # --------------------------------------------------------------------------
+# multi-rank timing: each rank times its own replica; the job takes the max
+# --------------------------------------------------------------------------
+def max_over_ranks(ms: float, device, world: int) -> float:
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Bytes every rank processed, over the slowest rank's time."""
+    return bytes_per_step * steps * world / (max_ms / 1e3) / 1e9
+
+
+# --------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, on a bounded sample of the workload
 # --------------------------------------------------------------------------
 def oracle_step(w, logits=None):
@@ -324,13 +343,7 @@ def run_ours(args, rank, world):
         e1.record(stream)
         e1.synchronize()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dev, world)
     ms_per_step = ms / steps_done
 
     # the same steps as a dependent chain (each waits for the previous kernel)
@@ -392,8 +405,7 @@ def run_ours(args, rank, world):
     ok = cs.workspace_fault(ws)
 
     alg = algorithmic_bytes(w)
-    world_bytes = alg * steps_done * world
-    value = world_bytes / (ms / 1e3) / 1e9
+    value = whole_job_gbs(alg, steps_done, world, ms)
     peak, peak_kind = measured_peaks()
     kernel_ms = ms_per_step / launches_per_step if launches_per_step == 1 else ms_per_step
     achieved = alg / (kernel_ms / 1e3) / 1e9

@@ -121,18 +121,21 @@ int chunk_for(int64_t vectors_per_cta) {
 // Few rows: one cluster of S CTAs per row, the largest S whose whole grid is
 // co-resident (one wave) and leaves each CTA at least 128 vectors.  Many
 // rows: the persistent grid over equal unit ranges.
-StatsPlan plan_stats(const DeviceInfo& d, int variant, int64_t T, int64_t V, int esize) {
+StatsPlan plan_stats(const DeviceInfo& d, int variant, int64_t T, int64_t V, int esize, bool overlap) {
   StatsPlan pl{};
   pl.nvec = (V * esize) / 16;
   pl.tail = static_cast<int32_t>(V - pl.nvec * (16 / esize));
+  // A call that overlaps the previous launch (DLLM_FLAG_INPUTS_READY) sizes
+  // its cluster grid to half the co-resident CTAs, so two steps stream at once.
   const int ctas = d.sms * d.occ[variant];
+  const int cluster_ctas = overlap ? std::max(1, ctas / 4) : ctas;
   for (int e = 4; e >= 1; --e) {
     const int S = 1 << e;
-    if (T <= d.clusters[variant][e] && T * S <= ctas && pl.nvec >= static_cast<int64_t>(S) * 128) {
+    if (T <= d.clusters[variant][e] && T * S <= cluster_ctas && pl.nvec >= static_cast<int64_t>(S) * 128) {
       pl.cluster = S;
       // slices are equal by construction: favour few, large copies
       const int64_t slice = pl.nvec / S;
-      pl.chunk_vec = slice >= 2048 ? 1024 : (slice >= 1024 ? 512 : 256);
+      pl.chunk_vec = slice >= 768 ? 1024 : (slice >= 384 ? 512 : 256);
       pl.stages = std::min(kMaxStages, kRingBytes / (pl.chunk_vec * 16));
       pl.P = static_cast<int32_t>(T * S);
       pl.K = 0;
@@ -209,7 +212,7 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   if (!ws || ws_bytes < lay.total) return DLLM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0) return DLLM_ERR_INVALID_ARGUMENT;
   const int variant = (bf16 ? 2 : 0) + (gumbel ? 1 : 0);
-  const StatsPlan pl = plan_stats(*d, variant, T, V, es);
+  const StatsPlan pl = plan_stats(*d, variant, T, V, es, early);
 
   StatsParams p{};
   p.logits = static_cast<const uint8_t*>(logits);

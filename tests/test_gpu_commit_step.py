@@ -122,8 +122,10 @@ def test_inputs_ready_pipelining_matches_plain_calls(cs):
             res.append((j, x0, prob, commit))
     torch.cuda.synchronize()
     for j, x0, prob, commit in res:
+        # x0 and the masks are exact; prob may differ in the last bits because an
+        # overlapping call sizes its grid differently (another fp32 summation order)
         assert torch.equal(x0, outs_plain[j][0]) and torch.equal(commit, outs_plain[j][2])
-        assert torch.equal(prob, outs_plain[j][1])
+        assert torch.allclose(prob, outs_plain[j][1], rtol=TOL["f32"][0], atol=TOL["f32"][1])
 
 
 def test_repeated_fused_calls_leave_workspace_clean(cs):

@@ -76,7 +76,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-constexpr uint32_t kSleepHintNs = 20000;  // one hardware sleep before the deadline is checked again
+constexpr uint32_t kSleepHintNs = 200;  // one hardware sleep before the deadline is checked again
 
 // Waits for the phase with the given parity to complete.  Gives up after
 // kWaitLimitCycles and returns false; the caller records the fault and stops.

@@ -1012,10 +1012,6 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
   }
   if (rank == static_cast<uint32_t>(S - 1) && !ctl.abort_flag) con.tail(row);
   con.resolve_index();
-  if (rank == 0 && p.early) {
-    pdl_wait();  // nothing is written, nor the canvas read, before the previous kernel ends
-    if (tid == 0) pre = load_row_pre(p, row);
-  }
   const Partial r = con.cta_reduce();
   if (tid == 0) ctl.result = r;
   __syncwarp();
@@ -1028,6 +1024,13 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
       for (int k = lane; k < S; k += 32) part_combine<GUMBEL>(tot, load_partial_dsmem(&ctl.result, k));
     __syncwarp();
     cluster_arrive();
+    // Everything above touched only this cluster's own memory.  In early mode
+    // the wait for the previous kernel comes here, so that only the row's
+    // finish (outputs, canvas, batch-row counters) follows that kernel's end.
+    if (p.early) {
+      pdl_wait();
+      if (tid == 0) pre = load_row_pre(p, row);
+    }
     if (warp == 0) {
       tot = warp_combine<GUMBEL>(tot);
       if (lane == 0) rule_b = ctl.abort_flag ? -1 : finish_row<GUMBEL>(p, row, tot, pre);

@@ -17,6 +17,7 @@ by batch row with no collective); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -48,6 +49,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
                     help="eager steps only (no graph, e2e or CPU leg): the command the ncu captures use")
+    ap.add_argument("--batch-rows", type=int, default=None,
+                    help="with --profile: only the first N batch rows of the workload (a capture small "
+                         "enough for a full ncu section set)")
     return ap.parse_args()
 
 
@@ -159,6 +163,19 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def recorded_kernel(workload: str) -> str:
+    """Name of the workload's dominant kernel as the committed ncu launch
+    summary lists it."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            e = json.load(f).get(workload)
+        if e and e.get("kernel"):
+            return e["kernel"] + " (fused statistics + commit rule)"
+    except (OSError, ValueError):
+        pass
+    return "dllm statistics kernel (fused statistics + commit rule)"
+
+
 def recorded_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources (else None)."""
@@ -250,7 +267,15 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    w = W.build(args.workload)
+    if args.batch_rows is not None:
+        if not args.profile:
+            raise SystemExit("--batch-rows is for --profile captures only")
+        full = W.build(args.workload, rows=np.arange(0))
+        nb = max(1, min(args.batch_rows, full.B))
+        w = W.build(args.workload, rows=np.arange(nb * full.L))
+        w = dataclasses.replace(w, B=nb, rows=None, candidates=w.candidates[:nb])
+    else:
+        w = W.build(args.workload)
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[w.name]
     warmup = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[w.name])
     props = torch.cuda.get_device_properties(dev)
@@ -309,22 +334,24 @@ def run_ours(args, rank, world):
     stream = torch.cuda.Stream(dev)
     stream.wait_stream(torch.cuda.current_stream(dev))
 
-    def capture(ready):
+    def capture(ready, n=G):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            for i in range(G):   # eager warm-up on the capture stream
+            for i in range(n):   # eager warm-up on the capture stream
                 step(i, ready)
         torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(G):
+            for i in range(n):
                 step(i, ready)
         return g
 
     g = capture(True)
     g_dep = capture(False)
+    # exactly `steps` timed steps: whole graphs, then one graph of the remainder
+    reps, rem = divmod(steps, G)
+    g_rem = capture(True, rem) if rem else None
     reps_w = max(1, math.ceil(warmup / G))
-    reps = max(1, math.ceil(steps / G))
-    steps_done = reps * G
+    steps_done = reps * G + rem
     with torch.cuda.stream(stream):
         for _ in range(reps_w):
             g.replay()
@@ -340,6 +367,8 @@ def run_ours(args, rank, world):
         with torch.cuda.stream(stream):
             for _ in range(reps):
                 g.replay()
+            if g_rem is not None:
+                g_rem.replay()
         e1.record(stream)
         e1.synchronize()
     torch.cuda.synchronize()
@@ -347,7 +376,7 @@ def run_ours(args, rank, world):
     ms_per_step = ms / steps_done
 
     # the same steps as a dependent chain (each waits for the previous kernel)
-    reps_dep = max(1, min(reps, math.ceil(20000 / G)))
+    reps_dep = max(1, min(max(reps, 1), math.ceil(20000 / G)))
     with torch.cuda.stream(stream):
         g_dep.replay()
     torch.cuda.synchronize()
@@ -428,7 +457,7 @@ def run_ours(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
-                     "kernel": "dllm::stats_kernel (fused statistics + commit rule)"},
+                     "kernel": recorded_kernel(w.name)},
         "e2e": {"value": round(nbytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(nbytes), "d2h_bytes_per_step": int(w.T * 13),
                 "ms_per_step": e2e_ms, "path": "pinned host logits -> cudaMemcpyAsync -> dllm_commit_step -> "

@@ -278,8 +278,9 @@ def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, su
                 out=None, counts=None, ws=None, stream=None, inputs_ready: bool = False):
     """Fused statistics pass + commit rule (+ edit rule and canvas update) in one launch.
 
-    ``inputs_ready`` sets DLLM_FLAG_INPUTS_READY: only when the logits were not
-    written by the kernel that precedes this call in the stream.
+    ``inputs_ready`` sets DLLM_FLAG_INPUTS_READY: only when neither the logits
+    nor ``cand`` were written by the kernel that precedes this call in the
+    stream.
 
     Returns (x0, prob, entropy, commit, edit_mask); commit/edit_mask are None
     when not requested.

@@ -143,8 +143,8 @@ __device__ __forceinline__ void bitonic_sort(uint64_t* keys, int n, int tid) {
 
 __device__ __forceinline__ bool is_candidate(const RuleArgs& a, int64_t b, int64_t l, int32_t* tok_out) {
   const int64_t i = b * a.L + l;
-  int32_t tok = 0;
-  if (a.canvas) tok = a.canvas[b * a.canvas_stride + a.canvas_offset + l];
+  int32_t tok = 0;  // the canvas token matters only to the edit rule and to a missing mask
+  if (a.canvas && (a.edit || !a.cand)) tok = a.canvas[b * a.canvas_stride + a.canvas_offset + l];
   *tok_out = tok;
   if (a.cand) return __ldcg(a.cand + i) != 0;
   return tok == a.mask_id;

@@ -997,7 +997,10 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
   // Rank 0 finishes the row; its candidate flag and canvas token are loaded
   // now so they are at hand then (after the grid dependency in early mode).
   RowPre pre;
-  if (rank == 0 && tid == 0 && !p.early) pre = load_row_pre(p, row);
+  // In early mode the candidate mask is an input like the logits; only a
+  // canvas (which steps rewrite) waits for the previous kernel.
+  const bool reads_canvas = p.rule.canvas != nullptr && (p.rule.edit || p.rule.cand == nullptr);
+  if (rank == 0 && tid == 0 && (!p.early || !reads_canvas)) pre = load_row_pre(p, row);
   RingPos rc;
   for (int64_t i = 0; i < n_units; ++i) {
     const int64_t v_unit = vb + i * p.chunk_vec;
@@ -1029,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
     // finish (outputs, canvas, batch-row counters) follows that kernel's end.
     if (p.early) {
       pdl_wait();
-      if (tid == 0) pre = load_row_pre(p, row);
+      if (tid == 0 && !pre.have) pre = load_row_pre(p, row);
     }
     if (warp == 0) {
       tot = warp_combine<GUMBEL>(tot);

@@ -235,11 +235,12 @@ typedef struct {
   int32_t flags;            /* 0, or DLLM_FLAG_INPUTS_READY */
 } dllm_commit_params;
 
-/* The logits were complete before the previous kernel in the stream began
- * (they are not that kernel's output): the call may start reading them while
- * that kernel still runs, and writes nothing until it has finished.  Lets
- * back-to-back steps over independent inputs overlap.  Never set it when the
- * previous kernel produces the logits (an LM-head GEMM, say). */
+/* The logits and the candidate mask (when one is given) were complete before
+ * the previous kernel in the stream began (they are not that kernel's
+ * output): the call may start reading them while that kernel still runs.  It
+ * reads the canvas, and writes anything, only after that kernel has finished.
+ * Lets back-to-back steps over independent inputs overlap.  Never set it when
+ * the previous kernel produces the logits or the mask (an LM-head GEMM, say). */
 #define DLLM_FLAG_INPUTS_READY 1
 
 dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,

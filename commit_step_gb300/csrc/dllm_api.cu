@@ -126,12 +126,16 @@ StatsPlan plan_stats(const DeviceInfo& d, int variant, int64_t T, int64_t V, int
   pl.nvec = (V * esize) / 16;
   pl.tail = static_cast<int32_t>(V - pl.nvec * (16 / esize));
   // A call that overlaps the previous launch (DLLM_FLAG_INPUTS_READY) sizes
-  // its cluster grid to half the co-resident CTAs, so two steps stream at once.
+  // its cluster grid to a quarter of the co-resident CTAs, so that several
+  // steps stream at once while earlier ones finish their rows; rows too many
+  // for a cluster grid that small take the whole budget before falling back
+  // to the persistent grid.
   const int ctas = d.sms * d.occ[variant];
-  const int cluster_ctas = overlap ? std::max(1, ctas / 4) : ctas;
+  const int budgets[2] = {overlap ? std::max(1, ctas / 4) : ctas, ctas};
+  for (int bi = 0; bi < 2; ++bi)
   for (int e = 4; e >= 1; --e) {
     const int S = 1 << e;
-    if (T <= d.clusters[variant][e] && T * S <= cluster_ctas && pl.nvec >= static_cast<int64_t>(S) * 128) {
+    if (T <= d.clusters[variant][e] && T * S <= budgets[bi] && pl.nvec >= static_cast<int64_t>(S) * 128) {
       pl.cluster = S;
       // slices are equal by construction: favour few, large copies
       const int64_t slice = pl.nvec / S;

@@ -279,16 +279,29 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long lon
   return old;
 }
 
-// Writes x0, prob and entropy of one row from its full reduction and, in the
-// fused step, makes the row's own commit / edit decisions.  Run by one thread.
-// Returns the batch row whose sorting rule this CTA must now run, or -1.
+// x0, prob and entropy of one row from its full reduction.
+struct RowOut {
+  int32_t x0;
+  float prob, H;
+};
+
 template <bool GUMBEL>
-__device__ int32_t finish_row(const StatsParams& p, int64_t row, const Partial& r, RowPre pre) {
-  const int32_t x0 = GUMBEL ? r.best_v : r.idx;
+__device__ __forceinline__ RowOut row_out(const StatsParams& p, const Partial& r) {
+  RowOut o;
+  o.x0 = GUMBEL ? r.best_v : r.idx;
   const float zx = GUMBEL ? r.best_z : r.m;
-  const float prob = ex2_approx((zx - r.m) * kLog2e) / r.Z;
-  float H = logf(r.Z) - r.S2 * kLn2 / r.Z;
-  H = fminf(fmaxf(H, 0.0f), p.ln_veff);
+  o.prob = ex2_approx((zx - r.m) * kLog2e) / r.Z;
+  const float H = logf(r.Z) - r.S2 * kLn2 / r.Z;
+  o.H = fminf(fmaxf(H, 0.0f), p.ln_veff);
+  return o;
+}
+
+// Writes x0, prob and entropy of one row and, in the fused step, makes the
+// row's own commit / edit decisions.  Run by one thread.  Returns the batch
+// row whose sorting rule this CTA must now run, or -1.
+__device__ int32_t finish_row(const StatsParams& p, int64_t row, const RowOut& o, RowPre pre) {
+  const int32_t x0 = o.x0;
+  const float prob = o.prob, H = o.H;
   p.x0[row] = x0;
   p.prob[row] = prob;
   p.entropy[row] = H;
@@ -911,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
       }
     }
     if (tid == 0) {
-      ctl.flag2 = action != 0 ? finish_row<GUMBEL>(p, row, ctl.result, RowPre()) : -1;
+      ctl.flag2 = action != 0 ? finish_row(p, row, row_out<GUMBEL>(p, ctl.result), RowPre()) : -1;
       ctl.cta_best = float_key(kNegInf);  // the next row starts with no pruning floor
     }
     named_sync(1, kConsumers);
@@ -1027,17 +1040,16 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
       for (int k = lane; k < S; k += 32) part_combine<GUMBEL>(tot, load_partial_dsmem(&ctl.result, k));
     __syncwarp();
     cluster_arrive();
+    RowOut o{};
+    if (warp == 0) o = row_out<GUMBEL>(p, warp_combine<GUMBEL>(tot));
     // Everything above touched only this cluster's own memory.  In early mode
     // the wait for the previous kernel comes here, so that only the row's
-    // finish (outputs, canvas, batch-row counters) follows that kernel's end.
+    // writes (outputs, canvas, batch-row counters) follow that kernel's end.
     if (p.early) {
       pdl_wait();
       if (tid == 0 && !pre.have) pre = load_row_pre(p, row);
     }
-    if (warp == 0) {
-      tot = warp_combine<GUMBEL>(tot);
-      if (lane == 0) rule_b = ctl.abort_flag ? -1 : finish_row<GUMBEL>(p, row, tot, pre);
-    }
+    if (tid == 0) rule_b = ctl.abort_flag ? -1 : finish_row(p, row, o, pre);
   } else {
     __syncwarp();
     cluster_sync_all();

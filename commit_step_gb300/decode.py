@@ -18,6 +18,8 @@ import torch
 
 from . import RULE_THRESHOLD, block_ranges, commit_step
 
+_GATE_CYCLES = 1_000_000   # about 0.5 ms of SM clock: well beyond what the host needs to enqueue a step
+
 
 def decode_with_editing(model, prompt: torch.Tensor, *, gen_len: int, block_len: int, mask_id: int,
                         threshold: float = 0.95, editing_threshold: float = 0.9, max_post_steps: int = 16,
@@ -50,6 +52,10 @@ def decode_with_editing(model, prompt: torch.Tensor, *, gen_len: int, block_len:
                     break
             logits = model(bi, step, lo, n).view(B, n, -1)
             if step_times is not None:
+                # Hold the GPU busy while the host enqueues the step, so that
+                # the events time the commit step rather than the host's launch
+                # (in a real loop the model's forward plays this part).
+                torch.cuda._sleep(_GATE_CYCLES)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
             commit_step(logits, rule=RULE_THRESHOLD, tau=threshold, strict=True, suppress_ids=suppress_ids,

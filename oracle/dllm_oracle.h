@@ -22,7 +22,10 @@ extern "C" {
 /* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): out = philox(ctr, key). */
 void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
 
-/* The project's fp32 natural logarithm (exponent split + atanh series). */
+/* The project's fp32 natural logarithm (exponent split + atanh series).
+ * Pinned to <= 2.5 ulp of the double logarithm over every u the sampler can
+ * draw; its exact bits are this project's own definition, which no value on
+ * the pages fixes: parity unpinned beyond that error bound. */
 float orc_ln_p(float x);
 void orc_ln_p_many(const float* x, int64_t n, float* out);
 

@@ -35,6 +35,8 @@ def lib():
         L.orc_gumbel_score.argtypes = [f32, f32, u64, i64, i64]
         L.orc_gumbel_score.restype = f32
         L.orc_token_stats.argtypes = [P, C.c_int, i64, i64, i64, P, f32, u64, P, i32, P, P, P, C.c_int]
+        L.orc_token_stats_ex.argtypes = [P, C.c_int, i64, i64, i64, P, f32, u64, f32, P, i32, P, P, P, P, P,
+                                         C.c_int]
         for name in ("orc_threshold_transfer",):
             getattr(L, name).argtypes = [P, P, i64, i64, f32, C.c_int, P]
         L.orc_topk_transfer.argtypes = [P, P, i64, i64, P, P]
@@ -108,6 +110,31 @@ def token_stats(logits: np.ndarray, dtype: str = "f32", temperature: float = 0.0
                                _p(x0), _p(prob), _p(ent), int(n_threads))
     _check(rc, "token_stats")
     return x0, prob, ent
+
+
+def token_stats_ex(logits: np.ndarray, dtype: str = "f32", temperature: float = 0.0, key: int = 0,
+                   logit_scale: float = 1.0, suppress_ids=(), row_ids=None, n_threads: int = 0):
+    """(x0, prob, entropy, margin, argmax) per row of the scaled logits
+    z' = fp32(z * logit_scale); margin = prob(x0) - prob(runner-up), argmax
+    = the first id of the largest z' (the greedy proposal when sampling)."""
+    dt = {"f32": 0, "bf16": 1}[dtype]
+    want = np.float32 if dt == 0 else np.uint16
+    z = np.ascontiguousarray(logits, dtype=want)
+    if z.ndim != 2:
+        raise ValueError("logits must be 2-D (rows, V)")
+    n, V = z.shape
+    rid = None if row_ids is None else np.ascontiguousarray(row_ids, dtype=np.int64)
+    sup = np.ascontiguousarray(list(suppress_ids), dtype=np.int32)
+    x0 = np.zeros(n, dtype=np.int32)
+    am = np.zeros(n, dtype=np.int32)
+    prob = np.zeros(n, dtype=np.float64)
+    ent = np.zeros(n, dtype=np.float64)
+    mar = np.zeros(n, dtype=np.float64)
+    rc = lib().orc_token_stats_ex(_p(z), dt, n, V, V, _p(rid), float(temperature), int(key) & (2**64 - 1),
+                                  float(np.float32(logit_scale)), _p(sup) if sup.size else None, int(sup.size),
+                                  _p(x0), _p(prob), _p(ent), _p(mar), _p(am), int(n_threads))
+    _check(rc, "token_stats_ex")
+    return x0, prob, ent, mar, am
 
 
 def _rule_inputs(conf, cand):

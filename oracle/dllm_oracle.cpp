@@ -144,7 +144,21 @@ struct RowOut {
   int32_t x0;
   double prob;
   double entropy;
+  double margin;   // prob(x0) - prob(runner-up)
+  int32_t argmax;  // first id of the largest scaled logit
 };
+
+// The logit of id v as the statistics see it: sanitised (load_logit), then
+// scaled by the caller's fp32 factor s in one fp32 multiplication (a logit
+// with no mass keeps none).  s = 1 leaves the logit as it is; s = 1/T gives
+// the temperature-scaled logits the uniform-noise loop of "dLLM block
+// decoding" (section "Uniform-noise decoding (DiffusionGemma)") measures its
+// entropy on and samples from.
+inline float scaled_logit(const void* logits, int dtype, int64_t idx, float s) {
+  const float z = load_logit(logits, dtype, idx);
+  if (z == -std::numeric_limits<float>::infinity()) return z;
+  return z * s;
+}
 
 // token_stats for one row.  [ARS] "What mlx-arsenal ships" and "Deviations":
 // per position the proposal x0, its probability and the entropy, computed
@@ -152,43 +166,51 @@ struct RowOut {
 // suppressed ids take no part in the softmax.  [MOJO] "Row statistics on the
 // device": the row max, sum exp(z - max) and sum exp(z - max)(z - max) give
 // both numbers; the argmax tie rule keeps the smallest id; the argmax has
-// p = 1 / sum.
+// p = 1 / sum; the largest logit at any other id gives the runner-up whose
+// probability topk_margin subtracts.
 RowOut stats_row(const void* logits, int dtype, int64_t row_off, int64_t V, int64_t grow,
-                 float t, uint64_t key, const std::vector<uint8_t>& absent, int64_t v_eff) {
+                 float t, uint64_t key, float s, const std::vector<uint8_t>& absent, int64_t v_eff) {
   const double inf = std::numeric_limits<double>::infinity();
-  // Pass 1: the max over the token set A (ids not suppressed).
+  auto zl = [&](int64_t v) { return scaled_logit(logits, dtype, row_off + v, s); };
+  // Pass 1: the max over the token set A (ids not suppressed) and its first id.
   float m = -std::numeric_limits<float>::infinity();
+  int64_t first_max = -1;
   for (int64_t v = 0; v < V; ++v) {
     if (absent[v]) continue;
-    m = std::max(m, load_logit(logits, dtype, row_off + v));
+    const float z = zl(v);
+    if (first_max < 0 || z > m) {
+      m = z;
+      first_max = v;
+    }
   }
   // x0: lowest id in A maximizing z (greedy) or the Gumbel score (t > 0).
-  int64_t x0 = -1;
+  int64_t x0 = first_max;
   if (t > 0.0f) {
     float best = 0.0f;
+    x0 = -1;
     for (int64_t v = 0; v < V; ++v) {
       if (absent[v]) continue;
-      const float s = gumbel_score(load_logit(logits, dtype, row_off + v), t, key, grow, v);
-      if (x0 < 0 || s > best) {
-        best = s;
+      const float sc = gumbel_score(zl(v), t, key, grow, v);
+      if (x0 < 0 || sc > best) {
+        best = sc;
         x0 = v;
-      }
-    }
-  } else {
-    for (int64_t v = 0; v < V; ++v) {
-      if (absent[v]) continue;
-      if (load_logit(logits, dtype, row_off + v) == m) {
-        x0 = v;
-        break;
       }
     }
   }
-  const double zx0 = load_logit(logits, dtype, row_off + x0);
-  RowOut out{static_cast<int32_t>(x0), 0.0, 0.0};
+  // The runner-up: the largest logit over A without x0 (-inf if A = {x0}).
+  float r = -std::numeric_limits<float>::infinity();
+  bool have_r = false;
+  for (int64_t v = 0; v < V; ++v) {
+    if (absent[v] || v == x0) continue;
+    r = have_r ? std::max(r, zl(v)) : zl(v);
+    have_r = true;
+  }
+  RowOut out{static_cast<int32_t>(x0), 0.0, 0.0, 0.0, static_cast<int32_t>(first_max)};
   if (m == -std::numeric_limits<float>::infinity()) {
     // No finite mass anywhere: the uniform limit over A.
     out.prob = 1.0 / static_cast<double>(v_eff);
     out.entropy = std::log(static_cast<double>(v_eff));
+    out.margin = out.prob - (have_r ? out.prob : 0.0);
     return out;
   }
   // Pass 2: Z = sum exp(z - m), S = sum exp(z - m)(z - m); -inf terms add 0.
@@ -196,14 +218,17 @@ RowOut stats_row(const void* logits, int dtype, int64_t row_off, int64_t V, int6
   double Z = 0.0, S = 0.0;
   for (int64_t v = 0; v < V; ++v) {
     if (absent[v]) continue;
-    const double z = load_logit(logits, dtype, row_off + v);
+    const double z = zl(v);
     if (z == -inf) continue;
     const double d = z - md;
     const double e = std::exp(d);
     Z += e;
     S += e * d;
   }
-  out.prob = std::exp(zx0 - md) / Z;
+  const double zx0 = zl(x0);
+  out.prob = zx0 == -inf ? 0.0 : std::exp(zx0 - md) / Z;
+  const double p_r = (have_r && r != -std::numeric_limits<float>::infinity()) ? std::exp(double(r) - md) / Z : 0.0;
+  out.margin = out.prob - p_r;
   // H = -sum p log p = log Z - S / Z, clamped to its range [0, log |A|].
   double H = std::log(Z) - S / Z;
   H = std::min(std::max(H, 0.0), std::log(static_cast<double>(v_eff)));
@@ -264,12 +289,14 @@ float orc_gumbel_score(float z, float temperature, uint64_t key, int64_t row, in
   return gumbel_score(z, temperature, key, row, v);
 }
 
-int orc_token_stats(const void* logits, int dtype, int64_t n_rows, int64_t V, int64_t row_stride,
-                    const int64_t* row_ids, float temperature, uint64_t key,
-                    const int32_t* suppress_ids, int32_t n_suppress,
-                    int32_t* x0, double* prob, double* entropy, int n_threads) {
+int orc_token_stats_ex(const void* logits, int dtype, int64_t n_rows, int64_t V, int64_t row_stride,
+                       const int64_t* row_ids, float temperature, uint64_t key, float logit_scale,
+                       const int32_t* suppress_ids, int32_t n_suppress,
+                       int32_t* x0, double* prob, double* entropy, double* margin, int32_t* argmax,
+                       int n_threads) {
   if (n_rows < 0 || V <= 0 || row_stride < V || (dtype != 0 && dtype != 1)) return -1;
   if (!(temperature >= 0.0f) || n_suppress < 0) return -1;
+  if (!(logit_scale > 0.0f) || !(logit_scale <= 65536.0f)) return -1;
   if (n_rows == 0) return 0;
   if (!logits || !x0 || !prob || !entropy) return -1;
   std::vector<uint8_t> absent(static_cast<size_t>(V), 0);
@@ -285,10 +312,12 @@ int orc_token_stats(const void* logits, int dtype, int64_t n_rows, int64_t V, in
   auto work = [&](int tid) {
     for (int64_t r = tid; r < n_rows; r += nt) {
       const int64_t grow = row_ids ? row_ids[r] : r;
-      const RowOut o = stats_row(logits, dtype, r * row_stride, V, grow, temperature, key, absent, v_eff);
+      const RowOut o = stats_row(logits, dtype, r * row_stride, V, grow, temperature, key, logit_scale, absent, v_eff);
       x0[r] = o.x0;
       prob[r] = o.prob;
       entropy[r] = o.entropy;
+      if (margin) margin[r] = o.margin;
+      if (argmax) argmax[r] = o.argmax;
     }
   };
   if (nt <= 1) {
@@ -299,6 +328,14 @@ int orc_token_stats(const void* logits, int dtype, int64_t n_rows, int64_t V, in
     for (auto& th : pool) th.join();
   }
   return 0;
+}
+
+int orc_token_stats(const void* logits, int dtype, int64_t n_rows, int64_t V, int64_t row_stride,
+                    const int64_t* row_ids, float temperature, uint64_t key,
+                    const int32_t* suppress_ids, int32_t n_suppress,
+                    int32_t* x0, double* prob, double* entropy, int n_threads) {
+  return orc_token_stats_ex(logits, dtype, n_rows, V, row_stride, row_ids, temperature, key, 1.0f, suppress_ids,
+                            n_suppress, x0, prob, entropy, nullptr, nullptr, n_threads);
 }
 
 // threshold_transfer.  [ARS] function table: a candidate commits when its

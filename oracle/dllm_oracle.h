@@ -42,6 +42,17 @@ int orc_token_stats(const void* logits, int dtype, int64_t n_rows, int64_t V, in
                     const int32_t* suppress_ids, int32_t n_suppress,
                     int32_t* x0, double* prob, double* entropy, int n_threads);
 
+/* The same pass on scaled logits z' = fp32(z * logit_scale), 0 < logit_scale
+ * <= 65536 (1 = orc_token_stats).  margin (nullable): prob(x0) minus the
+ * probability of the runner-up, the largest z' over the token set without
+ * x0.  argmax (nullable): the first id of the largest z' (equal to x0 when
+ * temperature == 0). */
+int orc_token_stats_ex(const void* logits, int dtype, int64_t n_rows, int64_t V, int64_t row_stride,
+                       const int64_t* row_ids, float temperature, uint64_t key, float logit_scale,
+                       const int32_t* suppress_ids, int32_t n_suppress,
+                       int32_t* x0, double* prob, double* entropy, double* margin, int32_t* argmax,
+                       int n_threads);
+
 /* Commit rules over (B, L) row-major confidences and 0/1 candidate masks. */
 int orc_threshold_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
                            float tau, int strict, uint8_t* commit);

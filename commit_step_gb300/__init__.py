@@ -33,7 +33,7 @@ EXPORTS = (
     "dllm_status_string", "dllm_version", "dllm_token_stats_workspace_size", "dllm_token_stats",
     "dllm_threshold_transfer", "dllm_topk_transfer", "dllm_factor_transfer", "dllm_entropy_bound_transfer",
     "dllm_edit_transfer", "dllm_transfer_schedule", "dllm_block_ranges", "dllm_commit_step",
-    "dllm_workspace_fault", "dllm_token_stats_noalloc",
+    "dllm_workspace_fault", "dllm_token_stats_noalloc", "dllm_token_stats_ex",
 )
 
 
@@ -41,6 +41,12 @@ class DllmError(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__(f"{what}: {status_string(status)}")
         self.status = status
+
+
+class StatsEx(C.Structure):
+    """Mirror of ``dllm_stats_ex``."""
+
+    _fields_ = [("logit_scale", C.c_float), ("margin", C.c_void_p), ("argmax", C.c_void_p)]
 
 
 class CommitParams(C.Structure):
@@ -51,7 +57,7 @@ class CommitParams(C.Structure):
         ("gamma", C.c_float), ("k", C.c_void_p), ("cand", C.c_void_p), ("mask_id", C.c_int32),
         ("edit", C.c_int32), ("tau_edit", C.c_float), ("commit", C.c_void_p), ("edit_mask", C.c_void_p),
         ("canvas", C.c_void_p), ("canvas_stride", C.c_int64), ("canvas_offset", C.c_int64),
-        ("counts", C.c_void_p), ("flags", C.c_int32),
+        ("counts", C.c_void_p), ("flags", C.c_int32), ("ex", C.POINTER(StatsEx)),
     ]
 
 
@@ -78,6 +84,7 @@ def _load() -> C.CDLL:
     lib.dllm_block_ranges.argtypes = [i64, i64, i64, C.c_int, P, i64, P]
     lib.dllm_workspace_fault.argtypes = [P, P, C.POINTER(C.c_int32)]
     lib.dllm_token_stats_noalloc.argtypes = stats_args + [P]
+    lib.dllm_token_stats_ex.argtypes = stats_args[:10] + [C.POINTER(StatsEx)] + stats_args[10:] + [P, sz, P]
     for name in EXPORTS[3:]:
         if name != "dllm_token_stats_workspace_size":
             getattr(lib, name).restype = C.c_int
@@ -173,6 +180,54 @@ def token_stats(logits: torch.Tensor, temperature: float = 0.0, key: int = 0, su
                                  sup, len(suppress_ids), _ptr(x0), _ptr(prob), _ptr(ent), _ptr(ws), ws.numel(),
                                  _stream(stream)), "dllm_token_stats")
     return x0, prob, ent
+
+
+def _stats_ex(shape, device, logit_scale, margin, argmax):
+    """The dllm_stats_ex of a call (None when no option departs from the
+    plain pass) and the margin / argmax tensors it writes.  ``margin`` and
+    ``argmax``: True (allocate), a tensor (write there) or None/False."""
+    if margin is True:
+        margin = torch.empty(shape, dtype=torch.float32, device=device)
+    if argmax is True:
+        argmax = torch.empty(shape, dtype=torch.int32, device=device)
+    margin = margin if torch.is_tensor(margin) else None
+    argmax = argmax if torch.is_tensor(argmax) else None
+    _need_cuda(margin, argmax)
+    if float(logit_scale) == 1.0 and margin is None and argmax is None:
+        return None, None, None
+    ex = StatsEx()
+    ex.logit_scale = float(logit_scale)
+    ex.margin = None if margin is None else margin.data_ptr()
+    ex.argmax = None if argmax is None else argmax.data_ptr()
+    return ex, margin, argmax
+
+
+def token_stats_ex(logits: torch.Tensor, temperature: float = 0.0, key: int = 0, suppress_ids: Sequence[int] = (),
+                   logit_scale: float = 1.0, margin=True, argmax=True, out=None, ws: Optional[torch.Tensor] = None,
+                   stream=None):
+    """Statistics of the scaled logits z' = fp32(z * logit_scale), with the
+    margin confidence (prob(x0) - prob(runner-up)) and the greedy argmax
+    beside a sample.  Returns (x0, prob, entropy, margin, argmax); margin /
+    argmax are None when not requested."""
+    _need_cuda(logits)
+    B, L, V, stride = _logits_view(logits)
+    dt = _dtype_code(logits)
+    shape = logits.shape[:-1]
+    if out is None:
+        x0 = torch.empty(shape, dtype=torch.int32, device=logits.device)
+        prob = torch.empty(shape, dtype=torch.float32, device=logits.device)
+        ent = torch.empty(shape, dtype=torch.float32, device=logits.device)
+    else:
+        x0, prob, ent = out
+    ex, margin, argmax = _stats_ex(shape, logits.device, logit_scale, margin, argmax)
+    sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
+    if ws is None:
+        ws = workspace(B, L, V, dt, logits.device, stream)
+    _check(_lib.dllm_token_stats_ex(_ptr(logits), dt, B, L, V, stride, float(temperature), int(key) & (2**64 - 1),
+                                    sup, len(suppress_ids), None if ex is None else C.byref(ex), _ptr(x0),
+                                    _ptr(prob), _ptr(ent), _ptr(ws), ws.numel(), _stream(stream)),
+           "dllm_token_stats_ex")
+    return x0, prob, ent, margin, argmax
 
 
 def _canvas_args(x0, canvas, canvas_offset):
@@ -275,8 +330,14 @@ def block_ranges(P: int, gen_len: int, block_len: int, align: bool = False):
 def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, suppress_ids: Sequence[int] = (),
                 cand=None, mask_id: int = -1, tau: float = 0.0, strict: bool = False, k=None, factor: float = 0.0,
                 gamma: float = 0.0, edit: bool = False, tau_edit: float = 1.0, canvas=None, canvas_offset: int = 0,
-                out=None, counts=None, ws=None, stream=None, inputs_ready: bool = False):
+                out=None, counts=None, ws=None, stream=None, inputs_ready: bool = False,
+                logit_scale: float = 1.0, margin: Optional[torch.Tensor] = None,
+                argmax: Optional[torch.Tensor] = None):
     """Fused statistics pass + commit rule (+ edit rule and canvas update) in one launch.
+
+    ``logit_scale``, ``margin`` and ``argmax`` (preallocated (B, L) float32 /
+    int32 tensors) are the extended statistics of ``token_stats_ex``; the
+    rules then decide on the statistics of the scaled logits.
 
     ``inputs_ready`` sets DLLM_FLAG_INPUTS_READY: only when neither the logits
     nor ``cand`` were written by the kernel that precedes this call in the
@@ -313,6 +374,9 @@ def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, su
         p.canvas, p.canvas_stride, p.canvas_offset = canvas.data_ptr(), canvas.stride(0), int(canvas_offset)
     p.counts = None if counts is None else counts.data_ptr()
     p.flags = FLAG_INPUTS_READY if inputs_ready else 0
+    ex, _, _ = _stats_ex((B, L), dev, logit_scale, margin, argmax)
+    if ex is not None:
+        p.ex = C.pointer(ex)
     sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
     if ws is None:
         ws = workspace(B, L, V, dt, dev, stream)

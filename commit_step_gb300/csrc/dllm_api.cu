@@ -13,8 +13,8 @@
 #include "dllm_stats.cuh"
 
 namespace dllm {
-const void* stats_kernel_ptr(bool bf16, bool gumbel);
-const void* stats_cluster_kernel_ptr(bool bf16, bool gumbel);
+const void* stats_kernel_ptr(bool bf16, int mode);
+const void* stats_cluster_kernel_ptr(bool bf16, int mode);
 const void* rules_kernel_ptr(int nt);
 const void* edit_kernel_ptr();
 const void* schedule_kernel_ptr();
@@ -29,8 +29,11 @@ constexpr size_t kStatsSmemMax = static_cast<size_t>(kRingBytes) + kFusedSortCap
 
 struct DeviceInfo {
   int sms = 0;
-  int occ[4] = {0, 0, 0, 0};  // CTAs per SM of stats_kernel<bf16, gumbel>, index 2*bf16+gumbel
-  int clusters[4][5] = {};    // co-resident clusters of stats_cluster_kernel per cluster size 1,2,4,8,16
+  // Per kernel variant, index bf16 * kModes + mode: CTAs per SM of
+  // stats_kernel, and co-resident clusters of stats_cluster_kernel per
+  // cluster size 1, 2, 4, 8, 16.
+  int occ[2 * kModes] = {};
+  int clusters[2 * kModes][5] = {};
   cudaError_t err = cudaSuccess;
 };
 
@@ -43,16 +46,16 @@ const DeviceInfo* device_info() {
   std::call_once(g_once[dev], [dev]() {
     DeviceInfo& d = g_dev[dev];
     d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    for (int v = 0; v < 4 && d.err == cudaSuccess; ++v) {
-      const void* k = stats_kernel_ptr(v >= 2, (v & 1) != 0);
+    for (int v = 0; v < 2 * kModes && d.err == cudaSuccess; ++v) {
+      const void* k = stats_kernel_ptr(v >= kModes, v % kModes);
       d.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmemMax));
       if (d.err != cudaSuccess) break;
       int n = 0;
       d.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kThreads, kStatsSmemMax);
       d.occ[v] = std::max(1, std::min(n, kMaxCtasPerSm));
     }
-    for (int v = 0; v < 4 && d.err == cudaSuccess; ++v) {
-      const void* k = stats_cluster_kernel_ptr(v >= 2, (v & 1) != 0);
+    for (int v = 0; v < 2 * kModes && d.err == cudaSuccess; ++v) {
+      const void* k = stats_cluster_kernel_ptr(v >= kModes, v % kModes);
       d.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmemMax));
       if (d.err == cudaSuccess) d.err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       for (int e = 0; e < 5 && d.err == cudaSuccess; ++e) {
@@ -203,19 +206,38 @@ dllm_status check_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L,
   return DLLM_OK;
 }
 
+// The extended statistics options, resolved (dllm_stats_ex or the defaults).
+struct StatsOpts {
+  float scale = 1.0f;
+  float* margin = nullptr;
+  int32_t* argmax = nullptr;
+};
+
+dllm_status resolve_ex(const dllm_stats_ex* ex, StatsOpts& o) {
+  o = StatsOpts();
+  if (!ex) return DLLM_OK;
+  if (!(ex->logit_scale > 0.0f) || !(ex->logit_scale <= 256.0f)) return DLLM_ERR_INVALID_ARGUMENT;
+  o.scale = ex->logit_scale;
+  o.margin = ex->margin;
+  o.argmax = ex->argmax;
+  return DLLM_OK;
+}
+
 dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
                       float temperature, uint64_t key, const std::vector<int32_t>& sup, int32_t* x0, float* prob,
                       float* entropy, const RuleArgs* rule, void* ws, size_t ws_bytes, cudaStream_t s,
-                      bool early = false) {
+                      bool early = false, const StatsOpts& opt = StatsOpts()) {
   const DeviceInfo* d = device_info();
   if (!d) return DLLM_ERR_CUDA;
   const bool bf16 = dt == DLLM_BF16, gumbel = temperature > 0.0f;
+  // A sample that must also report its row's argmax or margin tracks both.
+  const int mode = !gumbel ? kModeGreedy : ((opt.margin || opt.argmax) ? kModeDual : kModeGumbel);
   const int es = esize_of(dt);
   const int64_t T = B * L;
   const WsLayout lay = ws_layout(B, L, d->sms);
   if (!ws || ws_bytes < lay.total) return DLLM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0) return DLLM_ERR_INVALID_ARGUMENT;
-  const int variant = (bf16 ? 2 : 0) + (gumbel ? 1 : 0);
+  const int variant = (bf16 ? kModes : 0) + mode;
   const StatsPlan pl = plan_stats(*d, variant, T, V, es, early);
 
   StatsParams p{};
@@ -234,6 +256,7 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   p.P = pl.P;
   p.stages = pl.stages;
   p.temperature = temperature;
+  p.scale = opt.scale;
   {
     uint32_t k0 = static_cast<uint32_t>(key), k1 = static_cast<uint32_t>(key >> 32);
     for (int r = 0; r < 10; ++r) {
@@ -249,6 +272,8 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   p.x0 = x0;
   p.prob = prob;
   p.entropy = entropy;
+  p.margin = opt.margin;
+  p.argmax = opt.argmax;
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.fault = reinterpret_cast<int32_t*>(w + lay.fault);
   p.row_count = reinterpret_cast<int32_t*>(w + lay.row_count);
@@ -260,8 +285,8 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   const size_t smem = static_cast<size_t>(pl.stages) * pl.chunk_vec * 16 + (rule ? kFusedSortCap * 9 : 0);
   void* args[] = {&p};
   if (pl.cluster > 0)
-    return launch(stats_cluster_kernel_ptr(bf16, gumbel), dim3(pl.P), dim3(kThreads), smem, s, args, pl.cluster);
-  return launch(stats_kernel_ptr(bf16, gumbel), dim3(pl.P), dim3(kThreads), smem, s, args);
+    return launch(stats_cluster_kernel_ptr(bf16, mode), dim3(pl.P), dim3(kThreads), smem, s, args, pl.cluster);
+  return launch(stats_kernel_ptr(bf16, mode), dim3(pl.P), dim3(kThreads), smem, s, args);
 }
 
 int next_pow2(int64_t x) {
@@ -398,6 +423,21 @@ dllm_status dllm_token_stats(const void* logits, dllm_dtype dt, int64_t B, int64
                    workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+dllm_status dllm_token_stats_ex(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,
+                                int64_t row_stride, float temperature, uint64_t key, const int32_t* suppress_ids,
+                                int32_t n_suppress, const dllm_stats_ex* ex, int32_t* x0, float* prob,
+                                float* entropy, void* workspace, size_t workspace_bytes, dllm_stream_t stream) {
+  std::vector<int32_t> sup;
+  dllm_status st = check_stats(logits, dt, B, L, V, row_stride, temperature, suppress_ids, n_suppress, x0, prob,
+                               entropy, sup);
+  if (st != DLLM_OK) return st;
+  StatsOpts opt;
+  st = resolve_ex(ex, opt);
+  if (st != DLLM_OK || B * L == 0) return st;
+  return run_stats(logits, dt, B, L, V, row_stride, temperature, key, sup, x0, prob, entropy, nullptr, workspace,
+                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream), false, opt);
+}
+
 dllm_status dllm_threshold_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L, float tau,
                                     int strict, uint8_t* commit, const int32_t* x0, int32_t* canvas,
                                     int64_t canvas_stride, int64_t canvas_offset, dllm_stream_t stream) {
@@ -518,8 +558,11 @@ dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64
   a.counts = cp->counts;
   a.L = L;
   if (cp->flags & ~static_cast<int32_t>(DLLM_FLAG_INPUTS_READY)) return DLLM_ERR_INVALID_ARGUMENT;
+  StatsOpts opt;
+  if (resolve_ex(cp->ex, opt) != DLLM_OK) return DLLM_ERR_INVALID_ARGUMENT;
   return run_stats(logits, dt, B, L, V, row_stride, temperature, key, sup, x0, prob, entropy, &a, workspace,
-                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream), (cp->flags & DLLM_FLAG_INPUTS_READY) != 0);
+                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream), (cp->flags & DLLM_FLAG_INPUTS_READY) != 0,
+                   opt);
 }
 
 dllm_status dllm_token_stats_noalloc(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,

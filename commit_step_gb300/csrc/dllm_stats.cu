@@ -10,10 +10,13 @@
 //     producer thread streams its units into a shared-memory ring with
 //     cp.async.bulk (TMA bulk copies), one mbarrier per stage; eight consumer
 //     warps read each unit from shared memory.
-//   * Each consumer thread keeps an online softmax state: running max m,
-//     Z = sum 2^y and S2 = sum 2^y y with y = (z - m) log2 e (packed fp32x2
+//   * Each consumer thread keeps an online softmax state of the scaled logits
+//     z' = z s (s = 1 unless the caller scales them): running max m,
+//     Z = sum 2^y and S2 = sum 2^y y with y = (z s - m) log2 e (packed fp32x2
 //     accumulators), rescaled when the max grows; entropy = ln Z - S2 ln 2 / Z.
-//     The first index of the max is located only when the max grows.
+//     The first index of the max is located once per row, from the first
+//     vector that holds the thread's max; the largest value outside that
+//     element (the runner-up of the margin confidence) comes with it.
 //   * Gumbel-max: one Philox4x32-10 call per four ids; a bound on the noise
 //     from the largest uniform of each 16-byte vector lets most vectors skip
 //     the two logarithms; the warp shares its best score to tighten the bound.
@@ -42,10 +45,12 @@ struct Acc {
   uint64_t S2;      // two partial sums of 2^y y
   float negm;
   int32_t idx;      // first index of m among the tail elements (greedy)
-  float vm;         // max over the thread's full vectors (greedy)
+  float vm;         // max of z' over the thread's full vectors (greedy)
   int32_t vv;       // first id of the first vector holding vm, -1 if none
   uint32_t bw[4];   // that vector's sanitized words
-  float vm_tail;    // the thread's tail element, if any (greedy)
+  float m2o;        // max of z' over the thread's other full vectors; after
+                    // resolve_index, the thread's runner-up
+  float vm_tail;    // z' of the thread's tail element, if any (greedy)
   float best_s;
   int32_t best_v;
   float best_z;
@@ -71,6 +76,7 @@ __device__ __forceinline__ void acc_init(Acc& a) {
   a.vm = kMInit;
   a.vv = -1;
   a.bw[0] = a.bw[1] = a.bw[2] = a.bw[3] = 0u;
+  a.m2o = kMInit;
   a.vm_tail = kMInit;
   a.best_s = kNegInf;
   a.best_v = 0x7FFFFFFF;
@@ -87,17 +93,6 @@ __device__ __forceinline__ void acc_rescale(Acc& a, float mnew) {
   a.Z2 = mul2(a.Z2, c2);
   a.m = mnew;
   a.negm = -mnew;
-}
-
-// Adds two sanitized logits (already <= a.m) to the sums.
-__device__ __forceinline__ void acc_pair(Acc& a, float z0, float z1) {
-  const uint64_t d2 = add2(pack2(z0, z1), pack2(a.negm, a.negm));
-  const uint64_t y2 = mul2(d2, pack2(kLog2e, kLog2e));
-  float y0, y1;
-  unpack2(y2, y0, y1);
-  const uint64_t e2 = pack2(ex2_approx(y0), ex2_approx(y1));
-  a.Z2 = add2(a.Z2, e2);
-  a.S2 = fma2(e2, y2, a.S2);
 }
 
 __device__ __forceinline__ float sanitize(float z) {
@@ -118,8 +113,11 @@ __device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
 }
 
 // Adds two sanitized logits (<= the running max) to the sums (Z2, S2).
-__device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, float z1, uint64_t negm2) {
-  const uint64_t d2 = add2(pack2(z0, z1), negm2);
+// Adds two sanitized logits (z s <= m) to the sums: y = (z s - m) log2 e, the
+// product z s taken inside the fused multiply-add (exact when s = 1).
+__device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, float z1, uint64_t negm2,
+                                          uint64_t s2) {
+  const uint64_t d2 = fma2(pack2(z0, z1), s2, negm2);
   const uint64_t y2 = mul2(d2, pack2(kLog2e, kLog2e));
   float y0, y1;
   unpack2(y2, y0, y1);
@@ -128,20 +126,22 @@ __device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, 
   S2 = fma2(e2, y2, S2);
 }
 
-// Combines b into a (a and b may cover any id sets).
-template <bool GUMBEL>
+// Combines b into a (a and b may cover any id sets).  The runner-up of the
+// union is the larger of the winner's runner-up and the loser's max.
+template <int MODE>
 __device__ __forceinline__ void part_combine(Partial& a, const Partial& b) {
+  constexpr bool GUMBEL = MODE != kModeGreedy, GREEDY = MODE != kModeGumbel;
   const float m = fmaxf(a.m, b.m);
   const float da = (a.m - m) * kLog2e, db = (b.m - m) * kLog2e;
   const float ca = ex2_approx(da), cb = ex2_approx(db);
   const float Z = ca * a.Z + cb * b.Z;
   const float S2 = ca * fmaf(da, a.Z, a.S2) + cb * fmaf(db, b.Z, b.S2);
-  int32_t idx = a.idx;
-  if (b.m > a.m || (b.m == a.m && b.idx < a.idx)) idx = b.idx;
+  const bool b_wins = b.m > a.m || (b.m == a.m && b.idx < a.idx);
+  if (GREEDY) a.m2 = b_wins ? fmaxf(b.m2, a.m) : fmaxf(a.m2, b.m);
   a.m = m;
   a.Z = Z;
   a.S2 = S2;
-  a.idx = idx;
+  a.idx = b_wins ? b.idx : a.idx;
   if (GUMBEL) {
     if (b.best_s > a.best_s || (b.best_s == a.best_s && b.best_v < a.best_v)) {
       a.best_s = b.best_s;
@@ -160,7 +160,7 @@ __device__ __forceinline__ Partial empty_partial() {
   p.best_s = kNegInf;
   p.best_z = 0.0f;
   p.best_v = 0x7FFFFFFF;
-  p.pad = 0;
+  p.m2 = kMInit;
   return p;
 }
 
@@ -176,12 +176,13 @@ __device__ __forceinline__ Partial acc_to_partial(const Acc& a) {
   p.best_s = a.best_s;
   p.best_z = a.best_z;
   p.best_v = a.best_v;
-  p.pad = 0;
+  p.m2 = a.m2o;
   return p;
 }
 
-template <bool GUMBEL>
+template <int MODE>
 __device__ __forceinline__ Partial shfl_partial(const Partial& p, int o) {
+  constexpr bool GUMBEL = MODE != kModeGreedy, GREEDY = MODE != kModeGumbel;
   Partial q;
   q.m = __shfl_xor_sync(0xFFFFFFFFu, p.m, o);
   q.Z = __shfl_xor_sync(0xFFFFFFFFu, p.Z, o);
@@ -196,16 +197,16 @@ __device__ __forceinline__ Partial shfl_partial(const Partial& p, int o) {
     q.best_z = p.best_z;
     q.best_v = p.best_v;
   }
-  q.pad = 0;
+  q.m2 = GREEDY ? __shfl_xor_sync(0xFFFFFFFFu, p.m2, o) : p.m2;
   return q;
 }
 
-template <bool GUMBEL>
+template <int MODE>
 __device__ __forceinline__ Partial warp_combine(Partial part) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const Partial q = shfl_partial<GUMBEL>(part, o);
-    part_combine<GUMBEL>(part, q);
+    const Partial q = shfl_partial<MODE>(part, o);
+    part_combine<MODE>(part, q);
   }
   return part;
 }
@@ -281,18 +282,24 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long lon
 
 // x0, prob and entropy of one row from its full reduction.
 struct RowOut {
-  int32_t x0;
-  float prob, H;
+  int32_t x0, argmax;
+  float prob, H, margin;
 };
 
-template <bool GUMBEL>
+// The margin's runner-up is the largest z' without x0: the row's runner-up
+// when x0 is the argmax, else the max itself.
+template <int MODE>
 __device__ __forceinline__ RowOut row_out(const StatsParams& p, const Partial& r) {
+  constexpr bool GUMBEL = MODE != kModeGreedy;
   RowOut o;
   o.x0 = GUMBEL ? r.best_v : r.idx;
+  o.argmax = r.idx;
   const float zx = GUMBEL ? r.best_z : r.m;
   o.prob = ex2_approx((zx - r.m) * kLog2e) / r.Z;
   const float H = logf(r.Z) - r.S2 * kLn2 / r.Z;
   o.H = fminf(fmaxf(H, 0.0f), p.ln_veff);
+  const float r2 = (!GUMBEL || r.best_v == r.idx) ? r.m2 : r.m;
+  o.margin = o.prob - ex2_approx((r2 - r.m) * kLog2e) / r.Z;
   return o;
 }
 
@@ -305,6 +312,8 @@ __device__ int32_t finish_row(const StatsParams& p, int64_t row, const RowOut& o
   p.x0[row] = x0;
   p.prob[row] = prob;
   p.entropy[row] = H;
+  if (p.margin) p.margin[row] = o.margin;
+  if (p.argmax) p.argmax[row] = o.argmax;
   if (!p.fused) return -1;
 
   const RuleArgs& a = p.rule;
@@ -401,12 +410,12 @@ struct GumbelBest {
 // keeping it out of the streaming loop keeps that loop small.
 template <bool BF16>
 __device__ __noinline__ GumbelBest gumbel_exact(GumbelBest best, VecWords vw, GumbelWords r, int32_t v0, float t,
-                                                float t_ln2, float floor) {
+                                                float t_ln2, float floor, float s) {
   constexpr int EPV = BF16 ? 8 : 4;
 #pragma unroll 1
   for (int e = 0; e < EPV; ++e) {
     const uint32_t word = vw.w[BF16 ? (e >> 1) : e];
-    const float z = BF16 ? ((e & 1) ? bf16hi(word) : bf16lo(word)) : __uint_as_float(word);
+    const float z = __fmul_rn(BF16 ? ((e & 1) ? bf16hi(word) : bf16lo(word)) : __uint_as_float(word), s);
     const uint32_t re = r.w[e];
     const float w1 = __fsub_rn(1.0f, uniform_from_bits(re));
     const float bound = fmaf(t_ln2, -lg2_approx(w1), z + fmaf(fabsf(z), 1e-6f, 1e-3f));
@@ -422,14 +431,18 @@ __device__ __noinline__ GumbelBest gumbel_exact(GumbelBest best, VecWords vw, Gu
 }
 
 // Consumer-side state of one CTA.
-template <bool BF16, bool GUMBEL>
+template <bool BF16, int MODE>
 struct Consumer {
+  static constexpr bool GUMBEL = MODE != kModeGreedy;  // a Gumbel-max sample
+  static constexpr bool GREEDY = MODE != kModeGumbel;  // the argmax and its runner-up
   static constexpr int EPV = BF16 ? 8 : 4;  // elements per 16-byte vector
   const StatsParams& p;
   SharedCtl& ctl;
   uint32_t ring, chunk_bytes;
   int tid, warp, lane;
   float t, t_ln2;
+  float s;          // logit scale
+  uint64_t s2;      // (s, s)
   Acc acc;
   float warp_best;
 
@@ -440,6 +453,8 @@ struct Consumer {
     lane = tid & 31;
     t = p.temperature;
     t_ln2 = t * kLn2;
+    s = p.scale;
+    s2 = pack2(s, s);
     reset();
   }
 
@@ -497,8 +512,8 @@ struct Consumer {
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int32_t v0 = id0 + j * kConsumers * EPV;
-        for (int s = 0; s < p.n_sup; ++s) {
-          const int32_t off = p.sup[s] - v0;
+        for (int i = 0; i < p.n_sup; ++i) {
+          const int32_t off = p.sup[i] - v0;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (BF16) {
@@ -526,14 +541,24 @@ struct Consumer {
       }
       umax = kTopClamp;
     }
-    if (!GUMBEL) {
+    // Maxima of the scaled logits z' = z s (the scaling is monotone, so the
+    // max of the scaled elements is the scaled max, bit for bit).
+    float vms[NPT];
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) vms[j] = (FULL || valid[j]) ? __fmul_rn(vmax[j], s) : kMInit;
+    float umaxs = vms[0];
+#pragma unroll
+    for (int j = 1; j < NPT; ++j) umaxs = fmaxf(umaxs, vms[j]);
+    if (GREEDY) {
       // The first vector holding this thread's max (ids increase with j and
       // from unit to unit, so a strict > keeps the earliest), kept with its
-      // words; the element inside it is located once per row.
+      // words; the element inside it is located once per row.  Every other
+      // vector's max feeds the runner-up.
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
-        const bool better = vmax[j] > acc.vm;
-        acc.vm = better ? vmax[j] : acc.vm;
+        const bool better = vms[j] > acc.vm;
+        acc.m2o = fmaxf(acc.m2o, better ? acc.vm : vms[j]);
+        acc.vm = better ? vms[j] : acc.vm;
         acc.vv = better ? id0 + j * kConsumers * EPV : acc.vv;
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc.bw[k] = better ? w[j][k] : acc.bw[k];
@@ -541,7 +566,7 @@ struct Consumer {
     }
     // Branch-free rescale to the new running max (factor 1 when it did not grow).
     {
-      const float mnew = fmaxf(acc.m, umax);
+      const float mnew = fmaxf(acc.m, umaxs);
       const float d = (acc.m - mnew) * kLog2e;
       const float c = ex2_approx(d);
       const uint64_t d2 = pack2(d, d), c2 = pack2(c, c);
@@ -557,8 +582,8 @@ struct Consumer {
       if (!FULL && !valid[j]) continue;
 #pragma unroll
       for (int e = 0; e < EPV; e += 4) {
-        acc_pair2(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), negm2);
-        acc_pair2(Zb, Sb, elem(w[j], e + 2), elem(w[j], e + 3), negm2);
+        acc_pair2(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), negm2, s2);
+        acc_pair2(Zb, Sb, elem(w[j], e + 2), elem(w[j], e + 3), negm2, s2);
       }
     }
     acc.Z2 = add2(acc.Z2, Zb);
@@ -597,7 +622,7 @@ struct Consumer {
           // g = -ln(-ln u) <= -ln(1 - u) for every id of the vector; the
           // margin covers the fp32 rounding of ln_p, lg2.approx and the fmaf.
           const float w1 = __fsub_rn(1.0f, uniform_from_bits(rmax));
-          const float bound = fmaf(t_ln2, -lg2_approx(w1), vmax[j] + fmaf(fabsf(vmax[j]), 1e-6f, 1e-3f));
+          const float bound = fmaf(t_ln2, -lg2_approx(w1), vms[j] + fmaf(fabsf(vms[j]), 1e-6f, 1e-3f));
           survive[q] = (FULL || valid[j]) && !(bound < warp_best);
         }
 #pragma unroll
@@ -610,7 +635,7 @@ struct Consumer {
 #pragma unroll
               for (int k = 0; k < 4; ++k) vw.w[k] = w[j][k];
               GumbelBest b{acc.best_s, acc.best_v, acc.best_z};
-              b = gumbel_exact<BF16>(b, vw, r[q], id0 + j * kConsumers * EPV, t, t_ln2, warp_best);
+              b = gumbel_exact<BF16>(b, vw, r[q], id0 + j * kConsumers * EPV, t, t_ln2, warp_best, s);
               updated = b.s > acc.best_s;
               acc.best_s = b.s;
               acc.best_v = b.v;
@@ -665,12 +690,13 @@ struct Consumer {
       z = __ldg(reinterpret_cast<const float*>(rowp) + v);
     }
     z = sanitize(z);
-    for (int s = 0; s < p.n_sup; ++s)
-      if (p.sup[s] == v) z = kAbsent;
-    if (z > acc.m) acc_rescale(acc, z);
+    for (int i = 0; i < p.n_sup; ++i)
+      if (p.sup[i] == v) z = kAbsent;
+    const float zs = __fmul_rn(z, s);
+    if (zs > acc.m) acc_rescale(acc, zs);
     acc.idx = static_cast<int32_t>(v);  // one tail element per thread
-    acc.vm_tail = z;
-    const float y = (z - acc.m) * kLog2e;
+    acc.vm_tail = zs;
+    const float y = fmaf(z, s, acc.negm) * kLog2e;
     const float e = ex2_approx(y);
     acc.Z2 = add2(acc.Z2, pack2(e, 0.0f));
     acc.S2 = fma2(pack2(e, 0.0f), pack2(y, 0.0f), acc.S2);
@@ -679,11 +705,11 @@ struct Consumer {
                                     static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32), 0u, p.keys);
       const int w = static_cast<int>(v & 3);
       const uint32_t word = w == 0 ? o.x : (w == 1 ? o.y : (w == 2 ? o.z : o.w));
-      const float s = gumbel_score(z, t, word);
-      if (s > acc.best_s) {
-        acc.best_s = s;
+      const float sc = gumbel_score(zs, t, word);
+      if (sc > acc.best_s) {
+        acc.best_s = sc;
         acc.best_v = static_cast<int32_t>(v);
-        acc.best_z = z;
+        acc.best_z = zs;
       }
     }
   }
@@ -691,29 +717,43 @@ struct Consumer {
   // Greedy x0 bookkeeping: the first id holding this thread's max acc.m.  It
   // is in the best full vector (whose sanitized words the thread kept; its
   // ids are below every tail element) unless the tail element is larger.
+  // The thread's runner-up is the largest of its other vectors' maxima, the
+  // best vector's other elements and the tail element, whichever is not idx.
   __device__ void resolve_index() {
-    if (GUMBEL) return;
+    if (!GREEDY) return;
     int32_t idx = 0x7FFFFFFF;
+    float r2 = acc.m2o;
     if (acc.vv >= 0 && acc.vm == acc.m) {
+      bool found = false;
 #pragma unroll
-      for (int e = EPV - 1; e >= 0; --e)
-        if (elem(acc.bw, e) == acc.vm) idx = acc.vv + e;
+      for (int e = 0; e < EPV; ++e) {
+        const float ze = __fmul_rn(elem(acc.bw, e), s);
+        if (!found && ze == acc.vm) {
+          idx = acc.vv + e;
+          found = true;
+        } else {
+          r2 = fmaxf(r2, ze);
+        }
+      }
+      r2 = fmaxf(r2, acc.vm_tail);
     } else if (acc.vm_tail == acc.m && acc.m > kMInit) {
       idx = acc.idx;
+      r2 = fmaxf(r2, acc.vm);
     }
     acc.idx = idx;
+    acc.m2o = r2;
   }
 
   // Whether suppressed ids fall in [lo, hi) (the same answer in every thread).
   __device__ bool has_sup(int64_t lo, int64_t hi) const {
     bool any = false;
-    for (int s = 0; s < p.n_sup; ++s) any |= (p.sup[s] >= lo && p.sup[s] < hi);
+    for (int i = 0; i < p.n_sup; ++i) any |= (p.sup[i] >= lo && p.sup[i] < hi);
     return any;
   }
 
   // The CTA's reduction of all consumer states; valid in thread 0.
   __device__ Partial cta_reduce() {
-    Partial part = warp_combine<GUMBEL>(acc_to_partial(acc));
+    Partial part = warp_combine<MODE>(acc_to_partial(acc));
     if (lane == 0) ctl.warp_part[warp] = part;
     named_sync(1, kConsumers);
     Partial r = empty_partial();
@@ -721,8 +761,8 @@ struct Consumer {
       if (lane < kConsumerWarps) r = ctl.warp_part[lane];
 #pragma unroll
       for (int o = kConsumerWarps / 2; o > 0; o >>= 1) {
-        const Partial q = shfl_partial<GUMBEL>(r, o);
-        part_combine<GUMBEL>(r, q);
+        const Partial q = shfl_partial<MODE>(r, o);
+        part_combine<MODE>(r, q);
       }
     }
     return r;
@@ -833,7 +873,7 @@ __device__ __forceinline__ void release_unit(SharedCtl& ctl, const RingPos& r, i
 // ---------------------------------------------------------------------------
 // Persistent kernel: many rows.  CTA c owns units [c U / P, (c+1) U / P).
 // ---------------------------------------------------------------------------
-template <bool BF16, bool GUMBEL>
+template <bool BF16, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constant__ StatsParams p) {
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ SharedCtl ctl;
@@ -870,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
     return;
   }
 
-  Consumer<BF16, GUMBEL> con(p, ctl, ring, chunk_bytes);
+  Consumer<BF16, MODE> con(p, ctl, ring, chunk_bytes);
   uint8_t* rule_smem = dsmem + static_cast<size_t>(p.stages) * chunk_bytes;
   volatile int32_t* abort_flag = &ctl.abort_flag;
   int64_t cur_row = -1, seg_uk0 = 0;
@@ -915,16 +955,16 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
         const int64_t cc = cb + lane;
         Partial q = empty_partial();
         if (cc <= c1) q = load_partial(p.partials + 2 * cc + ((cc == c0 && c0_tail) ? 1 : 0));
-        part_combine<GUMBEL>(tot, q);
+        part_combine<MODE>(tot, q);
       }
-      tot = warp_combine<GUMBEL>(tot);
+      tot = warp_combine<MODE>(tot);
       if (lane == 0) {
         p.row_count[row] = 0;
         ctl.result = tot;
       }
     }
     if (tid == 0) {
-      ctl.flag2 = action != 0 ? finish_row(p, row, row_out<GUMBEL>(p, ctl.result), RowPre()) : -1;
+      ctl.flag2 = action != 0 ? finish_row(p, row, row_out<MODE>(p, ctl.result), RowPre()) : -1;
       ctl.cta_best = float_key(kNegInf);  // the next row starts with no pruning floor
     }
     named_sync(1, kConsumers);
@@ -964,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
 // tail).  Rank 0 combines the CTAs' partials through distributed shared
 // memory and finishes the row.
 // ---------------------------------------------------------------------------
-template <bool BF16, bool GUMBEL>
+template <bool BF16, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid_constant__ StatsParams p) {
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ SharedCtl ctl;
@@ -1006,7 +1046,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
     return;
   }
 
-  Consumer<BF16, GUMBEL> con(p, ctl, ring, chunk_bytes);
+  Consumer<BF16, MODE> con(p, ctl, ring, chunk_bytes);
   // Rank 0 finishes the row; its candidate flag and canvas token are loaded
   // now so they are at hand then (after the grid dependency in early mode).
   RowPre pre;
@@ -1037,11 +1077,11 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
     // exit and free their SM slots while rank 0 finishes the row).
     Partial tot = empty_partial();
     if (warp == 0)
-      for (int k = lane; k < S; k += 32) part_combine<GUMBEL>(tot, load_partial_dsmem(&ctl.result, k));
+      for (int k = lane; k < S; k += 32) part_combine<MODE>(tot, load_partial_dsmem(&ctl.result, k));
     __syncwarp();
     cluster_arrive();
     RowOut o{};
-    if (warp == 0) o = row_out<GUMBEL>(p, warp_combine<GUMBEL>(tot));
+    if (warp == 0) o = row_out<MODE>(p, warp_combine<MODE>(tot));
     // Everything above touched only this cluster's own memory.  In early mode
     // the wait for the previous kernel comes here, so that only the row's
     // writes (outputs, canvas, batch-row counters) follow that kernel's end.
@@ -1063,27 +1103,36 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
 }
 
 // Explicit instantiations used by the launcher.
-template __global__ void stats_kernel<false, false>(const __grid_constant__ StatsParams);
-template __global__ void stats_kernel<true, false>(const __grid_constant__ StatsParams);
-template __global__ void stats_kernel<false, true>(const __grid_constant__ StatsParams);
-template __global__ void stats_kernel<true, true>(const __grid_constant__ StatsParams);
-template __global__ void stats_cluster_kernel<false, false>(const __grid_constant__ StatsParams);
-template __global__ void stats_cluster_kernel<true, false>(const __grid_constant__ StatsParams);
-template __global__ void stats_cluster_kernel<false, true>(const __grid_constant__ StatsParams);
-template __global__ void stats_cluster_kernel<true, true>(const __grid_constant__ StatsParams);
+#define DLLM_STATS_INSTANTIATE(BF, MODE)                                                   \
+  template __global__ void stats_kernel<BF, MODE>(const __grid_constant__ StatsParams);   \
+  template __global__ void stats_cluster_kernel<BF, MODE>(const __grid_constant__ StatsParams);
+DLLM_STATS_INSTANTIATE(false, kModeGreedy)
+DLLM_STATS_INSTANTIATE(true, kModeGreedy)
+DLLM_STATS_INSTANTIATE(false, kModeGumbel)
+DLLM_STATS_INSTANTIATE(true, kModeGumbel)
+DLLM_STATS_INSTANTIATE(false, kModeDual)
+DLLM_STATS_INSTANTIATE(true, kModeDual)
+#undef DLLM_STATS_INSTANTIATE
 
-const void* stats_kernel_ptr(bool bf16, bool gumbel) {
-  if (bf16) return gumbel ? reinterpret_cast<const void*>(&stats_kernel<true, true>)
-                          : reinterpret_cast<const void*>(&stats_kernel<true, false>);
-  return gumbel ? reinterpret_cast<const void*>(&stats_kernel<false, true>)
-                : reinterpret_cast<const void*>(&stats_kernel<false, false>);
+template <bool BF16>
+const void* pick(int mode, bool cluster) {
+  switch (mode) {
+    case kModeGumbel:
+      return cluster ? reinterpret_cast<const void*>(&stats_cluster_kernel<BF16, kModeGumbel>)
+                     : reinterpret_cast<const void*>(&stats_kernel<BF16, kModeGumbel>);
+    case kModeDual:
+      return cluster ? reinterpret_cast<const void*>(&stats_cluster_kernel<BF16, kModeDual>)
+                     : reinterpret_cast<const void*>(&stats_kernel<BF16, kModeDual>);
+    default:
+      return cluster ? reinterpret_cast<const void*>(&stats_cluster_kernel<BF16, kModeGreedy>)
+                     : reinterpret_cast<const void*>(&stats_kernel<BF16, kModeGreedy>);
+  }
 }
 
-const void* stats_cluster_kernel_ptr(bool bf16, bool gumbel) {
-  if (bf16) return gumbel ? reinterpret_cast<const void*>(&stats_cluster_kernel<true, true>)
-                          : reinterpret_cast<const void*>(&stats_cluster_kernel<true, false>);
-  return gumbel ? reinterpret_cast<const void*>(&stats_cluster_kernel<false, true>)
-                : reinterpret_cast<const void*>(&stats_cluster_kernel<false, false>);
+const void* stats_kernel_ptr(bool bf16, int mode) { return bf16 ? pick<true>(mode, false) : pick<false>(mode, false); }
+
+const void* stats_cluster_kernel_ptr(bool bf16, int mode) {
+  return bf16 ? pick<true>(mode, true) : pick<false>(mode, true);
 }
 
 }  // namespace dllm

@@ -18,15 +18,21 @@ constexpr int kRingBytes = 64 * 1024;
 constexpr int kFusedSortCap = 1024;              // largest L the fused sorting rules take
 constexpr int kMaxCtasPerSm = 4;
 
-// Partial reduction of one row segment: max m, Z = sum 2^y and S2 = sum 2^y y
-// with y = (z - m) log2(e), the first index of m, and the best Gumbel score
-// with its id and logit.
+// What a row's pass tracks: the greedy argmax (with the runner-up), the
+// Gumbel-max sample, or both (a sample plus its row's argmax and runner-up,
+// for the margin and argmax outputs).
+enum : int { kModeGreedy = 0, kModeGumbel = 1, kModeDual = 2, kModes = 3 };
+
+// Partial reduction of one row segment, in scaled logits z' = z s: max m,
+// Z = sum 2^y and S2 = sum 2^y y with y = (z' - m) log2(e), the first index
+// of m, the best Gumbel score with its id and scaled logit, and m2, the
+// largest z' of the segment without the element at idx (the runner-up).
 struct alignas(16) Partial {
   float m, Z, S2;
   int32_t idx;
   float best_s, best_z;
   int32_t best_v;
-  int32_t pad;
+  float m2;
 };
 
 struct StatsParams {
@@ -42,6 +48,7 @@ struct StatsParams {
   int32_t P;                // CTAs in the grid
   int32_t stages;           // ring stages
   float temperature;
+  float scale;              // logit scale s: every statistic is of z' = fp32(z s)
   PhiloxSchedule keys;      // Philox round keys of the caller's key
   int32_t n_sup;
   int32_t sup[DLLM_MAX_SUPPRESS];  // sorted, distinct
@@ -49,6 +56,8 @@ struct StatsParams {
   int32_t* x0;
   float* prob;
   float* entropy;
+  float* margin;            // (T) or nullptr: prob(x0) - prob(runner-up)
+  int32_t* argmax;          // (T) or nullptr: first id of the largest z'
   int32_t* fault;
   int32_t* row_count;       // (T) contributions that arrived, split rows only
   // (B) per batch row, four 16-bit fields: rows finished | candidates | commits | edits

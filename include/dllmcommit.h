@@ -98,6 +98,42 @@ dllm_status dllm_token_stats(const void* logits, dllm_dtype dt, int64_t B, int64
                              void* workspace, size_t workspace_bytes, dllm_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Extended statistics: scaled logits, margin confidence, greedy argmax
+ * beside a sample.
+ *
+ * [MOJO] "Row statistics on the device": besides p = 1/Z, the sampler
+ * finishes topk_margin as p minus the runner-up's probability, the runner-up
+ * being the largest logit at any other index.  [ARS] "Uniform-noise decoding
+ * (DiffusionGemma)": the loop divides the logits by a temperature, measures
+ * the entropy of the scaled softmax, keeps the argmax canvas and draws a
+ * categorical sample from the same scaled logits.
+ *
+ * All statistics are those of z' = fp32(z * logit_scale) (one fp32
+ * multiplication of the sanitised logit; 1 = unscaled).  x0 is the first
+ * argmax of z' (temperature 0) or the Gumbel-max sample of z' (temperature t;
+ * t = 1 samples softmax(z')), prob and entropy are those of softmax(z').
+ *   margin  prob(x0) - prob(r), r the largest z' over A without x0 (its
+ *           probability counts as 0 when A = {x0}).  Negative only when a
+ *           sample is not the argmax.
+ *   argmax  the first id of the largest z' (equals x0 when temperature == 0).
+ * Within tolerance, prob/entropy/margin follow from z * logit_scale rounded
+ * once; x0 and argmax are decided on fp32(z * logit_scale) exactly.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  float logit_scale;        /* 0 < logit_scale <= 256 (else DLLM_ERR_INVALID_ARGUMENT) */
+  float* margin;            /* device (B, L) output or NULL */
+  int32_t* argmax;          /* device (B, L) output or NULL */
+} dllm_stats_ex;
+
+/* dllm_token_stats with the options above (ex == NULL: plain token_stats).
+ * Same arguments, workspace and errors otherwise. */
+dllm_status dllm_token_stats_ex(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,
+                                int64_t row_stride, float temperature, uint64_t key,
+                                const int32_t* suppress_ids, int32_t n_suppress, const dllm_stats_ex* ex,
+                                int32_t* x0, float* prob, float* entropy,
+                                void* workspace, size_t workspace_bytes, dllm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Statistics pass that allocates nothing.  The pages have no counterpart:
  * this entry point is an addition of this library.
  *
@@ -233,6 +269,8 @@ typedef struct {
   int64_t canvas_offset;    /* canvas column of position l = 0 */
   int32_t* counts;          /* device (B, 3) or NULL: per batch row [candidates, commits, edits] */
   int32_t flags;            /* 0, or DLLM_FLAG_INPUTS_READY */
+  const dllm_stats_ex* ex;  /* NULL, or the extended statistics options (scale, margin, argmax);
+                               the rules then decide on the scaled statistics */
 } dllm_commit_params;
 
 /* The logits and the candidate mask (when one is given) were complete before

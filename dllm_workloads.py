@@ -32,7 +32,7 @@ LLADA_VOCAB = 126464
 LLADA_MASK_ID = 126336
 DREAM_VOCAB = 152064
 
-_TAGS = {"tiny": 1, "llada": 2, "dream": 3, "large": 4, "loop": 5}
+_TAGS = {"tiny": 1, "llada": 2, "dream": 3, "large": 4, "loop": 5, "uniform": 6}
 
 
 def _rng(*entropy: int) -> np.random.Generator:
@@ -314,3 +314,102 @@ class LoopGenerator:
 
 def loop_spec(seed: int = 0) -> LoopSpec:
     return LoopSpec(seed=seed)
+
+
+# --------------------------------------------------------------------------
+# Uniform-noise decoding (DiffusionGemma-style canvas denoising).
+#
+# A stand-in for the model: every canvas position (b, j) has a target id and
+# an onset step.  Before its onset the position's logits are a background row
+# (one of a bank of seeded N(0, 1) rows, drawn afresh at every step), so its
+# prediction is uncertain (entropy near ln V) and its argmax wanders; from its
+# onset on, the row also carries a peak of height `peak` at the target, so the
+# prediction is confident and stable.  The canvas the loop feeds back is not
+# read (self-conditioning stays with a real model).  Entropies are thus
+# either tiny or large, far from the acceptance budget and the stopping
+# threshold, which keeps every decision of the loop away from rounding.
+# --------------------------------------------------------------------------
+
+GEMMA_VOCAB = 262144
+
+
+@dataclasses.dataclass
+class UniformSpec:
+    B: int = 1
+    N: int = 256                 # canvas length
+    V: int = GEMMA_VOCAB
+    dtype: str = "bf16"
+    num_steps: int = 48
+    entropy_bound: float = 0.1
+    t_min: float = 0.4
+    t_max: float = 0.8
+    stability_threshold: int = 1
+    confidence_threshold: float = 0.005
+    key: int = 0x5EED_0001
+    seed: int = 0
+    bank_rows: int = 64
+    peak: float = 24.0
+    max_onset: int = 24          # onsets are uniform in [0, max_onset]
+
+
+class UniformGenerator:
+    """Per-step logits of the uniform-noise loop (host numpy and device torch forms)."""
+
+    def __init__(self, spec: UniformSpec):
+        self.spec = s = spec
+        tag = _TAGS["uniform"]
+        g = _rng(s.seed, tag, 1)
+        self.targets = g.integers(0, s.V, size=(s.B, s.N)).astype(np.int64)
+        self.onset = g.integers(0, s.max_onset + 1, size=(s.B, s.N)).astype(np.int64)
+
+        def make_row(r):
+            return _rng(s.seed, tag, 3, r).standard_normal(s.V, dtype=np.float32)
+
+        self.bank_src = _fill_rows(make_row, np.arange(s.bank_rows), s.V, np.float32)
+        self.bank = f32_to_bf16_bits(self.bank_src) if s.dtype == "bf16" else self.bank_src
+        self._dev = None
+
+    def _rows(self, step: int):
+        s = self.spec
+        pick = _rng(s.seed, _TAGS["uniform"], 4, step).integers(0, s.bank_rows, size=(s.B, s.N))
+        on = self.onset <= step                                        # (B, N) confident positions
+        flat = np.flatnonzero(on.reshape(-1))
+        tgt = self.targets.reshape(-1)[flat]
+        val = (self.bank_src[pick.reshape(-1)[flat], tgt] + np.float32(s.peak)).astype(np.float32)
+        if s.dtype == "bf16":
+            val = f32_to_bf16_bits(val)
+        return pick.reshape(-1), flat, tgt, val
+
+    def host_logits(self, step: int) -> np.ndarray:
+        """(B*N, V) logits of step `step` (uint16 bf16 bits, or float32)."""
+        pick, flat, tgt, val = self._rows(step)
+        out = self.bank[pick].copy()
+        out[flat, tgt] = val
+        return out
+
+    def device_logits(self, step: int, out=None):
+        """The same rows as :meth:`host_logits`, assembled on the GPU with torch."""
+        import torch
+
+        s = self.spec
+        if self._dev is None:
+            if s.dtype == "bf16":
+                self._dev = torch.from_numpy(self.bank.view(np.int16)).cuda().view(torch.bfloat16)
+            else:
+                self._dev = torch.from_numpy(self.bank).cuda()
+        pick, flat, tgt, val = self._rows(step)
+        rows = torch.index_select(self._dev, 0, torch.from_numpy(pick).cuda())
+        if out is not None:
+            out.copy_(rows)
+            rows = out
+        if flat.size:
+            pos = torch.from_numpy((flat * s.V + tgt).astype(np.int64)).cuda()
+            if s.dtype == "bf16":
+                rows.view(torch.int16).view(-1).index_copy_(0, pos, torch.from_numpy(val.view(np.int16)).cuda())
+            else:
+                rows.view(-1).index_copy_(0, pos, torch.from_numpy(val).cuda())
+        return rows
+
+
+def uniform_spec(**kw) -> UniformSpec:
+    return UniformSpec(**kw)

@@ -46,6 +46,10 @@ def lib():
         L.orc_transfer_schedule.argtypes = [P, i64, i32, P]
         L.orc_block_ranges.argtypes = [i64, i64, i64, C.c_int, P, i64, P]
         L.orc_default_threads.argtypes = []
+        L.orc_linear_temperature.argtypes = [i32, i32, f32, f32, P]
+        L.orc_uniform_canvas.argtypes = [i64, i64, i64, u64, P]
+        L.orc_renoise.argtypes = [P, P, P, i64, P]
+        L.orc_stable_confident_stop.argtypes = [P, P, i64, i64, i32, f32, P, P, P]
         _lib = L
     return _lib
 
@@ -199,3 +203,50 @@ def block_ranges(P, gen_len, block_len, align=False):
     out = np.zeros((int(n[0]), 2), dtype=np.int64)
     _check(lib().orc_block_ranges(int(P), int(gen_len), int(block_len), int(bool(align)), _p(out), out.shape[0], _p(n)), "block_ranges")
     return [tuple(map(int, r)) for r in out]
+
+
+# ---------------------------------------------------------------------------
+# uniform-noise decoding helpers
+# ---------------------------------------------------------------------------
+def linear_temperature(remaining: int, num_steps: int, t_min: float = 0.4, t_max: float = 0.8) -> np.float32:
+    T = C.c_float(0.0)
+    _check(lib().orc_linear_temperature(int(remaining), int(num_steps), float(t_min), float(t_max), C.byref(T)),
+           "linear_temperature")
+    return np.float32(T.value)
+
+
+def uniform_canvas(B: int, N: int, V: int, key: int) -> np.ndarray:
+    out = np.zeros((B, N), dtype=np.int32)
+    _check(lib().orc_uniform_canvas(int(B), int(N), int(V), int(key) & (2**64 - 1), _p(out)), "uniform_canvas")
+    return out
+
+
+def renoise(sample, accepted, noise) -> np.ndarray:
+    s = np.ascontiguousarray(sample, dtype=np.int32)
+    a = np.ascontiguousarray(accepted, dtype=np.uint8)
+    n = np.ascontiguousarray(noise, dtype=np.int32)
+    if not (s.shape == a.shape == n.shape):
+        raise ValueError("renoise: shapes differ")
+    out = np.zeros_like(s)
+    _check(lib().orc_renoise(_p(s), _p(a), _p(n), s.size, _p(out)), "renoise")
+    return out
+
+
+class StableConfidentStopping:
+    """The oracle's stopping criterion with its state (prev canvas, count)."""
+
+    def __init__(self, B: int, L: int, stability_threshold: int = 1, confidence_threshold: float = 0.005):
+        self.prev = np.zeros((B, L), dtype=np.int32)
+        self.count = np.full(B, -1, dtype=np.int32)
+        self.stability_threshold = int(stability_threshold)
+        self.confidence_threshold = float(confidence_threshold)
+
+    def __call__(self, argmax, entropy) -> np.ndarray:
+        am = np.ascontiguousarray(argmax, dtype=np.int32)
+        en = np.ascontiguousarray(entropy, dtype=np.float32)
+        B, L = am.shape
+        stop = np.zeros(B, dtype=np.uint8)
+        _check(lib().orc_stable_confident_stop(_p(am), _p(en), B, L, self.stability_threshold,
+                                               self.confidence_threshold, _p(self.prev), _p(self.count), _p(stop)),
+               "stable_confident_stop")
+        return stop

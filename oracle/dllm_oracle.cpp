@@ -296,7 +296,7 @@ int orc_token_stats_ex(const void* logits, int dtype, int64_t n_rows, int64_t V,
                        int n_threads) {
   if (n_rows < 0 || V <= 0 || row_stride < V || (dtype != 0 && dtype != 1)) return -1;
   if (!(temperature >= 0.0f) || n_suppress < 0) return -1;
-  if (!(logit_scale > 0.0f) || !(logit_scale <= 65536.0f)) return -1;
+  if (!(logit_scale > 0.0f) || !(logit_scale <= 256.0f)) return -1;
   if (n_rows == 0) return 0;
   if (!logits || !x0 || !prob || !entropy) return -1;
   std::vector<uint8_t> absent(static_cast<size_t>(V), 0);
@@ -485,6 +485,73 @@ int orc_block_ranges(int64_t P, int64_t gen_len, int64_t block_len, int align,
   }
   *n_out = n;
   return n > cap ? -2 : 0;
+}
+
+// The helpers of uniform-noise decoding.  [ARS] function table
+// (linear_temperature, uniform_canvas, renoise, StableConfidentStopping) and
+// "Uniform-noise decoding (DiffusionGemma)": the canvas starts as uniformly
+// random tokens, the temperature decays linearly with the steps that remain,
+// the positions not accepted are re-noised, and a row stops once its argmax
+// canvas is stable and confident.
+
+// T = t_min + (t_max - t_min) remaining / num_steps, in double, rounded to fp32.
+int orc_linear_temperature(int32_t remaining, int32_t num_steps, float t_min, float t_max, float* T) {
+  if (num_steps <= 0 || remaining < 0 || remaining > num_steps || !T) return -1;
+  if (!(t_min > 0.0f) || !(t_max >= t_min) || std::isinf(t_max)) return -1;
+  const double frac = static_cast<double>(remaining) / static_cast<double>(num_steps);
+  *T = static_cast<float>(static_cast<double>(t_min) + (static_cast<double>(t_max) - t_min) * frac);
+  return 0;
+}
+
+// canvas[b, j] = floor(r V / 2^32), r = Philox4x32-10(counter (j >> 2, b lo,
+// b hi, 1), key (lo, hi)), word j & 3: every token of [0, V) is drawn with
+// probability within V / 2^32 of 1 / V.
+int orc_uniform_canvas(int64_t B, int64_t N, int64_t V, uint64_t key, int32_t* canvas) {
+  if (B < 0 || N < 0 || V <= 0 || V > INT32_MAX || (B * N > 0 && !canvas)) return -1;
+  const uint32_t k[2] = {static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32)};
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t j = 0; j < N; ++j) {
+      const uint32_t ctr[4] = {static_cast<uint32_t>(j >> 2), static_cast<uint32_t>(b),
+                               static_cast<uint32_t>(static_cast<uint64_t>(b) >> 32), 1u};
+      uint32_t out[4];
+      philox(ctr, k, out);
+      const uint64_t r = out[j & 3];
+      canvas[b * N + j] = static_cast<int32_t>((r * static_cast<uint64_t>(V)) >> 32);
+    }
+  }
+  return 0;
+}
+
+// out[i] = accepted[i] ? sample[i] : noise[i].
+int orc_renoise(const int32_t* sample, const uint8_t* accepted, const int32_t* noise, int64_t n, int32_t* out) {
+  if (n < 0 || (n > 0 && (!sample || !accepted || !noise || !out))) return -1;
+  for (int64_t i = 0; i < n; ++i) out[i] = accepted[i] ? sample[i] : noise[i];
+  return 0;
+}
+
+// One call of the stopping criterion on the (B, L) argmax canvas and
+// entropies.  count[b] < 0 means no previous canvas.  A row is stable when
+// its canvas equals the previous one; count[b] counts consecutive stable
+// calls; the row is confident when its mean entropy (summed in double in
+// position order, divided by L) is below confidence_threshold.  stop[b] =
+// count[b] >= stability_threshold and confident.  prev takes the canvas.
+int orc_stable_confident_stop(const int32_t* argmax, const float* entropy, int64_t B, int64_t L,
+                              int32_t stability_threshold, float confidence_threshold, int32_t* prev,
+                              int32_t* count, uint8_t* stop) {
+  if (B < 0 || L <= 0 || (B > 0 && (!argmax || !entropy || !prev || !count || !stop))) return -1;
+  for (int64_t b = 0; b < B; ++b) {
+    bool same = count[b] >= 0;
+    double sum = 0.0;
+    for (int64_t l = 0; l < L; ++l) {
+      same = same && argmax[b * L + l] == prev[b * L + l];
+      sum += static_cast<double>(entropy[b * L + l]);
+    }
+    count[b] = same ? count[b] + 1 : 0;
+    for (int64_t l = 0; l < L; ++l) prev[b * L + l] = argmax[b * L + l];
+    const bool confident = sum / static_cast<double>(L) < static_cast<double>(confidence_threshold);
+    stop[b] = (count[b] >= stability_threshold && confident) ? 1 : 0;
+  }
+  return 0;
 }
 
 }  // extern "C"

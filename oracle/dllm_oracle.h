@@ -43,7 +43,7 @@ int orc_token_stats(const void* logits, int dtype, int64_t n_rows, int64_t V, in
                     int32_t* x0, double* prob, double* entropy, int n_threads);
 
 /* The same pass on scaled logits z' = fp32(z * logit_scale), 0 < logit_scale
- * <= 65536 (1 = orc_token_stats).  margin (nullable): prob(x0) minus the
+ * <= 256 (1 = orc_token_stats).  margin (nullable): prob(x0) minus the
  * probability of the runner-up, the largest z' over the token set without
  * x0.  argmax (nullable): the first id of the largest z' (equal to x0 when
  * temperature == 0). */
@@ -69,6 +69,21 @@ int orc_edit_transfer(const int32_t* x0, const float* prob, const int32_t* token
 int orc_transfer_schedule(const int32_t* counts, int64_t B, int32_t steps, int32_t* quotas);
 int orc_block_ranges(int64_t P, int64_t gen_len, int64_t block_len, int align,
                      int64_t* ranges, int64_t cap, int64_t* n_out);
+
+/* Uniform-noise decoding helpers ("dLLM block decoding", function table and
+ * "Uniform-noise decoding (DiffusionGemma)").
+ * linear_temperature: T = fp32(t_min + (t_max - t_min) remaining / num_steps).
+ * uniform_canvas: (B, N) tokens floor(r V / 2^32), r the Philox4x32-10 word
+ *   j & 3 of counter (j >> 2, b lo, b hi, 1) under key.
+ * renoise: out = accepted ? sample : noise, elementwise.
+ * stable_confident_stop: one call of the stopping criterion; state prev
+ *   (B, L) and count (B) (count < 0: no previous canvas). */
+int orc_linear_temperature(int32_t remaining, int32_t num_steps, float t_min, float t_max, float* T);
+int orc_uniform_canvas(int64_t B, int64_t N, int64_t V, uint64_t key, int32_t* canvas);
+int orc_renoise(const int32_t* sample, const uint8_t* accepted, const int32_t* noise, int64_t n, int32_t* out);
+int orc_stable_confident_stop(const int32_t* argmax, const float* entropy, int64_t B, int64_t L,
+                              int32_t stability_threshold, float confidence_threshold, int32_t* prev,
+                              int32_t* count, uint8_t* stop);
 
 /* Threads orc_token_stats uses when asked for 0. */
 int orc_default_threads(void);

@@ -19,7 +19,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import block_ranges, edit_transfer, threshold_transfer, token_stats
+from . import (StableConfidentStopping, block_ranges, edit_transfer, entropy_bound_transfer, linear_temperature,
+               renoise, threshold_transfer, token_stats, token_stats_ex, uniform_canvas)
 
 
 def decode_with_editing(model, prompt: np.ndarray, *, gen_len: int, block_len: int, mask_id: int,
@@ -56,3 +57,57 @@ def decode_with_editing(model, prompt: np.ndarray, *, gen_len: int, block_len: i
             if not has_mask and not edit.any():
                 break
     return x[:, P:P + gen_len], forwards
+
+
+def uniform_keys(key: int, step: int):
+    """The Philox keys of one step of the uniform-noise loop: the initial
+    canvas uses `key` (step 0); step i >= 1 samples with key + 2i - 1 and
+    re-noises with key + 2i (mod 2^64)."""
+    m = 2**64
+    return (key + 2 * step - 1) % m, (key + 2 * step) % m
+
+
+def decode_uniform(model, *, batch: int, canvas_len: int, vocab_size: int, key: int, num_steps: int = 48,
+                   entropy_bound: float = 0.1, t_min: float = 0.4, t_max: float = 0.8, stability_threshold: int = 1,
+                   confidence_threshold: float = 0.005, dtype: str = "bf16", suppress_ids=(), n_threads: int = 0,
+                   trace=None):
+    """Uniform-noise decoding, composed from the oracle's primitives.
+
+    Follows the loop of the mlx-arsenal "dLLM block decoding" notes, section
+    "Uniform-noise decoding (DiffusionGemma)": the canvas starts uniformly
+    random; at every step the logits are divided by the linearly decaying
+    temperature, the entropy and argmax of the scaled softmax are taken and a
+    categorical sample drawn from it; the lowest-entropy positions are
+    accepted under the entropy budget (over all positions), every other
+    position is re-noised; rows that met the stopping criterion are frozen;
+    the loop ends when every row stopped or the steps ran out.  The scaled
+    logits are z' = fp32(z * fp32(1 / T)); the categorical sample is the
+    Gumbel-max sample at temperature 1 of z'.  ``model(step_index, canvas)``
+    returns the (B * N, V) logits.  Returns (argmax canvas (B, N), steps).
+    """
+    B, N, V = batch, canvas_len, vocab_size
+    canvas = uniform_canvas(B, N, V, key)
+    stop = StableConfidentStopping(B, N, stability_threshold, confidence_threshold)
+    everywhere = np.ones((B, N), dtype=np.uint8)
+    done = np.zeros(B, dtype=bool)
+    argmax = canvas.copy()
+    steps = 0
+    for remaining in range(num_steps, 0, -1):
+        steps += 1
+        T = linear_temperature(remaining, num_steps, t_min, t_max)
+        s = np.float32(1.0 / float(T))
+        k_sample, k_noise = uniform_keys(key, steps)
+        logits = model(steps - 1, canvas)
+        sample, _, ent, _, am = token_stats_ex(logits, dtype=dtype, temperature=1.0, key=k_sample, logit_scale=s,
+                                               suppress_ids=suppress_ids, n_threads=n_threads)
+        ent32 = ent.astype(np.float32).reshape(B, N)        # entropies are float32 values
+        accepted = entropy_bound_transfer(ent32, everywhere, entropy_bound)
+        new_canvas = renoise(sample.reshape(B, N), accepted, uniform_canvas(B, N, V, k_noise))
+        argmax = np.where(done[:, None], argmax, am.reshape(B, N))
+        canvas = np.where(done[:, None], canvas, new_canvas)
+        done = done | (stop(argmax, ent32) != 0)
+        if trace is not None:
+            trace.append((steps, int(accepted.sum()), int(done.sum())))
+        if done.all():
+            break
+    return argmax, steps

@@ -33,7 +33,8 @@ EXPORTS = (
     "dllm_status_string", "dllm_version", "dllm_token_stats_workspace_size", "dllm_token_stats",
     "dllm_threshold_transfer", "dllm_topk_transfer", "dllm_factor_transfer", "dllm_entropy_bound_transfer",
     "dllm_edit_transfer", "dllm_transfer_schedule", "dllm_block_ranges", "dllm_commit_step",
-    "dllm_workspace_fault", "dllm_token_stats_noalloc", "dllm_token_stats_ex",
+    "dllm_workspace_fault", "dllm_token_stats_noalloc", "dllm_token_stats_ex", "dllm_linear_temperature",
+    "dllm_uniform_canvas", "dllm_renoise", "dllm_stable_confident_stop",
 )
 
 
@@ -85,6 +86,10 @@ def _load() -> C.CDLL:
     lib.dllm_workspace_fault.argtypes = [P, P, C.POINTER(C.c_int32)]
     lib.dllm_token_stats_noalloc.argtypes = stats_args + [P]
     lib.dllm_token_stats_ex.argtypes = stats_args[:10] + [C.POINTER(StatsEx)] + stats_args[10:] + [P, sz, P]
+    lib.dllm_linear_temperature.argtypes = [i32, i32, f32, f32, C.POINTER(C.c_float)]
+    lib.dllm_uniform_canvas.argtypes = [i64, i64, i64, u64, P, i64, P]
+    lib.dllm_renoise.argtypes = [P, P, P, P, i64, i64, P, P]
+    lib.dllm_stable_confident_stop.argtypes = [P, P, i64, i64, i32, f32, P, P, P, P, P]
     for name in EXPORTS[3:]:
         if name != "dllm_token_stats_workspace_size":
             getattr(lib, name).restype = C.c_int
@@ -414,3 +419,75 @@ def workspace_fault(ws: torch.Tensor, stream=None) -> int:
 
 def lib_handle() -> C.CDLL:
     return _lib
+
+
+# ---------------------------------------------------------------------------
+# uniform-noise decoding helpers
+# ---------------------------------------------------------------------------
+def linear_temperature(remaining: int, num_steps: int, t_min: float = 0.4, t_max: float = 0.8) -> float:
+    """fp32(t_min + (t_max - t_min) * remaining / num_steps) (host)."""
+    T = C.c_float(0.0)
+    _check(_lib.dllm_linear_temperature(int(remaining), int(num_steps), float(t_min), float(t_max), C.byref(T)),
+           "dllm_linear_temperature")
+    return T.value
+
+
+def uniform_canvas(B: int, N: int, V: int, key: int, out: Optional[torch.Tensor] = None, device=None,
+                   stream=None) -> torch.Tensor:
+    """(B, N) int32 uniformly random tokens of [0, V) keyed by ``key``."""
+    if out is None:
+        out = torch.empty((B, N), dtype=torch.int32, device=device or "cuda")
+    _need_cuda(out)
+    if out.shape != (B, N) or out.dtype != torch.int32 or out.stride(1) != 1:
+        raise ValueError("out must be a (B, N) int32 tensor with unit column stride")
+    _check(_lib.dllm_uniform_canvas(B, N, V, int(key) & (2**64 - 1), _ptr(out), out.stride(0), _stream(stream)),
+           "dllm_uniform_canvas")
+    return out
+
+
+def renoise(sample: torch.Tensor, accepted: Optional[torch.Tensor], noise: Optional[torch.Tensor],
+            out: Optional[torch.Tensor] = None, frozen: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out = accepted ? sample : noise over a contiguous (B, N) canvas; rows
+    with frozen[b] != 0 keep ``out``."""
+    _need_cuda(sample, accepted, noise, out, frozen)
+    if sample.dim() != 2 or sample.dtype != torch.int32 or not sample.is_contiguous():
+        raise ValueError("sample must be a contiguous (B, N) int32 tensor")
+    B, N = sample.shape
+    for t, dt in ((accepted, (torch.uint8, torch.bool)), (noise, (torch.int32,))):
+        if t is not None and (t.shape != sample.shape or t.dtype not in dt or not t.is_contiguous()):
+            raise ValueError("accepted / noise must be contiguous and shaped like sample")
+    if out is None:
+        out = torch.empty_like(sample)
+    if out.shape != sample.shape or out.dtype != torch.int32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous (B, N) int32 tensor")
+    _check(_lib.dllm_renoise(_ptr(sample), _ptr(accepted), _ptr(noise), _ptr(frozen), B, N, _ptr(out),
+                             _stream(stream)), "dllm_renoise")
+    return out
+
+
+class StableConfidentStopping:
+    """The stable-and-confident stopping criterion with its device state
+    (the previous argmax canvas and the count of consecutive stable calls)."""
+
+    def __init__(self, B: int, L: int, stability_threshold: int = 1, confidence_threshold: float = 0.005,
+                 device=None):
+        dev = device or "cuda"
+        self.prev = torch.zeros((B, L), dtype=torch.int32, device=dev)
+        self.count = torch.full((B,), -1, dtype=torch.int32, device=dev)
+        self.stability_threshold = int(stability_threshold)
+        self.confidence_threshold = float(confidence_threshold)
+
+    def __call__(self, argmax: torch.Tensor, entropy: torch.Tensor, done: Optional[torch.Tensor] = None,
+                 stop: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        _need_cuda(argmax, entropy, done, stop)
+        B, L = self.prev.shape
+        if argmax.shape != (B, L) or entropy.shape != (B, L) or not argmax.is_contiguous() or \
+                not entropy.is_contiguous() or argmax.dtype != torch.int32 or entropy.dtype != torch.float32:
+            raise ValueError("argmax / entropy must be contiguous (B, L) int32 / float32 tensors")
+        if stop is None:
+            stop = torch.empty((B,), dtype=torch.uint8, device=argmax.device)
+        _check(_lib.dllm_stable_confident_stop(_ptr(argmax), _ptr(entropy), B, L, self.stability_threshold,
+                                               self.confidence_threshold, _ptr(self.prev), _ptr(self.count),
+                                               _ptr(stop), _ptr(done), _stream(stream)),
+               "dllm_stable_confident_stop")
+        return stop

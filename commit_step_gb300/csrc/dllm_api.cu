@@ -18,6 +18,9 @@ const void* stats_cluster_kernel_ptr(bool bf16, int mode);
 const void* rules_kernel_ptr(int nt);
 const void* edit_kernel_ptr();
 const void* schedule_kernel_ptr();
+const void* uniform_canvas_kernel_ptr();
+const void* renoise_kernel_ptr();
+const void* stop_kernel_ptr();
 }  // namespace dllm
 
 namespace {
@@ -206,6 +209,20 @@ dllm_status check_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L,
   return DLLM_OK;
 }
 
+// The round keys of Philox4x32-10 for a 64-bit key: round i uses
+// (lo + i 0x9E3779B9, hi + i 0xBB67AE85) mod 2^32.
+PhiloxSchedule philox_schedule(uint64_t key) {
+  PhiloxSchedule ks;
+  uint32_t k0 = static_cast<uint32_t>(key), k1 = static_cast<uint32_t>(key >> 32);
+  for (int r = 0; r < 10; ++r) {
+    ks.k[r][0] = k0;
+    ks.k[r][1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return ks;
+}
+
 // The extended statistics options, resolved (dllm_stats_ex or the defaults).
 struct StatsOpts {
   float scale = 1.0f;
@@ -257,15 +274,7 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   p.stages = pl.stages;
   p.temperature = temperature;
   p.scale = opt.scale;
-  {
-    uint32_t k0 = static_cast<uint32_t>(key), k1 = static_cast<uint32_t>(key >> 32);
-    for (int r = 0; r < 10; ++r) {
-      p.keys.k[r][0] = k0;
-      p.keys.k[r][1] = k1;
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-  }
+  p.keys = philox_schedule(key);
   p.n_sup = static_cast<int32_t>(sup.size());
   for (size_t i = 0; i < sup.size(); ++i) p.sup[i] = sup[i];
   p.ln_veff = static_cast<float>(std::log(static_cast<double>(V - static_cast<int64_t>(sup.size()))));
@@ -492,6 +501,58 @@ dllm_status dllm_transfer_schedule(const int32_t* counts, int64_t B, int32_t ste
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(d->sms) * 8);
   void* args[] = {const_cast<int32_t**>(&counts), &B, &steps, &quotas};
   return launch(schedule_kernel_ptr(), dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                reinterpret_cast<cudaStream_t>(stream), args);
+}
+
+dllm_status dllm_linear_temperature(int32_t remaining, int32_t num_steps, float t_min, float t_max,
+                                    float* temperature) {
+  if (!temperature || num_steps <= 0 || remaining < 0 || remaining > num_steps) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!(t_min > 0.0f) || !(t_max >= t_min) || std::isinf(t_max)) return DLLM_ERR_INVALID_ARGUMENT;
+  const double frac = static_cast<double>(remaining) / static_cast<double>(num_steps);
+  *temperature = static_cast<float>(static_cast<double>(t_min) + (static_cast<double>(t_max) - t_min) * frac);
+  return DLLM_OK;
+}
+
+dllm_status dllm_uniform_canvas(int64_t B, int64_t N, int64_t V, uint64_t key, int32_t* canvas,
+                                int64_t canvas_stride, dllm_stream_t stream) {
+  if (B < 0 || N < 0 || V <= 0 || V > INT32_MAX || canvas_stride < N) return DLLM_ERR_INVALID_ARGUMENT;
+  if (B * N == 0) return DLLM_OK;
+  if (!canvas) return DLLM_ERR_INVALID_ARGUMENT;
+  const DeviceInfo* d = device_info();
+  if (!d) return DLLM_ERR_CUDA;
+  PhiloxSchedule ks = philox_schedule(key);
+  uint32_t v32 = static_cast<uint32_t>(V);
+  const int64_t work = B * ((N + 3) / 4);
+  const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(d->sms) * 8);
+  void* args[] = {&ks, &B, &N, &v32, &canvas, &canvas_stride};
+  return launch(uniform_canvas_kernel_ptr(), dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                reinterpret_cast<cudaStream_t>(stream), args);
+}
+
+dllm_status dllm_renoise(const int32_t* sample, const uint8_t* accepted, const int32_t* noise, const uint8_t* frozen,
+                         int64_t B, int64_t N, int32_t* out, dllm_stream_t stream) {
+  if (B < 0 || N < 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (B * N == 0) return DLLM_OK;
+  if (!sample || !out || (accepted && !noise)) return DLLM_ERR_INVALID_ARGUMENT;
+  const DeviceInfo* d = device_info();
+  if (!d) return DLLM_ERR_CUDA;
+  const int64_t blocks = std::min<int64_t>((B * N + 255) / 256, static_cast<int64_t>(d->sms) * 8);
+  void* args[] = {const_cast<int32_t**>(&sample), const_cast<uint8_t**>(&accepted), const_cast<int32_t**>(&noise),
+                  const_cast<uint8_t**>(&frozen), &B, &N, &out};
+  return launch(renoise_kernel_ptr(), dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                reinterpret_cast<cudaStream_t>(stream), args);
+}
+
+dllm_status dllm_stable_confident_stop(const int32_t* argmax, const float* entropy, int64_t B, int64_t L,
+                                       int32_t stability_threshold, float confidence_threshold, int32_t* prev,
+                                       int32_t* count, uint8_t* stop, uint8_t* done, dllm_stream_t stream) {
+  if (B < 0 || L <= 0 || stability_threshold < 0 || std::isnan(confidence_threshold))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (B == 0) return DLLM_OK;
+  if (B > INT32_MAX || !argmax || !entropy || !prev || !count) return DLLM_ERR_INVALID_ARGUMENT;
+  void* args[] = {const_cast<int32_t**>(&argmax), const_cast<float**>(&entropy), &L, &stability_threshold,
+                  &confidence_threshold, &prev, &count, &stop, &done};
+  return launch(stop_kernel_ptr(), dim3(static_cast<unsigned>(B)), dim3(256), 0,
                 reinterpret_cast<cudaStream_t>(stream), args);
 }
 

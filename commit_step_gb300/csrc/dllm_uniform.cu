@@ -1,0 +1,104 @@
+// dllm_uniform.cu -- the helpers of uniform-noise decoding on the device.
+//
+// mlx-arsenal "dLLM block decoding", function table (uniform_canvas, renoise,
+// StableConfidentStopping) and "Uniform-noise decoding (DiffusionGemma)": the
+// canvas starts as uniformly random tokens, the positions a step does not
+// accept are re-noised, and a row stops for good once its argmax canvas is
+// stable and confident; stopped rows stay frozen.  All three are element- or
+// row-wise and tiny next to the statistics pass.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dllm_device.cuh"
+#include "dllm_gumbel.cuh"
+
+namespace dllm {
+
+// canvas[b, j] = floor(r V / 2^32), r = Philox4x32-10(counter (j >> 2, b lo,
+// b hi, 1), key) word j & 3: one Philox call per four tokens.
+__global__ void uniform_canvas_kernel(const __grid_constant__ PhiloxSchedule ks, int64_t B, int64_t N, uint32_t V,
+                                      int32_t* __restrict__ canvas, int64_t stride) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t groups = (N + 3) / 4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < B * groups;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t b = i / groups, g = i - b * groups;
+    const uint4 r = philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(b),
+                                  static_cast<uint32_t>(static_cast<uint64_t>(b) >> 32), 1u, ks);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t j = 4 * g + k;
+      if (j < N) canvas[b * stride + j] = static_cast<int32_t>((static_cast<uint64_t>(w[k]) * V) >> 32);
+    }
+  }
+}
+
+// out[b, j] = accepted[b, j] ? sample[b, j] : noise[b, j] (accepted == nullptr:
+// sample everywhere), except in rows with frozen[b] != 0, which keep out.
+__global__ void renoise_kernel(const int32_t* __restrict__ sample, const uint8_t* __restrict__ accepted,
+                               const int32_t* __restrict__ noise, const uint8_t* __restrict__ frozen, int64_t B,
+                               int64_t N, int32_t* out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < B * N;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (frozen && frozen[i / N]) continue;
+    out[i] = (!accepted || accepted[i]) ? sample[i] : noise[i];
+  }
+}
+
+constexpr int kStopThreads = 256;
+constexpr int kStopChunk = 1024;
+
+// One call of the stopping criterion, one CTA per batch row b: the row is
+// stable when its argmax canvas equals prev (count[b] >= 0 says prev holds
+// a canvas); count[b] counts consecutive stable calls; the row is confident
+// when its mean entropy -- summed in double in position order by one thread,
+// then divided by L -- is below the threshold.  prev takes the canvas;
+// stop[b] = count >= stability and confident; done[b] |= stop[b].
+__global__ void __launch_bounds__(kStopThreads) stop_kernel(const int32_t* __restrict__ argmax,
+                                                             const float* __restrict__ entropy, int64_t L,
+                                                             int32_t stability, float threshold, int32_t* prev,
+                                                             int32_t* count, uint8_t* stop, uint8_t* done) {
+  __shared__ float chunk[kStopChunk];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t b = blockIdx.x;
+  const int32_t* a = argmax + b * L;
+  int32_t* pv = prev + b * L;
+  const float* e = entropy + b * L;
+  int diff = 0;
+  for (int64_t l = threadIdx.x; l < L; l += kStopThreads) {
+    const int32_t v = a[l];
+    diff |= v != pv[l] ? 1 : 0;
+    pv[l] = v;
+  }
+  const int any_diff = __syncthreads_or(diff);
+  double sum = 0.0;
+  for (int64_t c0 = 0; c0 < L; c0 += kStopChunk) {
+    const int n = static_cast<int>(L - c0 < kStopChunk ? L - c0 : kStopChunk);
+    for (int k = threadIdx.x; k < n; k += kStopThreads) chunk[k] = e[c0 + k];
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int k = 0; k < n; ++k) sum = __dadd_rn(sum, static_cast<double>(chunk[k]));
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int32_t c = count[b];
+    const int32_t nc = (c >= 0 && !any_diff) ? c + 1 : 0;
+    count[b] = nc;
+    const bool confident = __ddiv_rn(sum, static_cast<double>(L)) < static_cast<double>(threshold);
+    const uint8_t st = (nc >= stability && confident) ? 1 : 0;
+    if (stop) stop[b] = st;
+    if (done && st) done[b] = 1;
+  }
+}
+
+const void* uniform_canvas_kernel_ptr() { return reinterpret_cast<const void*>(&uniform_canvas_kernel); }
+const void* renoise_kernel_ptr() { return reinterpret_cast<const void*>(&renoise_kernel); }
+const void* stop_kernel_ptr() { return reinterpret_cast<const void*>(&stop_kernel); }
+
+}  // namespace dllm

@@ -236,6 +236,51 @@ dllm_status dllm_block_ranges(int64_t P, int64_t gen_len, int64_t block_len, int
                               int64_t* ranges, int64_t cap, int64_t* n_out);
 
 /* ------------------------------------------------------------------------
+ * Uniform-noise decoding helpers ([ARS] function table: linear_temperature,
+ * uniform_canvas, renoise, StableConfidentStopping; "Uniform-noise decoding
+ * (DiffusionGemma)").  The loop: the canvas starts uniformly random; each
+ * step scales the logits by 1 / linear_temperature, takes the argmax,
+ * entropy and a categorical sample of the scaled softmax
+ * (dllm_token_stats_ex or the fused step with temperature 1), accepts the
+ * lowest-entropy positions under the entropy bound over all positions,
+ * re-noises the rest, and freezes the rows that meet the stopping criterion.
+ * ------------------------------------------------------------------------ */
+
+/* Host-only, pure: *temperature = fp32(t_min + (t_max - t_min) * remaining /
+ * num_steps), evaluated in double.  0 <= remaining <= num_steps, num_steps >
+ * 0, 0 < t_min <= t_max finite (else DLLM_ERR_INVALID_ARGUMENT). */
+dllm_status dllm_linear_temperature(int32_t remaining, int32_t num_steps, float t_min, float t_max,
+                                    float* temperature);
+
+/* canvas[b * canvas_stride + j] = floor(r * V / 2^32) for b < B, j < N, with
+ * r the word j & 3 of Philox4x32-10(counter (j >> 2, b lo, b hi, 1), key
+ * (key lo, key hi)): every id of [0, V) has probability within V / 2^32 of
+ * 1/V.  canvas: device int32; canvas_stride >= N; 0 < V <= 2^31 - 1. */
+dllm_status dllm_uniform_canvas(int64_t B, int64_t N, int64_t V, uint64_t key, int32_t* canvas,
+                                int64_t canvas_stride, dllm_stream_t stream);
+
+/* out[b, j] = accepted[b, j] ? sample[b, j] : noise[b, j] over a (B, N)
+ * row-major canvas; accepted == NULL takes sample everywhere (noise may then
+ * be NULL).  frozen (device (B) uint8, nullable): rows with frozen[b] != 0
+ * keep out as it is (rows that already stopped).  out may alias sample or
+ * noise.  All device arrays. */
+dllm_status dllm_renoise(const int32_t* sample, const uint8_t* accepted, const int32_t* noise,
+                         const uint8_t* frozen, int64_t B, int64_t N, int32_t* out, dllm_stream_t stream);
+
+/* One call of the stable-and-confident stopping criterion on the (B, L)
+ * argmax canvas and entropies (device).  State, device, owned by the caller:
+ * prev (B, L) int32, the previous canvas; count (B) int32, consecutive
+ * stable calls, -1 before the first call (then nothing is stable).  Per row:
+ * stable = count >= 0 and argmax == prev everywhere; count = stable ? count
+ * + 1 : 0; prev = argmax; confident = (sum of the L entropies in double in
+ * position order) / L < confidence_threshold; stop[b] = count >=
+ * stability_threshold and confident.  stop (B) uint8 and done (B) uint8 are
+ * nullable outputs; done[b] becomes 1 when stop[b] is (never 0). */
+dllm_status dllm_stable_confident_stop(const int32_t* argmax, const float* entropy, int64_t B, int64_t L,
+                                       int32_t stability_threshold, float confidence_threshold, int32_t* prev,
+                                       int32_t* count, uint8_t* stop, uint8_t* done, dllm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Fused commit step: the statistics pass and one commit rule (plus the
  * optional edit rule and canvas update) in one launch.  The rule of batch
  * row b runs as soon as its L rows' statistics are complete, inside the same

@@ -50,6 +50,7 @@ def lib():
         L.orc_uniform_canvas.argtypes = [i64, i64, i64, u64, P]
         L.orc_renoise.argtypes = [P, P, P, i64, P]
         L.orc_stable_confident_stop.argtypes = [P, P, i64, i64, i32, f32, P, P, P]
+        L.orc_block_causal_mask.argtypes = [i64, i64, i64, i64, i64, P]
         _lib = L
     return _lib
 
@@ -250,3 +251,12 @@ class StableConfidentStopping:
                                                self.confidence_threshold, _p(self.prev), _p(self.count), _p(stop)),
                "stable_confident_stop")
         return stop
+
+
+def block_causal_mask(Lq: int, block_len: int, Lk: int = None, q_offset: int = 0, k_offset: int = 0) -> np.ndarray:
+    """(Lq, Lk) additive mask in float64: 0 where query block >= key block, -inf elsewhere."""
+    Lk = Lq if Lk is None else Lk
+    out = np.zeros((Lq, Lk), dtype=np.float64)
+    _check(lib().orc_block_causal_mask(int(Lq), int(Lk), int(q_offset), int(k_offset), int(block_len), _p(out)),
+           "block_causal_mask")
+    return out

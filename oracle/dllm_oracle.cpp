@@ -554,4 +554,24 @@ int orc_stable_confident_stop(const int32_t* argmax, const float* entropy, int64
   return 0;
 }
 
+// block_causal_mask.  [ARS] "What mlx-arsenal ships" (attention): the mask
+// block-diffusion models are trained with -- bidirectional inside a block,
+// causal across blocks, blocks aligned on absolute positions; "Mask
+// conventions": additive, 0 where attention is allowed and -inf where it is
+// blocked.  Query i sits at absolute position q_offset + i, key j at
+// k_offset + j; attend iff block(query) >= block(key), block(p) =
+// floor(p / block_len).  out: (Lq, Lk) row-major doubles.
+int orc_block_causal_mask(int64_t Lq, int64_t Lk, int64_t q_offset, int64_t k_offset, int64_t block_len,
+                          double* out) {
+  if (Lq < 0 || Lk < 0 || q_offset < 0 || k_offset < 0 || block_len <= 0 || (Lq * Lk > 0 && !out)) return -1;
+  for (int64_t i = 0; i < Lq; ++i) {
+    const int64_t bq = (q_offset + i) / block_len;
+    for (int64_t j = 0; j < Lk; ++j) {
+      const int64_t bk = (k_offset + j) / block_len;
+      out[i * Lk + j] = bq >= bk ? 0.0 : -std::numeric_limits<double>::infinity();
+    }
+  }
+  return 0;
+}
+
 }  // extern "C"

@@ -85,6 +85,12 @@ int orc_stable_confident_stop(const int32_t* argmax, const float* entropy, int64
                               int32_t stability_threshold, float confidence_threshold, int32_t* prev,
                               int32_t* count, uint8_t* stop);
 
+/* block_causal_mask ("dLLM block decoding", attention helper and "Mask
+ * conventions"): out[i, j] = 0 if floor((q_offset + i) / block_len) >=
+ * floor((k_offset + j) / block_len), else -inf.  (Lq, Lk) row-major. */
+int orc_block_causal_mask(int64_t Lq, int64_t Lk, int64_t q_offset, int64_t k_offset, int64_t block_len,
+                          double* out);
+
 /* Threads orc_token_stats uses when asked for 0. */
 int orc_default_threads(void);
 

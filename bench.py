@@ -35,7 +35,8 @@ sys.path.insert(0, ROOT)
 import dllm_workloads as W  # noqa: E402
 
 METRIC = "token_stats+commit logits GB/s (% of GB300 HBM peak); canvas positions/s"
-KERNEL_SOURCES = ("dllm_stats.cu", "dllm_stats.cuh", "dllm_rules.cuh", "dllm_device.cuh", "dllm_gumbel.cuh")
+KERNEL_SOURCES = ("dllm_stats_kernels.cuh", "dllm_stats.cuh", "dllm_rules.cuh", "dllm_device.cuh", "dllm_gumbel.cuh",
+                  "dllm_stats_greedy.cu", "dllm_stats_sample.cu", "dllm_stats_margin.cu", "dllm_stats_dispatch.cu")
 
 
 def parse():
@@ -43,7 +44,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="llada", choices=["llada", "tiny", "dream", "large", "loop"])
+    ap.add_argument("--workload", default="llada", choices=["llada", "tiny", "dream", "large", "loop", "uniform", "mask"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -518,6 +519,114 @@ def run_loop(args, rank, world):
     }
 
 
+def run_uniform(args, rank, world):
+    """The uniform-noise loop workload: B=1, canvas N=256, V=262144 bf16 (a
+    DiffusionGemma-sized vocabulary), 48 steps at most, entropy bound 0.1,
+    temperatures 0.8 -> 0.4, stop when stable once and mean entropy < 0.005;
+    a seeded generator makes each position confident from a random onset
+    step in [0, 24].  Reports the GB/s of the per-step GPU work (the fused
+    statistics + acceptance launch, noise, re-noising, stopping update) and
+    canvas positions per second of that time."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from commit_step_gb300.decode import decode_uniform
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    spec = W.uniform_spec()
+    gen = W.UniformGenerator(spec)
+    buf = torch.empty((spec.B * spec.N, spec.V), dtype=torch.bfloat16, device=dev)
+    model = lambda st, c: gen.device_logits(st, out=buf)
+    kw = dict(batch=spec.B, canvas_len=spec.N, vocab_size=spec.V, key=spec.key, num_steps=spec.num_steps,
+              entropy_bound=spec.entropy_bound, t_min=spec.t_min, t_max=spec.t_max,
+              stability_threshold=spec.stability_threshold, confidence_threshold=spec.confidence_threshold)
+    _, warm_steps = decode_uniform(model, **kw)                 # warm-up: one whole decode
+    times = []
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_query_id(torch.cuda.get_device_properties(dev), dev.index)) as clk:
+        out, steps = decode_uniform(model, step_times=times, **kw)
+    total_ms = float(sum(times))
+    rows = spec.B * spec.N
+    bytes_per_step = rows * (spec.V * 2 + 12 + 1 + 4 * 4)    # logits; stats out; accepted; noise/canvas/argmax traffic
+    peak, _ = measured_peaks()
+    value = bytes_per_step * steps / (total_ms / 1e3) / 1e9 * world
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": warm_steps, "ms_per_step": total_ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator, dllm_workloads.py)",
+        "config": {"workload": f"uniform: B={spec.B}, canvas {spec.N}, V={spec.V} bf16, <= {spec.num_steps} steps, "
+                               f"entropy bound {spec.entropy_bound}, T {spec.t_max} -> {spec.t_min}",
+                   "global_batch": spec.B * world, "seq_len": spec.N, "vocab": spec.V,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "per-step logits (134 MB) are written by the generator just before the step"},
+        "positions_per_s": round(rows * steps * world / (total_ms / 1e3), 1),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 1),
+        "gpu_launches": 5 * steps, "clocks": clk.summary(),
+    }
+
+
+def run_mask(args, rank, world):
+    """block_causal_mask of an 8192-token window in blocks of 32 (a
+    LLaDA2-style window), fp32 additive: 256 MiB of pure writes per call.
+    Reports the write GB/s (graph replay of independent calls, CUDA events)."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import commit_step_gb300 as cs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    L, bl = 8192, 32
+    steps = args.steps if args.steps is not None else 2000
+    warmup = max(3, args.warmup if args.warmup is not None else 10)
+    outs = [torch.empty((L, L), dtype=torch.float32, device=dev) for _ in range(2)]
+    G = 10
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(stream):
+        for i in range(G):
+            cs.block_causal_mask(L, bl, out=outs[i % 2], stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(G):
+            cs.block_causal_mask(L, bl, out=outs[i % 2], stream=stream)
+    reps = max(1, steps // G)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, warmup // G)):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_query_id(torch.cuda.get_device_properties(dev), dev.index)) as clk:
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev, world)
+    n = reps * G
+    nbytes = L * L * 4
+    value = nbytes * n * world / (ms / 1e3) / 1e9
+    peak, kind = measured_peaks()
+    return {
+        "metric": "block_causal_mask write GB/s", "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": n, "warmup": max(1, warmup // G) * G, "ms_per_step": ms / n, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (mask of an 8192-token window)",
+        "config": {"workload": f"block_causal_mask L={L} block_len={bl} fp32 additive", "l2": "two 256 MiB outputs, "
+                   "alternating (each larger than L2)"},
+        "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / world / peak, 4), "traffic": None,
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({kind})"},
+        "gpu_launches": n, "clocks": clk.summary(),
+    }
+
+
 def run_reference(args, rank, world):
     w = W.build(args.workload)
     steps = args.steps if args.steps is not None else 3
@@ -560,8 +669,8 @@ def main():
 
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    if args.workload == "loop":
-        res = run_loop(args, rank, world)
+    if args.workload in ("loop", "uniform", "mask"):
+        res = {"loop": run_loop, "uniform": run_uniform, "mask": run_mask}[args.workload](args, rank, world)
         if rank == 0:
             print(json.dumps(res))
         return 0

@@ -34,7 +34,7 @@ EXPORTS = (
     "dllm_threshold_transfer", "dllm_topk_transfer", "dllm_factor_transfer", "dllm_entropy_bound_transfer",
     "dllm_edit_transfer", "dllm_transfer_schedule", "dllm_block_ranges", "dllm_commit_step",
     "dllm_workspace_fault", "dllm_token_stats_noalloc", "dllm_token_stats_ex", "dllm_linear_temperature",
-    "dllm_uniform_canvas", "dllm_renoise", "dllm_stable_confident_stop",
+    "dllm_uniform_canvas", "dllm_renoise", "dllm_stable_confident_stop", "dllm_block_causal_mask",
 )
 
 
@@ -90,6 +90,7 @@ def _load() -> C.CDLL:
     lib.dllm_uniform_canvas.argtypes = [i64, i64, i64, u64, P, i64, P]
     lib.dllm_renoise.argtypes = [P, P, P, P, i64, i64, P, P]
     lib.dllm_stable_confident_stop.argtypes = [P, P, i64, i64, i32, f32, P, P, P, P, P]
+    lib.dllm_block_causal_mask.argtypes = [i64, i64, i64, i64, i64, C.c_int, P, i64, P]
     for name in EXPORTS[3:]:
         if name != "dllm_token_stats_workspace_size":
             getattr(lib, name).restype = C.c_int
@@ -491,3 +492,24 @@ class StableConfidentStopping:
                                                _ptr(stop), _ptr(done), _stream(stream)),
                "dllm_stable_confident_stop")
         return stop
+
+
+MASK_F32, MASK_BF16, MASK_KEEP_U8 = 0, 1, 2
+
+
+def block_causal_mask(L: int, block_len: int, Lk: Optional[int] = None, q_offset: int = 0, k_offset: int = 0,
+                      dtype=torch.float32, out: Optional[torch.Tensor] = None, device=None,
+                      stream=None) -> torch.Tensor:
+    """(L, Lk) block-causal attention mask: additive (float32 / bfloat16: 0
+    attend, -inf blocked) or, with dtype=torch.bool / torch.uint8, the keep
+    mask (True / 1 attend)."""
+    Lk = L if Lk is None else Lk
+    kinds = {torch.float32: MASK_F32, torch.bfloat16: MASK_BF16, torch.uint8: MASK_KEEP_U8, torch.bool: MASK_KEEP_U8}
+    if out is None:
+        out = torch.empty((L, Lk), dtype=dtype, device=device or "cuda")
+    _need_cuda(out)
+    if out.dim() != 2 or out.shape != (L, Lk) or out.stride(1) != 1 or out.dtype not in kinds:
+        raise ValueError("out must be an (L, Lk) float32 / bfloat16 / uint8 / bool tensor with unit column stride")
+    _check(_lib.dllm_block_causal_mask(L, Lk, q_offset, k_offset, block_len, kinds[out.dtype], _ptr(out),
+                                       out.stride(0), _stream(stream)), "dllm_block_causal_mask")
+    return out

@@ -13,14 +13,13 @@
 #include "dllm_stats.cuh"
 
 namespace dllm {
-const void* stats_kernel_ptr(bool bf16, int mode);
-const void* stats_cluster_kernel_ptr(bool bf16, int mode);
 const void* rules_kernel_ptr(int nt);
 const void* edit_kernel_ptr();
 const void* schedule_kernel_ptr();
 const void* uniform_canvas_kernel_ptr();
 const void* renoise_kernel_ptr();
 const void* stop_kernel_ptr();
+const void* mask_kernel_ptr(int es);
 }  // namespace dllm
 
 namespace {
@@ -32,11 +31,11 @@ constexpr size_t kStatsSmemMax = static_cast<size_t>(kRingBytes) + kFusedSortCap
 
 struct DeviceInfo {
   int sms = 0;
-  // Per kernel variant, index bf16 * kModes + mode: CTAs per SM of
+  // Per kernel variant, index bf16 * kModeSlots + mode: CTAs per SM of
   // stats_kernel, and co-resident clusters of stats_cluster_kernel per
   // cluster size 1, 2, 4, 8, 16.
-  int occ[2 * kModes] = {};
-  int clusters[2 * kModes][5] = {};
+  int occ[2 * kModeSlots] = {};
+  int clusters[2 * kModeSlots][5] = {};
   cudaError_t err = cudaSuccess;
 };
 
@@ -49,16 +48,18 @@ const DeviceInfo* device_info() {
   std::call_once(g_once[dev], [dev]() {
     DeviceInfo& d = g_dev[dev];
     d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    for (int v = 0; v < 2 * kModes && d.err == cudaSuccess; ++v) {
-      const void* k = stats_kernel_ptr(v >= kModes, v % kModes);
+    for (int v = 0; v < 2 * kModeSlots && d.err == cudaSuccess; ++v) {
+      if (!mode_built(v % kModeSlots)) continue;
+      const void* k = stats_kernel_ptr(v >= kModeSlots, v % kModeSlots, false);
       d.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmemMax));
       if (d.err != cudaSuccess) break;
       int n = 0;
       d.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kThreads, kStatsSmemMax);
       d.occ[v] = std::max(1, std::min(n, kMaxCtasPerSm));
     }
-    for (int v = 0; v < 2 * kModes && d.err == cudaSuccess; ++v) {
-      const void* k = stats_cluster_kernel_ptr(v >= kModes, v % kModes);
+    for (int v = 0; v < 2 * kModeSlots && d.err == cudaSuccess; ++v) {
+      if (!mode_built(v % kModeSlots)) continue;
+      const void* k = stats_kernel_ptr(v >= kModeSlots, v % kModeSlots, true);
       d.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmemMax));
       if (d.err == cudaSuccess) d.err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       for (int e = 0; e < 5 && d.err == cudaSuccess; ++e) {
@@ -247,14 +248,18 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   const DeviceInfo* d = device_info();
   if (!d) return DLLM_ERR_CUDA;
   const bool bf16 = dt == DLLM_BF16, gumbel = temperature > 0.0f;
-  // A sample that must also report its row's argmax or margin tracks both.
-  const int mode = !gumbel ? kModeGreedy : ((opt.margin || opt.argmax) ? kModeDual : kModeGumbel);
+  // Track only what the outputs need: the argmax beside a sample when the
+  // argmax or the margin is asked for, the runner-up only for the margin.
+  int mode = gumbel ? kModeSample : 0;
+  if (gumbel && (opt.margin || opt.argmax)) mode |= kModeArgmax;
+  if (opt.margin) mode |= kModeRunner;
+  if (opt.scale != 1.0f) mode |= kModeScaled;
   const int es = esize_of(dt);
   const int64_t T = B * L;
   const WsLayout lay = ws_layout(B, L, d->sms);
   if (!ws || ws_bytes < lay.total) return DLLM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0) return DLLM_ERR_INVALID_ARGUMENT;
-  const int variant = (bf16 ? kModes : 0) + mode;
+  const int variant = (bf16 ? kModeSlots : 0) + mode;
   const StatsPlan pl = plan_stats(*d, variant, T, V, es, early);
 
   StatsParams p{};
@@ -274,6 +279,7 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   p.stages = pl.stages;
   p.temperature = temperature;
   p.scale = opt.scale;
+  p.cs = opt.scale * kLog2e;
   p.keys = philox_schedule(key);
   p.n_sup = static_cast<int32_t>(sup.size());
   for (size_t i = 0; i < sup.size(); ++i) p.sup[i] = sup[i];
@@ -294,8 +300,8 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   const size_t smem = static_cast<size_t>(pl.stages) * pl.chunk_vec * 16 + (rule ? kFusedSortCap * 9 : 0);
   void* args[] = {&p};
   if (pl.cluster > 0)
-    return launch(stats_cluster_kernel_ptr(bf16, mode), dim3(pl.P), dim3(kThreads), smem, s, args, pl.cluster);
-  return launch(stats_kernel_ptr(bf16, mode), dim3(pl.P), dim3(kThreads), smem, s, args);
+    return launch(stats_kernel_ptr(bf16, mode, true), dim3(pl.P), dim3(kThreads), smem, s, args, pl.cluster);
+  return launch(stats_kernel_ptr(bf16, mode, false), dim3(pl.P), dim3(kThreads), smem, s, args);
 }
 
 int next_pow2(int64_t x) {
@@ -553,6 +559,30 @@ dllm_status dllm_stable_confident_stop(const int32_t* argmax, const float* entro
   void* args[] = {const_cast<int32_t**>(&argmax), const_cast<float**>(&entropy), &L, &stability_threshold,
                   &confidence_threshold, &prev, &count, &stop, &done};
   return launch(stop_kernel_ptr(), dim3(static_cast<unsigned>(B)), dim3(256), 0,
+                reinterpret_cast<cudaStream_t>(stream), args);
+}
+
+dllm_status dllm_block_causal_mask(int64_t Lq, int64_t Lk, int64_t q_offset, int64_t k_offset, int64_t block_len,
+                                   dllm_mask_kind kind, void* out, int64_t row_stride, dllm_stream_t stream) {
+  if (Lq < 0 || Lk < 0 || q_offset < 0 || k_offset < 0 || block_len <= 0 || row_stride < Lk)
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (kind != DLLM_MASK_F32 && kind != DLLM_MASK_BF16 && kind != DLLM_MASK_KEEP_U8) return DLLM_ERR_INVALID_ARGUMENT;
+  if (q_offset > INT64_MAX / 2 - Lq || k_offset > INT64_MAX / 2 - Lk || block_len > INT64_MAX / 4)
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (Lq * Lk == 0) return DLLM_OK;
+  if (!out) return DLLM_ERR_INVALID_ARGUMENT;
+  const DeviceInfo* d = device_info();
+  if (!d) return DLLM_ERR_CUDA;
+  const int es = kind == DLLM_MASK_F32 ? 4 : (kind == DLLM_MASK_BF16 ? 2 : 1);
+  uint32_t attend = kind == DLLM_MASK_KEEP_U8 ? 1u : 0u;
+  uint32_t blocked = kind == DLLM_MASK_F32 ? 0xFF800000u : (kind == DLLM_MASK_BF16 ? 0xFF80u : 0u);
+  int64_t row_bytes = row_stride * es;
+  int vec = ((reinterpret_cast<uintptr_t>(out) & 15u) == 0 && row_bytes % 16 == 0) ? 1 : 0;
+  const int64_t warps = 8;
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((Lq + warps - 1) / warps, static_cast<int64_t>(d->sms) * 8));
+  uint8_t* o = static_cast<uint8_t*>(out);
+  void* args[] = {&Lq, &Lk, &q_offset, &k_offset, &block_len, &o, &row_bytes, &attend, &blocked, &vec};
+  return launch(mask_kernel_ptr(es), dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
                 reinterpret_cast<cudaStream_t>(stream), args);
 }
 

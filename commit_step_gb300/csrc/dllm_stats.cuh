@@ -18,10 +18,26 @@ constexpr int kRingBytes = 64 * 1024;
 constexpr int kFusedSortCap = 1024;              // largest L the fused sorting rules take
 constexpr int kMaxCtasPerSm = 4;
 
-// What a row's pass tracks: the greedy argmax (with the runner-up), the
-// Gumbel-max sample, or both (a sample plus its row's argmax and runner-up,
-// for the margin and argmax outputs).
-enum : int { kModeGreedy = 0, kModeGumbel = 1, kModeDual = 2, kModes = 3 };
+// What a row's pass tracks, as bits: kModeSample, a Gumbel-max sample
+// (else the greedy argmax); kModeArgmax, the first argmax beside a sample;
+// kModeRunner, the runner-up of the argmax (the margin output); kModeScaled,
+// a logit scale other than 1 (the unscaled kernels carry no scaling
+// arithmetic at all).  The tracking modes built: greedy (0), greedy +
+// runner-up (4), sample (1), sample + argmax (3), sample + argmax + runner-up
+// (7), each with and without kModeScaled.
+enum : int { kModeSample = 1, kModeArgmax = 2, kModeRunner = 4, kModeScaled = 8, kModeSlots = 16 };
+
+__host__ __device__ constexpr bool mode_sample(int m) { return (m & kModeSample) != 0; }
+__host__ __device__ constexpr bool mode_argmax(int m) { return !mode_sample(m) || (m & kModeArgmax) != 0; }
+__host__ __device__ constexpr bool mode_runner(int m) { return (m & kModeRunner) != 0; }
+__host__ __device__ constexpr bool mode_scaled(int m) { return (m & kModeScaled) != 0; }
+__host__ __device__ constexpr bool mode_built(int m) {
+  return (m & 7) == 0 || (m & 7) == 4 || (m & 7) == 1 || (m & 7) == 3 || (m & 7) == 7;
+}
+
+// Launchable statistics kernels, one per (dtype, mode, grid kind); defined
+// in dllm_stats_{greedy,sample,margin}{,_scaled}.cu.
+const void* stats_kernel_ptr(bool bf16, int mode, bool cluster);
 
 // Partial reduction of one row segment, in scaled logits z' = z s: max m,
 // Z = sum 2^y and S2 = sum 2^y y with y = (z' - m) log2(e), the first index
@@ -49,6 +65,7 @@ struct StatsParams {
   int32_t stages;           // ring stages
   float temperature;
   float scale;              // logit scale s: every statistic is of z' = fp32(z s)
+  float cs;                 // fp32(s log2 e): the exponent scale of the sums (log2 e when s = 1)
   PhiloxSchedule keys;      // Philox round keys of the caller's key
   int32_t n_sup;
   int32_t sup[DLLM_MAX_SUPPRESS];  // sorted, distinct

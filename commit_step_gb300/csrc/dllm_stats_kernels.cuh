@@ -1,4 +1,6 @@
-// dllm_stats.cu -- the statistics pass (and the fused commit step) on sm_103a.
+// dllm_stats_kernels.cuh -- the statistics pass (and the fused commit step) on
+// sm_103a: the kernel templates.  dllm_stats_{greedy,sample,margin}.cu
+// instantiate them per mode, in parallel translation units.
 //
 // What it computes (mlx-arsenal "dLLM block decoding", "What mlx-arsenal
 // ships": token_stats; mojo-dllm manual, "Row statistics on the device"): for
@@ -11,9 +13,11 @@
 //     cp.async.bulk (TMA bulk copies), one mbarrier per stage; eight consumer
 //     warps read each unit from shared memory.
 //   * Each consumer thread keeps an online softmax state of the scaled logits
-//     z' = z s (s = 1 unless the caller scales them): running max m,
-//     Z = sum 2^y and S2 = sum 2^y y with y = (z s - m) log2 e (packed fp32x2
-//     accumulators), rescaled when the max grows; entropy = ln Z - S2 ln 2 / Z.
+//     z' = z s (s = 1 unless the caller scales them): running max m of the
+//     raw logits, Z = sum 2^y and S2 = sum 2^y y with y = (z - m) c,
+//     c = s log2 e (packed fp32x2 accumulators), rescaled when the max grows;
+//     entropy = ln Z - S2 ln 2 / Z.  Decisions (argmax, ties, Gumbel scores)
+//     compare the scaled values fp32(z s) themselves.
 //     The first index of the max is located once per row, from the first
 //     vector that holds the thread's max; the largest value outside that
 //     element (the runner-up of the margin confidence) comes with it.
@@ -31,6 +35,8 @@
 //     threshold / edit decision and canvas update; the last row of a batch row
 //     applies the forced commit when nothing passed (or, for the sorting rules,
 //     its CTA runs the whole rule).
+#pragma once
+
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -40,7 +46,7 @@
 namespace dllm {
 
 struct Acc {
-  float m;
+  float m;          // running max of the raw logits
   uint64_t Z2;      // two partial sums of 2^y
   uint64_t S2;      // two partial sums of 2^y y
   float negm;
@@ -76,17 +82,16 @@ __device__ __forceinline__ void acc_init(Acc& a) {
   a.vm = kMInit;
   a.vv = -1;
   a.bw[0] = a.bw[1] = a.bw[2] = a.bw[3] = 0u;
-  a.m2o = kMInit;
   a.vm_tail = kMInit;
   a.best_s = kNegInf;
   a.best_v = 0x7FFFFFFF;
   a.best_z = 0.0f;
 }
 
-// Raise the running max to mnew (> a.m): Z' = c Z, S2' = c (S2 + d Z),
-// c = 2^d, d = (m - mnew) log2 e.
-__device__ __forceinline__ void acc_rescale(Acc& a, float mnew) {
-  const float d = (a.m - mnew) * kLog2e;
+// Raise the running max to mnew (> a.m): Z' = f Z, S2' = f (S2 + d Z),
+// f = 2^d, d = (m - mnew) cs, cs = s log2 e.
+__device__ __forceinline__ void acc_rescale(Acc& a, float mnew, float cs) {
+  const float d = (a.m - mnew) * cs;
   const float c = ex2_approx(d);
   const uint64_t d2 = pack2(d, d), c2 = pack2(c, c);
   a.S2 = mul2(c2, fma2(d2, a.Z2, a.S2));
@@ -113,12 +118,11 @@ __device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
 }
 
 // Adds two sanitized logits (<= the running max) to the sums (Z2, S2).
-// Adds two sanitized logits (z s <= m) to the sums: y = (z s - m) log2 e, the
-// product z s taken inside the fused multiply-add (exact when s = 1).
+// Adds two sanitized logits (<= m) to the sums: y = (z - m) cs, cs = s log2 e.
 __device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, float z1, uint64_t negm2,
-                                          uint64_t s2) {
-  const uint64_t d2 = fma2(pack2(z0, z1), s2, negm2);
-  const uint64_t y2 = mul2(d2, pack2(kLog2e, kLog2e));
+                                          uint64_t cs2) {
+  const uint64_t d2 = add2(pack2(z0, z1), negm2);
+  const uint64_t y2 = mul2(d2, cs2);
   float y0, y1;
   unpack2(y2, y0, y1);
   const uint64_t e2 = pack2(ex2_approx(y0), ex2_approx(y1));
@@ -126,18 +130,22 @@ __device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, 
   S2 = fma2(e2, y2, S2);
 }
 
-// Combines b into a (a and b may cover any id sets).  The runner-up of the
-// union is the larger of the winner's runner-up and the loser's max.
+// Combines b into a (a and b may cover any id sets; m is the raw max, the
+// argmax is decided on the scaled maxima fp32(m s), ties to the lower id).
+// The runner-up of the union is the larger of the winner's runner-up and the
+// loser's (scaled) max.
 template <int MODE>
-__device__ __forceinline__ void part_combine(Partial& a, const Partial& b) {
-  constexpr bool GUMBEL = MODE != kModeGreedy, GREEDY = MODE != kModeGumbel;
+__device__ __forceinline__ void part_combine(Partial& a, const Partial& b, float s, float cs) {
+  constexpr bool GUMBEL = mode_sample(MODE), RUNNER = mode_runner(MODE), SCALED = mode_scaled(MODE);
+  if (!SCALED) cs = kLog2e;
   const float m = fmaxf(a.m, b.m);
-  const float da = (a.m - m) * kLog2e, db = (b.m - m) * kLog2e;
+  const float da = (a.m - m) * cs, db = (b.m - m) * cs;
   const float ca = ex2_approx(da), cb = ex2_approx(db);
   const float Z = ca * a.Z + cb * b.Z;
   const float S2 = ca * fmaf(da, a.Z, a.S2) + cb * fmaf(db, b.Z, b.S2);
-  const bool b_wins = b.m > a.m || (b.m == a.m && b.idx < a.idx);
-  if (GREEDY) a.m2 = b_wins ? fmaxf(b.m2, a.m) : fmaxf(a.m2, b.m);
+  const float sa = SCALED ? __fmul_rn(a.m, s) : a.m, sb = SCALED ? __fmul_rn(b.m, s) : b.m;
+  const bool b_wins = sb > sa || (sb == sa && b.idx < a.idx);
+  if (RUNNER) a.m2 = b_wins ? fmaxf(b.m2, sa) : fmaxf(a.m2, sb);
   a.m = m;
   a.Z = Z;
   a.S2 = S2;
@@ -164,6 +172,9 @@ __device__ __forceinline__ Partial empty_partial() {
   return p;
 }
 
+// RUNNER: the thread tracked a runner-up (else m2 is not carried, so the
+// field holds no register through the streaming loop).
+template <bool RUNNER>
 __device__ __forceinline__ Partial acc_to_partial(const Acc& a) {
   Partial p;
   float z0, z1, s0, s1;
@@ -176,13 +187,13 @@ __device__ __forceinline__ Partial acc_to_partial(const Acc& a) {
   p.best_s = a.best_s;
   p.best_z = a.best_z;
   p.best_v = a.best_v;
-  p.m2 = a.m2o;
+  p.m2 = RUNNER ? a.m2o : kMInit;
   return p;
 }
 
 template <int MODE>
 __device__ __forceinline__ Partial shfl_partial(const Partial& p, int o) {
-  constexpr bool GUMBEL = MODE != kModeGreedy, GREEDY = MODE != kModeGumbel;
+  constexpr bool GUMBEL = mode_sample(MODE), RUNNER = mode_runner(MODE);
   Partial q;
   q.m = __shfl_xor_sync(0xFFFFFFFFu, p.m, o);
   q.Z = __shfl_xor_sync(0xFFFFFFFFu, p.Z, o);
@@ -197,16 +208,16 @@ __device__ __forceinline__ Partial shfl_partial(const Partial& p, int o) {
     q.best_z = p.best_z;
     q.best_v = p.best_v;
   }
-  q.m2 = GREEDY ? __shfl_xor_sync(0xFFFFFFFFu, p.m2, o) : p.m2;
+  q.m2 = RUNNER ? __shfl_xor_sync(0xFFFFFFFFu, p.m2, o) : p.m2;
   return q;
 }
 
 template <int MODE>
-__device__ __forceinline__ Partial warp_combine(Partial part) {
+__device__ __forceinline__ Partial warp_combine(Partial part, float s, float cs) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const Partial q = shfl_partial<MODE>(part, o);
-    part_combine<MODE>(part, q);
+    part_combine<MODE>(part, q, s, cs);
   }
   return part;
 }
@@ -290,23 +301,27 @@ struct RowOut {
 // when x0 is the argmax, else the max itself.
 template <int MODE>
 __device__ __forceinline__ RowOut row_out(const StatsParams& p, const Partial& r) {
-  constexpr bool GUMBEL = MODE != kModeGreedy;
+  constexpr bool GUMBEL = mode_sample(MODE), RUNNER = mode_runner(MODE), SCALED = mode_scaled(MODE);
   RowOut o;
   o.x0 = GUMBEL ? r.best_v : r.idx;
   o.argmax = r.idx;
-  const float zx = GUMBEL ? r.best_z : r.m;
-  o.prob = ex2_approx((zx - r.m) * kLog2e) / r.Z;
+  const float ms = SCALED ? __fmul_rn(r.m, p.scale) : r.m;   // the scaled max
+  const float zx = GUMBEL ? r.best_z : ms;
+  o.prob = ex2_approx((zx - ms) * kLog2e) / r.Z;
   const float H = logf(r.Z) - r.S2 * kLn2 / r.Z;
   o.H = fminf(fmaxf(H, 0.0f), p.ln_veff);
-  const float r2 = (!GUMBEL || r.best_v == r.idx) ? r.m2 : r.m;
-  o.margin = o.prob - ex2_approx((r2 - r.m) * kLog2e) / r.Z;
+  o.margin = 0.0f;
+  if (RUNNER) {
+    const float r2 = (!GUMBEL || r.best_v == r.idx) ? r.m2 : ms;
+    o.margin = o.prob - ex2_approx((r2 - ms) * kLog2e) / r.Z;
+  }
   return o;
 }
 
 // Writes x0, prob and entropy of one row and, in the fused step, makes the
 // row's own commit / edit decisions.  Run by one thread.  Returns the batch
 // row whose sorting rule this CTA must now run, or -1.
-__device__ int32_t finish_row(const StatsParams& p, int64_t row, const RowOut& o, RowPre pre) {
+inline __device__ int32_t finish_row(const StatsParams& p, int64_t row, const RowOut& o, RowPre pre) {
   const int32_t x0 = o.x0;
   const float prob = o.prob, H = o.H;
   p.x0[row] = x0;
@@ -433,8 +448,10 @@ __device__ __noinline__ GumbelBest gumbel_exact(GumbelBest best, VecWords vw, Gu
 // Consumer-side state of one CTA.
 template <bool BF16, int MODE>
 struct Consumer {
-  static constexpr bool GUMBEL = MODE != kModeGreedy;  // a Gumbel-max sample
-  static constexpr bool GREEDY = MODE != kModeGumbel;  // the argmax and its runner-up
+  static constexpr bool GUMBEL = mode_sample(MODE);    // a Gumbel-max sample
+  static constexpr bool GREEDY = mode_argmax(MODE);    // the first argmax
+  static constexpr bool RUNNER = mode_runner(MODE);    // and its runner-up
+  static constexpr bool SCALED = mode_scaled(MODE);    // logit scale s != 1
   static constexpr int EPV = BF16 ? 8 : 4;  // elements per 16-byte vector
   const StatsParams& p;
   SharedCtl& ctl;
@@ -442,7 +459,8 @@ struct Consumer {
   int tid, warp, lane;
   float t, t_ln2;
   float s;          // logit scale
-  uint64_t s2;      // (s, s)
+  float cs;         // s log2 e
+  uint64_t cs2;     // (cs, cs)
   Acc acc;
   float warp_best;
 
@@ -453,8 +471,9 @@ struct Consumer {
     lane = tid & 31;
     t = p.temperature;
     t_ln2 = t * kLn2;
-    s = p.scale;
-    s2 = pack2(s, s);
+    s = SCALED ? p.scale : 1.0f;
+    cs = p.cs;   // log2 e when unscaled; read from the parameters in every mode (it schedules better)
+    cs2 = pack2(cs, cs);
     reset();
   }
 
@@ -462,6 +481,7 @@ struct Consumer {
   // start of the kernel and at the end of every flush, before a barrier).
   __device__ void reset() {
     acc_init(acc);
+    if (RUNNER) acc.m2o = kMInit;
     warp_best = kNegInf;
   }
 
@@ -545,10 +565,7 @@ struct Consumer {
     // max of the scaled elements is the scaled max, bit for bit).
     float vms[NPT];
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) vms[j] = (FULL || valid[j]) ? __fmul_rn(vmax[j], s) : kMInit;
-    float umaxs = vms[0];
-#pragma unroll
-    for (int j = 1; j < NPT; ++j) umaxs = fmaxf(umaxs, vms[j]);
+    for (int j = 0; j < NPT; ++j) vms[j] = !SCALED ? vmax[j] : ((FULL || valid[j]) ? __fmul_rn(vmax[j], s) : kMInit);
     if (GREEDY) {
       // The first vector holding this thread's max (ids increase with j and
       // from unit to unit, so a strict > keeps the earliest), kept with its
@@ -557,7 +574,7 @@ struct Consumer {
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const bool better = vms[j] > acc.vm;
-        acc.m2o = fmaxf(acc.m2o, better ? acc.vm : vms[j]);
+        if (RUNNER) acc.m2o = fmaxf(acc.m2o, better ? acc.vm : vms[j]);
         acc.vm = better ? vms[j] : acc.vm;
         acc.vv = better ? id0 + j * kConsumers * EPV : acc.vv;
 #pragma unroll
@@ -566,8 +583,8 @@ struct Consumer {
     }
     // Branch-free rescale to the new running max (factor 1 when it did not grow).
     {
-      const float mnew = fmaxf(acc.m, umaxs);
-      const float d = (acc.m - mnew) * kLog2e;
+      const float mnew = fmaxf(acc.m, umax);
+      const float d = (acc.m - mnew) * cs;
       const float c = ex2_approx(d);
       const uint64_t d2 = pack2(d, d), c2 = pack2(c, c);
       acc.S2 = mul2(c2, fma2(d2, acc.Z2, acc.S2));
@@ -582,8 +599,8 @@ struct Consumer {
       if (!FULL && !valid[j]) continue;
 #pragma unroll
       for (int e = 0; e < EPV; e += 4) {
-        acc_pair2(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), negm2, s2);
-        acc_pair2(Zb, Sb, elem(w[j], e + 2), elem(w[j], e + 3), negm2, s2);
+        acc_pair2(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), negm2, cs2);
+        acc_pair2(Zb, Sb, elem(w[j], e + 2), elem(w[j], e + 3), negm2, cs2);
       }
     }
     acc.Z2 = add2(acc.Z2, Zb);
@@ -692,11 +709,11 @@ struct Consumer {
     z = sanitize(z);
     for (int i = 0; i < p.n_sup; ++i)
       if (p.sup[i] == v) z = kAbsent;
-    const float zs = __fmul_rn(z, s);
-    if (zs > acc.m) acc_rescale(acc, zs);
+    const float zs = SCALED ? __fmul_rn(z, s) : z;
+    if (z > acc.m) acc_rescale(acc, z, cs);
     acc.idx = static_cast<int32_t>(v);  // one tail element per thread
     acc.vm_tail = zs;
-    const float y = fmaf(z, s, acc.negm) * kLog2e;
+    const float y = (z - acc.m) * cs;
     const float e = ex2_approx(y);
     acc.Z2 = add2(acc.Z2, pack2(e, 0.0f));
     acc.S2 = fma2(pack2(e, 0.0f), pack2(y, 0.0f), acc.S2);
@@ -722,23 +739,24 @@ struct Consumer {
   __device__ void resolve_index() {
     if (!GREEDY) return;
     int32_t idx = 0x7FFFFFFF;
-    float r2 = acc.m2o;
-    if (acc.vv >= 0 && acc.vm == acc.m) {
+    float r2 = RUNNER ? acc.m2o : kMInit;
+    const float ms = SCALED ? __fmul_rn(acc.m, s) : acc.m;   // the thread's scaled max
+    if (acc.vv >= 0 && acc.vm == ms) {
       bool found = false;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        const float ze = __fmul_rn(elem(acc.bw, e), s);
+        const float ze = SCALED ? __fmul_rn(elem(acc.bw, e), s) : elem(acc.bw, e);
         if (!found && ze == acc.vm) {
           idx = acc.vv + e;
           found = true;
-        } else {
+        } else if (RUNNER) {
           r2 = fmaxf(r2, ze);
         }
       }
-      r2 = fmaxf(r2, acc.vm_tail);
-    } else if (acc.vm_tail == acc.m && acc.m > kMInit) {
+      if (RUNNER) r2 = fmaxf(r2, acc.vm_tail);
+    } else if (acc.vm_tail == ms && acc.m > kMInit) {
       idx = acc.idx;
-      r2 = fmaxf(r2, acc.vm);
+      if (RUNNER) r2 = fmaxf(r2, acc.vm);
     }
     acc.idx = idx;
     acc.m2o = r2;
@@ -753,7 +771,7 @@ struct Consumer {
 
   // The CTA's reduction of all consumer states; valid in thread 0.
   __device__ Partial cta_reduce() {
-    Partial part = warp_combine<MODE>(acc_to_partial(acc));
+    Partial part = warp_combine<MODE>(acc_to_partial<RUNNER>(acc), s, cs);
     if (lane == 0) ctl.warp_part[warp] = part;
     named_sync(1, kConsumers);
     Partial r = empty_partial();
@@ -762,7 +780,7 @@ struct Consumer {
 #pragma unroll
       for (int o = kConsumerWarps / 2; o > 0; o >>= 1) {
         const Partial q = shfl_partial<MODE>(r, o);
-        part_combine<MODE>(r, q);
+        part_combine<MODE>(r, q, s, cs);
       }
     }
     return r;
@@ -955,9 +973,9 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
         const int64_t cc = cb + lane;
         Partial q = empty_partial();
         if (cc <= c1) q = load_partial(p.partials + 2 * cc + ((cc == c0 && c0_tail) ? 1 : 0));
-        part_combine<MODE>(tot, q);
+        part_combine<MODE>(tot, q, p.scale, p.cs);
       }
-      tot = warp_combine<MODE>(tot);
+      tot = warp_combine<MODE>(tot, p.scale, p.cs);
       if (lane == 0) {
         p.row_count[row] = 0;
         ctl.result = tot;
@@ -1077,11 +1095,11 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
     // exit and free their SM slots while rank 0 finishes the row).
     Partial tot = empty_partial();
     if (warp == 0)
-      for (int k = lane; k < S; k += 32) part_combine<MODE>(tot, load_partial_dsmem(&ctl.result, k));
+      for (int k = lane; k < S; k += 32) part_combine<MODE>(tot, load_partial_dsmem(&ctl.result, k), p.scale, p.cs);
     __syncwarp();
     cluster_arrive();
     RowOut o{};
-    if (warp == 0) o = row_out<MODE>(p, warp_combine<MODE>(tot));
+    if (warp == 0) o = row_out<MODE>(p, warp_combine<MODE>(tot, p.scale, p.cs));
     // Everything above touched only this cluster's own memory.  In early mode
     // the wait for the previous kernel comes here, so that only the row's
     // writes (outputs, canvas, batch-row counters) follow that kernel's end.
@@ -1102,37 +1120,11 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
   }
 }
 
-// Explicit instantiations used by the launcher.
-#define DLLM_STATS_INSTANTIATE(BF, MODE)                                                   \
-  template __global__ void stats_kernel<BF, MODE>(const __grid_constant__ StatsParams);   \
-  template __global__ void stats_cluster_kernel<BF, MODE>(const __grid_constant__ StatsParams);
-DLLM_STATS_INSTANTIATE(false, kModeGreedy)
-DLLM_STATS_INSTANTIATE(true, kModeGreedy)
-DLLM_STATS_INSTANTIATE(false, kModeGumbel)
-DLLM_STATS_INSTANTIATE(true, kModeGumbel)
-DLLM_STATS_INSTANTIATE(false, kModeDual)
-DLLM_STATS_INSTANTIATE(true, kModeDual)
-#undef DLLM_STATS_INSTANTIATE
-
-template <bool BF16>
-const void* pick(int mode, bool cluster) {
-  switch (mode) {
-    case kModeGumbel:
-      return cluster ? reinterpret_cast<const void*>(&stats_cluster_kernel<BF16, kModeGumbel>)
-                     : reinterpret_cast<const void*>(&stats_kernel<BF16, kModeGumbel>);
-    case kModeDual:
-      return cluster ? reinterpret_cast<const void*>(&stats_cluster_kernel<BF16, kModeDual>)
-                     : reinterpret_cast<const void*>(&stats_kernel<BF16, kModeDual>);
-    default:
-      return cluster ? reinterpret_cast<const void*>(&stats_cluster_kernel<BF16, kModeGreedy>)
-                     : reinterpret_cast<const void*>(&stats_kernel<BF16, kModeGreedy>);
-  }
-}
-
-const void* stats_kernel_ptr(bool bf16, int mode) { return bf16 ? pick<true>(mode, false) : pick<false>(mode, false); }
-
-const void* stats_cluster_kernel_ptr(bool bf16, int mode) {
-  return bf16 ? pick<true>(mode, true) : pick<false>(mode, true);
+// Kernel entry of (dtype, mode, grid kind) as a launchable pointer.
+template <bool BF16, int MODE>
+const void* stats_entry(bool cluster) {
+  return cluster ? reinterpret_cast<const void*>(&stats_cluster_kernel<BF16, MODE>)
+                 : reinterpret_cast<const void*>(&stats_kernel<BF16, MODE>);
 }
 
 }  // namespace dllm

@@ -1,0 +1,19 @@
+// dllm_stats_margin.cu -- the statistics kernels of Gumbel-max rows with their
+// argmax and its runner-up (mode 7).
+#include "dllm_stats_kernels.cuh"
+
+namespace dllm {
+
+template __global__ void stats_kernel<false, 7>(const __grid_constant__ StatsParams);
+template __global__ void stats_cluster_kernel<false, 7>(const __grid_constant__ StatsParams);
+template __global__ void stats_kernel<true, 7>(const __grid_constant__ StatsParams);
+template __global__ void stats_cluster_kernel<true, 7>(const __grid_constant__ StatsParams);
+
+const void* stats_kernel_ptr_margin(bool bf16, int mode, bool cluster) {
+  switch (mode) {
+    case 7: return bf16 ? stats_entry<true, 7>(cluster) : stats_entry<false, 7>(cluster);
+    default: return nullptr;
+  }
+}
+
+}  // namespace dllm

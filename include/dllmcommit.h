@@ -281,6 +281,26 @@ dllm_status dllm_stable_confident_stop(const int32_t* argmax, const float* entro
                                        int32_t* count, uint8_t* stop, uint8_t* done, dllm_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * block_causal_mask ([ARS] "What mlx-arsenal ships": the mask block-diffusion
+ * models are trained with -- bidirectional inside a block, causal across
+ * blocks, aligned on absolute positions; "Mask conventions": additive, 0
+ * attend and -inf blocked; boolean-mask runtimes want the inverse reading).
+ *
+ * out[i * row_stride + j] for i < Lq (query at absolute position q_offset +
+ * i) and j < Lk (key at k_offset + j) is "attend" when floor((q_offset + i)
+ * / block_len) >= floor((k_offset + j) / block_len), else "blocked":
+ *   DLLM_MASK_F32 / DLLM_MASK_BF16  additive: 0 attend, -inf blocked;
+ *   DLLM_MASK_KEEP_U8               1 attend, 0 blocked.
+ * block_causal_mask(L, block_len) over a window from position 0 is Lq = Lk =
+ * L with zero offsets.  out: device; row_stride (elements) >= Lk.  Rows whose
+ * base and stride are 16-byte aligned are written with vector stores.
+ * ------------------------------------------------------------------------ */
+typedef enum { DLLM_MASK_F32 = 0, DLLM_MASK_BF16 = 1, DLLM_MASK_KEEP_U8 = 2 } dllm_mask_kind;
+
+dllm_status dllm_block_causal_mask(int64_t Lq, int64_t Lk, int64_t q_offset, int64_t k_offset, int64_t block_len,
+                                   dllm_mask_kind kind, void* out, int64_t row_stride, dllm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Fused commit step: the statistics pass and one commit rule (plus the
  * optional edit rule and canvas update) in one launch.  The rule of batch
  * row b runs as soon as its L rows' statistics are complete, inside the same

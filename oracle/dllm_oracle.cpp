@@ -241,6 +241,24 @@ inline float conf_of(float c) { return std::isnan(c) ? -std::numeric_limits<floa
 // An entropy as the entropy-bound rule sees it: NaN ranks as +inf.
 inline float ent_of(float h) { return std::isnan(h) ? std::numeric_limits<float>::infinity() : h; }
 
+// Entropies in the exact sums of the entropy-bound rule and the stopping
+// criterion: fixed point with 40 fractional bits, q(h) = floor(min(max(h, 0),
+// 64) 2^40), NaN counting as 64.  Exact: the clamped value times 2^40 is an
+// integer-or-fraction fp32 value below 2^46 whose floor converts exactly, and
+// sums of at most 2^16 of them stay below 2^62.
+int64_t fixed_q(float h) {
+  const float c = std::isnan(h) ? 64.0f : std::min(std::max(h, 0.0f), 64.0f);
+  return static_cast<int64_t>(std::floor(static_cast<double>(c) * 1099511627776.0));
+}
+
+// A bound compared with such a sum: S <= bound <=> S <= floor(bound 2^40)
+// (S is an integer); -1 for a negative bound (nothing is within it); bounds
+// above 2^22 (more than any sum reaches) count as 2^22.
+int64_t fixed_bound(float bound) {
+  if (bound < 0.0f) return -1;
+  return static_cast<int64_t>(std::floor(static_cast<double>(std::min(bound, 4194304.0f)) * 1099511627776.0));
+}
+
 // Candidate positions of batch row b, ranked by descending confidence.  The
 // sort is stable: among equal confidences the smaller position ranks first
 // ([ARS] "Deviations", the paragraph on ties).
@@ -409,10 +427,12 @@ int orc_factor_transfer(const float* conf, const uint8_t* cand, int64_t B, int64
 // entropy_bound_transfer.  [ARS] function table: rank by ascending entropy
 // and take the longest prefix whose members satisfy sum_{j<i} H_(j) <= gamma.
 // [MLXC] "Samplers and Reveal Policies": the rule always accepts one position
-// or more.  The prefix sum is accumulated in double, strictly in ranking order.
+// or more.  The pages fix no precision for the sum: it is taken exactly, in
+// the fixed point of fixed_q (40 fractional bits), and compared exactly with
+// gamma.
 int orc_entropy_bound_transfer(const float* entropy, const uint8_t* cand, int64_t B, int64_t L,
                                float gamma, uint8_t* commit) {
-  if (B < 0 || L < 0) return -1;
+  if (B < 0 || L < 0 || L > (static_cast<int64_t>(1) << 16) || std::isnan(gamma)) return -1;
   for (int64_t b = 0; b < B; ++b) {
     std::vector<int64_t> order;
     for (int64_t l = 0; l < L; ++l) {
@@ -423,10 +443,13 @@ int orc_entropy_bound_transfer(const float* entropy, const uint8_t* cand, int64_
       return ent_of(entropy[b * L + a]) < ent_of(entropy[b * L + c]);
     });
     const int64_t n_cand = static_cast<int64_t>(order.size());
-    double prefix = 0.0;  // sum of the entropies ranked before position i
+    // The prefix sums are exact in the fixed point of fixed_q, compared
+    // exactly with gamma (fixed_bound).
+    const int64_t gamma_q = fixed_bound(gamma);
+    int64_t prefix = 0;   // sum of q(H) over the entropies ranked before position i
     int64_t n = 0;
-    while (n < n_cand && prefix <= static_cast<double>(gamma)) {
-      prefix += static_cast<double>(ent_of(entropy[b * L + order[n]]));
+    while (n < n_cand && prefix <= gamma_q) {
+      prefix += fixed_q(ent_of(entropy[b * L + order[n]]));
       ++n;
     }
     if (n_cand > 0) n = std::max<int64_t>(n, 1);
@@ -532,23 +555,27 @@ int orc_renoise(const int32_t* sample, const uint8_t* accepted, const int32_t* n
 // One call of the stopping criterion on the (B, L) argmax canvas and
 // entropies.  count[b] < 0 means no previous canvas.  A row is stable when
 // its canvas equals the previous one; count[b] counts consecutive stable
-// calls; the row is confident when its mean entropy (summed in double in
-// position order, divided by L) is below confidence_threshold.  stop[b] =
-// count[b] >= stability_threshold and confident.  prev takes the canvas.
+// calls; the row is confident when its mean entropy is below
+// confidence_threshold, compared exactly in the fixed point of fixed_q:
+// sum_l q(H_l) < L q(threshold).  stop[b] = count[b] >= stability_threshold
+// and confident.  prev takes the canvas.  L <= 2^16, 0 <= threshold <= 64.
 int orc_stable_confident_stop(const int32_t* argmax, const float* entropy, int64_t B, int64_t L,
                               int32_t stability_threshold, float confidence_threshold, int32_t* prev,
                               int32_t* count, uint8_t* stop) {
-  if (B < 0 || L <= 0 || (B > 0 && (!argmax || !entropy || !prev || !count || !stop))) return -1;
+  if (B < 0 || L <= 0 || L > (static_cast<int64_t>(1) << 16) || stability_threshold < 0) return -1;
+  if (!(confidence_threshold >= 0.0f && confidence_threshold <= 64.0f)) return -1;
+  if (B > 0 && (!argmax || !entropy || !prev || !count || !stop)) return -1;
+  const int64_t thr_q = fixed_q(confidence_threshold);
   for (int64_t b = 0; b < B; ++b) {
     bool same = count[b] >= 0;
-    double sum = 0.0;
+    int64_t sum = 0;
     for (int64_t l = 0; l < L; ++l) {
       same = same && argmax[b * L + l] == prev[b * L + l];
-      sum += static_cast<double>(entropy[b * L + l]);
+      sum += fixed_q(entropy[b * L + l]);
     }
     count[b] = same ? count[b] + 1 : 0;
     for (int64_t l = 0; l < L; ++l) prev[b * L + l] = argmax[b * L + l];
-    const bool confident = sum / static_cast<double>(L) < static_cast<double>(confidence_threshold);
+    const bool confident = sum < L * thr_q;
     stop[b] = (count[b] >= stability_threshold && confident) ? 1 : 0;
   }
   return 0;

@@ -53,7 +53,10 @@ int orc_token_stats_ex(const void* logits, int dtype, int64_t n_rows, int64_t V,
                        int32_t* x0, double* prob, double* entropy, double* margin, int32_t* argmax,
                        int n_threads);
 
-/* Commit rules over (B, L) row-major confidences and 0/1 candidate masks. */
+/* Commit rules over (B, L) row-major confidences and 0/1 candidate masks.
+ * entropy_bound sums the ranked entropies exactly in fixed point with 40
+ * fractional bits (q as in stable_confident_stop) and compares exactly with
+ * gamma; L <= 2^16. */
 int orc_threshold_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
                            float tau, int strict, uint8_t* commit);
 int orc_topk_transfer(const float* conf, const uint8_t* cand, int64_t B, int64_t L,
@@ -77,7 +80,9 @@ int orc_block_ranges(int64_t P, int64_t gen_len, int64_t block_len, int align,
  *   j & 3 of counter (j >> 2, b lo, b hi, 1) under key.
  * renoise: out = accepted ? sample : noise, elementwise.
  * stable_confident_stop: one call of the stopping criterion; state prev
- *   (B, L) and count (B) (count < 0: no previous canvas). */
+ *   (B, L) and count (B) (count < 0: no previous canvas); a row is confident
+ *   when sum_l q(H_l) < L q(threshold), q(h) = floor(clamp(h, 0, 64) 2^40)
+ *   (NaN as 64): the mean entropy against the threshold, exactly.  L <= 2^16. */
 int orc_linear_temperature(int32_t remaining, int32_t num_steps, float t_min, float t_max, float* T);
 int orc_uniform_canvas(int64_t B, int64_t N, int64_t V, uint64_t key, int32_t* canvas);
 int orc_renoise(const int32_t* sample, const uint8_t* accepted, const int32_t* noise, int64_t n, int32_t* out);

@@ -214,3 +214,23 @@ def test_block_ranges_tile_the_generation_region():
                 assert r[0][0] == P
     assert len(oracle.block_ranges(128, 1024, 32)) == 32
     assert oracle.block_ranges(128, 1024, 32, True) == oracle.block_ranges(128, 1024, 32, False)
+
+
+def test_entropy_bound_sums_exactly():
+    """The prefix sums of the entropy-bound rule are exact (fixed point, 40
+    fractional bits) and compared exactly with gamma: sums that reach gamma
+    exactly are within it; a tiny excess is not; a NaN entropy ranks last."""
+    e = np.array([[0.25, 0.25, 0.5]], np.float32)          # exclusive sums 0, 0.25, 0.5
+    assert oracle.entropy_bound_transfer(e, np.ones_like(e, np.uint8), 0.5).tolist() == [[1, 1, 1]]
+    assert oracle.entropy_bound_transfer(e, np.ones_like(e, np.uint8), np.nextafter(np.float32(0.5), np.float32(0))
+                                         ).tolist() == [[1, 1, 0]]
+    # 1000 entropies of 2^-30 sum to 1000 * 2^-30 exactly: within gamma = 1000 * 2^-30, one ulp below is not
+    tiny = np.full((1, 1001), 2.0**-30, np.float32)
+    g = np.float32(1000 * 2.0**-30)
+    assert oracle.entropy_bound_transfer(tiny, np.ones_like(tiny, np.uint8), g).sum() == 1001
+    assert oracle.entropy_bound_transfer(tiny, np.ones_like(tiny, np.uint8),
+                                         np.nextafter(g, np.float32(0))).sum() == 1000
+    # NaN ranks last; its exclusive prefix is the other two: 0.01 > 0.005
+    n = np.array([[np.nan, 0.0, 0.01]], np.float32)
+    assert oracle.entropy_bound_transfer(n, np.ones_like(n, np.uint8), 100.0).tolist() == [[1, 1, 1]]
+    assert oracle.entropy_bound_transfer(n, np.ones_like(n, np.uint8), 0.005).tolist() == [[0, 1, 1]]

@@ -71,11 +71,20 @@ def test_stopping_criterion_sequences():
     assert st(b, e_low)[0] == 1
     st2 = oracle.StableConfidentStopping(1, 4, stability_threshold=2, confidence_threshold=0.005)
     assert [int(st2(a, e_low)[0]) for _ in range(4)] == [0, 0, 1, 1]
-    # confident means a mean strictly below the threshold
+    # confident means a mean strictly below the threshold, decided exactly:
+    # (0.25 + 0.75) / 2 equals 0.5, and one ulp less is below it
     st3 = oracle.StableConfidentStopping(1, 2, 1, 0.5)
     half = np.array([[0.25, 0.75]], np.float32)
     st3(np.array([[0, 0]], np.int32), half)
     assert st3(np.array([[0, 0]], np.int32), half)[0] == 0
+    below = np.array([[0.25, np.nextafter(np.float32(0.75), np.float32(0))]], np.float32)
+    assert st3(np.array([[0, 0]], np.int32), below)[0] == 1
+    # NaN and huge entropies count as 64; the threshold must lie in [0, 64]
+    st5 = oracle.StableConfidentStopping(1, 2, 0, 40.0)
+    assert st5(np.array([[0, 0]], np.int32), np.array([[np.nan, 0.0]], np.float32))[0] == 1   # mean 32
+    assert st5(np.array([[0, 0]], np.int32), np.array([[np.nan, 17.0]], np.float32))[0] == 0  # mean 40.5
+    with pytest.raises(ValueError):
+        oracle.StableConfidentStopping(1, 2, 1, 65.0)(np.zeros((1, 2), np.int32), np.zeros((1, 2), np.float32))
     # rows are independent
     st4 = oracle.StableConfidentStopping(2, 4, 1, 0.005)
     st4(np.vstack([a, a]), np.vstack([e_low, e_low]))

@@ -552,8 +552,8 @@ dllm_status dllm_renoise(const int32_t* sample, const uint8_t* accepted, const i
 dllm_status dllm_stable_confident_stop(const int32_t* argmax, const float* entropy, int64_t B, int64_t L,
                                        int32_t stability_threshold, float confidence_threshold, int32_t* prev,
                                        int32_t* count, uint8_t* stop, uint8_t* done, dllm_stream_t stream) {
-  if (B < 0 || L <= 0 || stability_threshold < 0 || std::isnan(confidence_threshold))
-    return DLLM_ERR_INVALID_ARGUMENT;
+  if (B < 0 || L <= 0 || L > (static_cast<int64_t>(1) << 16) || stability_threshold < 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!(confidence_threshold >= 0.0f && confidence_threshold <= 64.0f)) return DLLM_ERR_INVALID_ARGUMENT;
   if (B == 0) return DLLM_OK;
   if (B > INT32_MAX || !argmax || !entropy || !prev || !count) return DLLM_ERR_INVALID_ARGUMENT;
   void* args[] = {const_cast<int32_t**>(&argmax), const_cast<float**>(&entropy), &L, &stability_threshold,

@@ -163,6 +163,28 @@ __device__ __forceinline__ uint32_t float_key(float x) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Inverse of float_key.
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Exact sums of entropies (the entropy-bound rule, the stopping criterion):
+// fixed point with 40 fractional bits, q(h) = floor(min(max(h, 0), 64) 2^40),
+// NaN counting as 64.  The clamped value times 2^40 is exact in fp32 (a
+// power-of-two scaling) and below 2^46, so the conversion is exact and sums
+// of up to 2^16 values stay below 2^62; integer sums agree in any order.
+__device__ __forceinline__ long long fixed_q(float h) {
+  const float c = isnan(h) ? 64.0f : fminf(fmaxf(h, 0.0f), 64.0f);
+  return __float2ll_rz(c * 0x1p+40f);
+}
+
+// A bound compared with such a sum S: S <= bound <=> S <= floor(bound 2^40);
+// -1 for a negative bound; bounds above 2^22 (beyond any sum) count as 2^22.
+__device__ __forceinline__ long long fixed_bound(float bound) {
+  if (bound < 0.0f) return -1;
+  return __float2ll_rz(fminf(bound, 0x1p+22f) * 0x1p+40f);
+}
+
 constexpr float kSentinel = -0x1p+100f;   // NaN and values <= -2^100 become this
 constexpr float kAbsent = -0x1p+120f;     // suppressed ids become this (no mass, never chosen)
 constexpr uint32_t kSentinelBf16x2 = 0xF180F180u;  // two bf16 -2^100

@@ -67,6 +67,11 @@ __device__ __forceinline__ void rsync() {
     named_sync(BAR, NT);
 }
 
+// Exclusive prefix sum of one int64 per thread over the NT threads (in
+// thread order).  Uses s.red64; all NT threads must call it.
+template <int NT, int BAR>
+__device__ __forceinline__ long long rule_excl_scan(long long v, const struct RuleScratch& s, int tid);
+
 struct RuleScratch {
   uint64_t* keys;     // capacity `cap` keys (power of two)
   uint8_t* flags;     // capacity `cap` bytes
@@ -121,10 +126,18 @@ __device__ __forceinline__ int4 rule_sum4(int4 v, const RuleScratch& s, int tid)
 }
 
 // Ascending bitonic sort of n (a power of two) keys in shared memory.
+// Compare-exchange steps whose partners are 32 or more apart go through
+// shared memory with a barrier each; the steps below 32 of every stage run in
+// registers with warp shuffles (element e lives in thread e mod NT, so
+// partners e ^ j with j < 32 are lanes of the same warp).  Every lane of every
+// warp takes part in the shuffles: lanes past n carry dummy keys, which (n
+// being a power of two) only ever meet each other.
 template <int NT, int BAR>
 __device__ __forceinline__ void bitonic_sort(uint64_t* keys, int n, int tid) {
+  const int lane = tid & 31;
   for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+    int stride = size >> 1;
+    for (; stride >= 32; stride >>= 1) {
       rsync<NT, BAR>();
       for (int i = tid; i < (n >> 1); i += NT) {
         const int lo = 2 * i - (i & (stride - 1));
@@ -137,6 +150,18 @@ __device__ __forceinline__ void bitonic_sort(uint64_t* keys, int n, int tid) {
         }
       }
     }
+    rsync<NT, BAR>();
+    for (int r = 0; r * NT < n; ++r) {
+      const int e = r * NT + tid;
+      uint64_t v = e < n ? keys[e] : kNoKey;
+      const bool up = (e & size) == 0;
+      for (int j = stride; j > 0; j >>= 1) {
+        const uint64_t w = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+        const bool keep_min = ((lane & j) == 0) == up;
+        v = keep_min ? (w < v ? w : v) : (w > v ? w : v);
+      }
+      if (e < n) keys[e] = v;
+    }
   }
   rsync<NT, BAR>();
 }
@@ -148,6 +173,23 @@ __device__ __forceinline__ bool is_candidate(const RuleArgs& a, int64_t b, int64
   *tok_out = tok;
   if (a.cand) return __ldcg(a.cand + i) != 0;
   return tok == a.mask_id;
+}
+
+template <int NT, int BAR>
+__device__ __forceinline__ long long rule_excl_scan(long long v, const RuleScratch& s, int tid) {
+  const int lane = tid & 31, w = tid >> 5;
+  long long x = v;  // inclusive scan within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s.red64[w] = static_cast<uint64_t>(x);
+  rsync<NT, BAR>();
+  long long off = 0;
+  for (int k = 0; k < w; ++k) off += static_cast<long long>(s.red64[k]);
+  rsync<NT, BAR>();
+  return off + x - v;
 }
 
 // Runs the rule of batch row b.  All NT threads must call it.  Inputs written
@@ -216,21 +258,23 @@ __device__ void run_rule(const RuleArgs& a, int64_t b, const RuleScratch& s, int
         }
       }
       n_take = static_cast<int64_t>(rule_min_u64<NT, BAR>(first_fail, s, tid));
-    } else {  // entropy bound: sequential double prefix in ranking order
-      if (tid == 0) {
-        double prefix = 0.0;
-        int64_t n_acc = 0;
-        while (n_acc < n_cand_total && prefix <= static_cast<double>(a.gamma)) {
-          const int64_t l = static_cast<int64_t>(s.keys[n_acc] & 0xFFFFFFFFu);
-          const float h = nan_to(__ldcg(a.entropy + base + l), __int_as_float(0x7F800000));
-          prefix = __dadd_rn(prefix, static_cast<double>(h));
-          ++n_acc;
-        }
-        s.red64[0] = static_cast<uint64_t>(n_acc);
+    } else {  // entropy bound: exact fixed-point prefix sums of the ranking, in parallel
+      // Each thread takes a contiguous run of ranks; the entropy of a rank is
+      // read back from its key.  S_i (the sum of the ranks before i) never
+      // decreases, so the ranks within the bound are a prefix: count them.
+      const long long bound = fixed_bound(a.gamma);
+      const int per = (n_cand_total + NT - 1) / NT;
+      const int i0 = tid * per < n_cand_total ? tid * per : n_cand_total;
+      const int i1 = i0 + per < n_cand_total ? i0 + per : n_cand_total;
+      long long run = 0;
+      for (int i = i0; i < i1; ++i) run += fixed_q(key_to_float(static_cast<uint32_t>(s.keys[i] >> 32)));
+      long long S = rule_excl_scan<NT, BAR>(run, s, tid);
+      int within = 0;
+      for (int i = i0; i < i1; ++i) {
+        within += S <= bound ? 1 : 0;
+        S += fixed_q(key_to_float(static_cast<uint32_t>(s.keys[i] >> 32)));
       }
-      rsync<NT, BAR>();
-      n_take = static_cast<int64_t>(s.red64[0]);
-      rsync<NT, BAR>();
+      n_take = rule_sum4<NT, BAR>(make_int4(within, 0, 0, 0), s, tid).x;
     }
     if (a.rule != kRuleTopk && n_cand_total > 0 && n_take < 1) n_take = 1;
     // flags[l] = 1 for the first n_take ranked candidates

@@ -51,19 +51,19 @@ __global__ void renoise_kernel(const int32_t* __restrict__ sample, const uint8_t
 }
 
 constexpr int kStopThreads = 256;
-constexpr int kStopChunk = 1024;
 
 // One call of the stopping criterion, one CTA per batch row b: the row is
 // stable when its argmax canvas equals prev (count[b] >= 0 says prev holds
 // a canvas); count[b] counts consecutive stable calls; the row is confident
-// when its mean entropy -- summed in double in position order by one thread,
-// then divided by L -- is below the threshold.  prev takes the canvas;
-// stop[b] = count >= stability and confident; done[b] |= stop[b].
+// when its mean entropy is below the threshold, decided exactly in the fixed
+// point of fixed_q (sum_l q(H_l) < L q(threshold): integer sums, so any order
+// gives the same answer).  prev takes the canvas; stop[b] = count >=
+// stability and confident; done[b] |= stop[b].
 __global__ void __launch_bounds__(kStopThreads) stop_kernel(const int32_t* __restrict__ argmax,
                                                              const float* __restrict__ entropy, int64_t L,
                                                              int32_t stability, float threshold, int32_t* prev,
                                                              int32_t* count, uint8_t* stop, uint8_t* done) {
-  __shared__ float chunk[kStopChunk];
+  __shared__ long long part[kStopThreads / 32];
   pdl_wait();
   pdl_launch_dependents();
   const int64_t b = blockIdx.x;
@@ -71,26 +71,24 @@ __global__ void __launch_bounds__(kStopThreads) stop_kernel(const int32_t* __res
   int32_t* pv = prev + b * L;
   const float* e = entropy + b * L;
   int diff = 0;
+  long long sum = 0;
   for (int64_t l = threadIdx.x; l < L; l += kStopThreads) {
     const int32_t v = a[l];
     diff |= v != pv[l] ? 1 : 0;
     pv[l] = v;
+    sum += fixed_q(e[l]);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = sum;
   const int any_diff = __syncthreads_or(diff);
-  double sum = 0.0;
-  for (int64_t c0 = 0; c0 < L; c0 += kStopChunk) {
-    const int n = static_cast<int>(L - c0 < kStopChunk ? L - c0 : kStopChunk);
-    for (int k = threadIdx.x; k < n; k += kStopThreads) chunk[k] = e[c0 + k];
-    __syncthreads();
-    if (threadIdx.x == 0)
-      for (int k = 0; k < n; ++k) sum = __dadd_rn(sum, static_cast<double>(chunk[k]));
-    __syncthreads();
-  }
   if (threadIdx.x == 0) {
+    long long total = 0;
+    for (int w = 0; w < kStopThreads / 32; ++w) total += part[w];
     const int32_t c = count[b];
     const int32_t nc = (c >= 0 && !any_diff) ? c + 1 : 0;
     count[b] = nc;
-    const bool confident = __ddiv_rn(sum, static_cast<double>(L)) < static_cast<double>(threshold);
+    const bool confident = total < static_cast<long long>(L) * fixed_q(threshold);
     const uint8_t st = (nc >= stability && confident) ? 1 : 0;
     if (stop) stop[b] = st;
     if (done && st) done[b] = 1;

@@ -205,8 +205,9 @@ dllm_status dllm_factor_transfer(const float* conf, const uint8_t* cand, int64_t
 
 /* [ARS] entropy_bound_transfer; [MLXC] at least one accepted: commit the
  * longest prefix of the ascending-entropy ranking whose members have
- * sum_{j<i} H_(j) <= gamma, the sum accumulated in double in ranking order;
- * at least one when the row has candidates. */
+ * sum_{j<i} H_(j) <= gamma, the sum taken exactly in fixed point with 40
+ * fractional bits (each H as floor(clamp(H, 0, 64) 2^40), NaN ranking last)
+ * and compared exactly with gamma; at least one when the row has candidates. */
 dllm_status dllm_entropy_bound_transfer(const float* entropy, const uint8_t* cand, int64_t B,
                                         int64_t L, float gamma, uint8_t* commit,
                                         const int32_t* x0, int32_t* canvas, int64_t canvas_stride,
@@ -272,10 +273,12 @@ dllm_status dllm_renoise(const int32_t* sample, const uint8_t* accepted, const i
  * prev (B, L) int32, the previous canvas; count (B) int32, consecutive
  * stable calls, -1 before the first call (then nothing is stable).  Per row:
  * stable = count >= 0 and argmax == prev everywhere; count = stable ? count
- * + 1 : 0; prev = argmax; confident = (sum of the L entropies in double in
- * position order) / L < confidence_threshold; stop[b] = count >=
- * stability_threshold and confident.  stop (B) uint8 and done (B) uint8 are
- * nullable outputs; done[b] becomes 1 when stop[b] is (never 0). */
+ * + 1 : 0; prev = argmax; confident = the mean entropy is below
+ * confidence_threshold, decided exactly in fixed point: sum_l q(H_l) <
+ * L q(confidence_threshold), q(h) = floor(clamp(h, 0, 64) 2^40), NaN as 64;
+ * stop[b] = count >= stability_threshold and confident.  stop (B) uint8 and
+ * done (B) uint8 are nullable outputs; done[b] becomes 1 when stop[b] is
+ * (never 0).  L <= 2^16, 0 <= confidence_threshold <= 64, stability >= 0. */
 dllm_status dllm_stable_confident_stop(const int32_t* argmax, const float* entropy, int64_t B, int64_t L,
                                        int32_t stability_threshold, float confidence_threshold, int32_t* prev,
                                        int32_t* count, uint8_t* stop, uint8_t* done, dllm_stream_t stream);

@@ -260,3 +260,22 @@ def block_causal_mask(Lq: int, block_len: int, Lk: int = None, q_offset: int = 0
     _check(lib().orc_block_causal_mask(int(Lq), int(Lk), int(q_offset), int(k_offset), int(block_len), _p(out)),
            "block_causal_mask")
     return out
+
+
+# ---------------------------------------------------------------------------
+# fused LM head + statistics
+# ---------------------------------------------------------------------------
+def lm_head_logits(hidden_bits: np.ndarray, weight_bits: np.ndarray) -> np.ndarray:
+    """logits = hidden @ weight^T from bf16 bit arrays, (T, d) and (V, d): the
+    exact products summed in double (a library matmul in float64), rounded
+    once to fp32 -- what an fp32-accumulating GEMM approximates."""
+    h = (np.ascontiguousarray(hidden_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    w = (np.ascontiguousarray(weight_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    return (h.astype(np.float64) @ w.astype(np.float64).T).astype(np.float32)
+
+
+def lm_head_stats(hidden_bits, weight_bits, temperature: float = 0.0, key: int = 0, suppress_ids=(),
+                  n_threads: int = 0):
+    """token_stats of the LM head's logits (lm_head_logits): x0, prob, entropy per row of hidden."""
+    return token_stats(lm_head_logits(hidden_bits, weight_bits), dtype="f32", temperature=temperature, key=key,
+                       suppress_ids=suppress_ids, n_threads=n_threads)

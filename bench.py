@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="llada", choices=["llada", "tiny", "dream", "large", "loop", "uniform", "mask"])
+    ap.add_argument("--workload", default="llada", choices=["llada", "tiny", "dream", "large", "loop", "uniform", "mask", "lmhead"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -627,6 +627,89 @@ def run_mask(args, rank, world):
     }
 
 
+def run_lmhead(args, rank, world):
+    """The LM head fused with the statistics pass at the LLaDA-8B LM head
+    shape: 32 hidden states (one 32-token block) x a 126464 x 4096 bf16
+    weight, greedy, suppressing the mask id.  Reports the GB/s of the bytes
+    the fused call must read (weight + hidden, the logits never written), the
+    tensor-core rate, and the unfused path (cuBLAS logits, then token_stats)
+    timed the same way."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import commit_step_gb300 as cs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    T, d, V = 32, 4096, 126464
+    h, w, _ = W.lm_head_inputs(0, T, d, V)
+    hd = torch.from_numpy(h.view(np.int16)).to(dev).view(torch.bfloat16)
+    wd = torch.from_numpy(w.view(np.int16)).to(dev).view(torch.bfloat16)
+    del w
+    out = (torch.empty(T, dtype=torch.int32, device=dev), torch.empty(T, device=dev), torch.empty(T, device=dev))
+    steps = args.steps if args.steps is not None else 400
+    warmup = max(3, args.warmup if args.warmup is not None else 10)
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    logits16 = torch.empty((T, V), dtype=torch.bfloat16, device=dev)
+
+    def fused():
+        cs.lm_head_stats(hd, wd, suppress_ids=[126336], out=out, stream=stream)
+
+    def unfused():
+        torch.matmul(hd, wd.t(), out=logits16)
+        cs.token_stats(logits16, suppress_ids=[126336], out=out, stream=stream)
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.synchronize()
+        G = 20
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(G):
+                fn()
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, n // G)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / (reps * G), reps * G
+
+    with ClockSampler(gpu_query_id(torch.cuda.get_device_properties(dev), dev.index)) as clk:
+        ms, n = timed(fused, steps)
+    ms = max_over_ranks(ms, dev, world)
+    ms_unfused, _ = timed(unfused, max(20, steps // 4))
+    nbytes = V * d * 2 + T * d * 2
+    value = nbytes / (ms / 1e3) / 1e9 * world
+    peak, kind = measured_peaks()
+    flops = 2.0 * T * d * V
+    return {
+        "metric": "fused LM head + token_stats GB/s (weight read)", "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": n, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator, dllm_workloads.lm_head_inputs)",
+        "config": {"workload": f"LM head T={T} d={d} V={V} bf16 (LLaDA-8B head shape), greedy, suppress mask id",
+                   "l2": "the 1.04 GB weight is larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / world / peak, 4), "traffic": None,
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({kind})"},
+        "tensor_tflops": round(flops / (ms / 1e3) / 1e12, 1),
+        "unfused": {"ms_per_step": ms_unfused, "path": "torch.matmul (cuBLAS) to bf16 logits, then token_stats",
+                    "speedup_of_fused": round(ms_unfused / ms, 3)},
+        "gpu_launches": 2 * n, "clocks": clk.summary(),
+    }
+
+
 def run_reference(args, rank, world):
     w = W.build(args.workload)
     steps = args.steps if args.steps is not None else 3
@@ -669,8 +752,9 @@ def main():
 
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    if args.workload in ("loop", "uniform", "mask"):
-        res = {"loop": run_loop, "uniform": run_uniform, "mask": run_mask}[args.workload](args, rank, world)
+    if args.workload in ("loop", "uniform", "mask", "lmhead"):
+        res = {"loop": run_loop, "uniform": run_uniform, "mask": run_mask,
+               "lmhead": run_lmhead}[args.workload](args, rank, world)
         if rank == 0:
             print(json.dumps(res))
         return 0

@@ -35,6 +35,7 @@ EXPORTS = (
     "dllm_edit_transfer", "dllm_transfer_schedule", "dllm_block_ranges", "dllm_commit_step",
     "dllm_workspace_fault", "dllm_token_stats_noalloc", "dllm_token_stats_ex", "dllm_linear_temperature",
     "dllm_uniform_canvas", "dllm_renoise", "dllm_stable_confident_stop", "dllm_block_causal_mask",
+    "dllm_lm_head_stats_workspace_size", "dllm_lm_head_stats",
 )
 
 
@@ -91,8 +92,11 @@ def _load() -> C.CDLL:
     lib.dllm_renoise.argtypes = [P, P, P, P, i64, i64, P, P]
     lib.dllm_stable_confident_stop.argtypes = [P, P, i64, i64, i32, f32, P, P, P, P, P]
     lib.dllm_block_causal_mask.argtypes = [i64, i64, i64, i64, i64, C.c_int, P, i64, P]
+    lib.dllm_lm_head_stats_workspace_size.argtypes = [i64, i64, i64]
+    lib.dllm_lm_head_stats_workspace_size.restype = sz
+    lib.dllm_lm_head_stats.argtypes = [P, i64, i64, i64, P, i64, i64, f32, u64, P, i32, P, P, P, P, i64, P, sz, P]
     for name in EXPORTS[3:]:
-        if name != "dllm_token_stats_workspace_size":
+        if name not in ("dllm_token_stats_workspace_size", "dllm_lm_head_stats_workspace_size"):
             getattr(lib, name).restype = C.c_int
     return lib
 
@@ -513,3 +517,42 @@ def block_causal_mask(L: int, block_len: int, Lk: Optional[int] = None, q_offset
     _check(_lib.dllm_block_causal_mask(L, Lk, q_offset, k_offset, block_len, kinds[out.dtype], _ptr(out),
                                        out.stride(0), _stream(stream)), "dllm_block_causal_mask")
     return out
+
+
+_WS_LH = {}
+
+
+def lm_head_stats(hidden: torch.Tensor, weight: torch.Tensor, temperature: float = 0.0, key: int = 0,
+                  suppress_ids: Sequence[int] = (), out=None, logits: Optional[torch.Tensor] = None,
+                  ws: Optional[torch.Tensor] = None, stream=None):
+    """The LM head fused with the statistics pass: x0, prob, entropy of the
+    logits hidden @ weight^T (bf16 in, fp32 tensor-core accumulation) without
+    storing them.  hidden (T, d) and weight (V, d) bf16 with unit column
+    stride; ``logits`` (T, V) float32, if given, receives the logits too."""
+    _need_cuda(hidden, weight, logits)
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16 or hidden.dim() != 2 or weight.dim() != 2:
+        raise TypeError("hidden and weight must be 2-D bfloat16 tensors")
+    if hidden.stride(1) != 1 or weight.stride(1) != 1 or hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden (T, d) and weight (V, d) need unit column stride and the same d")
+    T, d = hidden.shape
+    V = weight.shape[0]
+    if out is None:
+        out = (torch.empty((T,), dtype=torch.int32, device=hidden.device),
+               torch.empty((T,), dtype=torch.float32, device=hidden.device),
+               torch.empty((T,), dtype=torch.float32, device=hidden.device))
+    x0, prob, ent = out
+    if logits is not None and (logits.dtype != torch.float32 or logits.shape != (T, V) or logits.stride(1) != 1):
+        raise ValueError("logits must be a (T, V) float32 tensor with unit column stride")
+    if ws is None:
+        need = int(_lib.dllm_lm_head_stats_workspace_size(T, V, d))
+        key_ = (hidden.device.index,)
+        ws = _WS_LH.get(key_)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(need, dtype=torch.uint8, device=hidden.device)
+            _WS_LH[key_] = ws
+    sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
+    _check(_lib.dllm_lm_head_stats(_ptr(hidden), T, d, hidden.stride(0), _ptr(weight), V, weight.stride(0),
+                                   float(temperature), int(key) & (2**64 - 1), sup, len(suppress_ids), _ptr(x0),
+                                   _ptr(prob), _ptr(ent), _ptr(logits), 0 if logits is None else logits.stride(0),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "dllm_lm_head_stats")
+    return x0, prob, ent

@@ -45,9 +45,13 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     Input construction only: it decides which bf16 values the workload holds.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32).astype(np.uint64)
-    rounded = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+    b = x.view(np.uint32)
     nan = np.isnan(x)
+    # below 2^32 for every non-NaN pattern (at most 0xFF800000 + 0x8000)
+    bb = np.where(nan, np.uint32(0), b)
+    bb += np.uint32(0x7FFF)
+    bb += (b >> np.uint32(16)) & np.uint32(1)
+    rounded = (bb >> np.uint32(16)).astype(np.uint16)
     if nan.any():
         rounded[nan] = ((b[nan] >> 16) | 0x40).astype(np.uint16)  # keep it a quiet NaN
     return rounded
@@ -413,3 +417,30 @@ class UniformGenerator:
 
 def uniform_spec(**kw) -> UniformSpec:
     return UniformSpec(**kw)
+
+
+# --------------------------------------------------------------------------
+# Fused LM head + statistics: hidden states and an LM-head weight.
+#
+# hidden ~ N(0, 1) per element; weight ~ N(0, 1/d), so the logits are about
+# N(0, 1); then for every token t the weight row of a seeded target id gets
+# + boost h_t / |h_t|^2 added, which raises that token's logit at the target
+# by about `boost` (its argmax is then the target unless the boost is small).
+# Both returned as bf16 bits; generated in row chunks so any V fits.
+# --------------------------------------------------------------------------
+
+def lm_head_inputs(seed: int, T: int, d: int, V: int, boost: float = 8.0):
+    tag = 7
+    g = _rng(seed, tag, 1)
+    hidden = g.standard_normal((T, d), dtype=np.float32)
+    weight = np.empty((V, d), dtype=np.uint16)
+    targets = _rng(seed, tag, 2).integers(0, V, size=T)
+    chunk = 8192
+    for c0 in range(0, V, chunk):
+        c1 = min(V, c0 + chunk)
+        wc = _rng(seed, tag, 3, c0).standard_normal((c1 - c0, d), dtype=np.float32) * np.float32(1.0 / np.sqrt(d))
+        for t in np.flatnonzero((targets >= c0) & (targets < c1)):
+            h = hidden[t]
+            wc[targets[t] - c0] += np.float32(boost) * h / np.float32(h @ h)
+        weight[c0:c1] = f32_to_bf16_bits(wc)
+    return f32_to_bf16_bits(hidden), weight, targets

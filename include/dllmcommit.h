@@ -304,6 +304,33 @@ dllm_status dllm_block_causal_mask(int64_t Lq, int64_t Lk, int64_t q_offset, int
                                    dllm_mask_kind kind, void* out, int64_t row_stride, dllm_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * LM head fused with the statistics pass (mojo-dllm manual, "The GPU path":
+ * the LM head's rows only feed the row statistics; the logits need not reach
+ * HBM).  logits[t, v] = sum_k hidden[t, k] weight[v, k] (bf16 inputs, fp32
+ * tensor-core accumulation), then x0 / prob / entropy exactly as
+ * dllm_token_stats defines them (greedy or Gumbel-max with the same noise:
+ * row = t), without the logits ever being stored.
+ *
+ * hidden  device bf16 (T, d), rows hidden_stride elements apart.
+ * weight  device bf16 (V, d), rows weight_stride elements apart (the LM
+ *         head's weight in its usual [vocab, hidden] layout).
+ * d a multiple of 64; both bases 16-byte aligned and both row strides a
+ * multiple of 8 elements (else DLLM_ERR_UNSUPPORTED).
+ * logits  optional device fp32 (T, V) output with row stride logits_stride
+ *         (NULL: the logits are not written -- the point of the fusion).
+ * workspace >= dllm_lm_head_stats_workspace_size(T, V, d) bytes (any
+ *         contents; it holds per-CTA partials).  Other arguments as in
+ *         dllm_token_stats.
+ * ------------------------------------------------------------------------ */
+size_t dllm_lm_head_stats_workspace_size(int64_t T, int64_t V, int64_t d);
+
+dllm_status dllm_lm_head_stats(const void* hidden, int64_t T, int64_t d, int64_t hidden_stride,
+                               const void* weight, int64_t V, int64_t weight_stride, float temperature,
+                               uint64_t key, const int32_t* suppress_ids, int32_t n_suppress, int32_t* x0,
+                               float* prob, float* entropy, float* logits, int64_t logits_stride,
+                               void* workspace, size_t workspace_bytes, dllm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Fused commit step: the statistics pass and one commit rule (plus the
  * optional edit rule and canvas update) in one launch.  The rule of batch
  * row b runs as soon as its L rows' statistics are complete, inside the same

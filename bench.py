@@ -36,7 +36,8 @@ import dllm_workloads as W  # noqa: E402
 
 METRIC = "token_stats+commit logits GB/s (% of GB300 HBM peak); canvas positions/s"
 KERNEL_SOURCES = ("dllm_stats_kernels.cuh", "dllm_stats.cuh", "dllm_rules.cuh", "dllm_device.cuh", "dllm_gumbel.cuh",
-                  "dllm_stats_greedy.cu", "dllm_stats_sample.cu", "dllm_stats_margin.cu", "dllm_stats_dispatch.cu")
+                  "dllm_stats_greedy.cu", "dllm_stats_sample.cu", "dllm_stats_margin.cu", "dllm_stats_dispatch.cu",
+                  "dllm_lmhead.cu")
 
 
 def parse():
@@ -701,8 +702,8 @@ def run_lmhead(args, rank, world):
         "config": {"workload": f"LM head T={T} d={d} V={V} bf16 (LLaDA-8B head shape), greedy, suppress mask id",
                    "l2": "the 1.04 GB weight is larger than L2"},
         "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(value / world / peak, 4), "traffic": None,
-                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({kind})"},
+                     "frac": round(value / world / peak, 4), "traffic": recorded_traffic("lmhead"),
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({kind})", "kernel": recorded_kernel("lmhead")},
         "tensor_tflops": round(flops / (ms / 1e3) / 1e12, 1),
         "unfused": {"ms_per_step": ms_unfused, "path": "torch.matmul (cuBLAS) to bf16 logits, then token_stats",
                     "speedup_of_fused": round(ms_unfused / ms, 3)},

@@ -5,7 +5,8 @@
 // consumed by the row statistics, so the logits z = h W^T need not reach
 // HBM.  logits tile = hidden tile (128 tokens x d) x weight tile (128 ids x
 // d)^T on the 5th-generation tensor cores: TMA brings 64-wide K slabs of both
-// into a shared-memory ring of up to 16 stages (128-byte swizzle), one thread issues
+// into a shared-memory ring of up to 16 stages filling the CTA's shared memory
+// (128-byte swizzle), one thread issues
 // tcgen05.mma (kind::f16, bf16 in, fp32 accumulate) into one of two TMEM
 // accumulators (128 lanes x 128 columns each), and four epilogue warps read
 // each finished accumulator back with tcgen05.ld -- thread i of warp w holds
@@ -39,15 +40,16 @@ constexpr int kLhBK = 64;                        // K per stage: one 128-byte sw
 constexpr int kLhUK = 16;                        // K of one tcgen05.mma.kind::f16
 constexpr int kLhMaxStages = 16;
 constexpr int kLhATile = kLhBM * kLhBK * 2;      // 16 KB: a full 128-row hidden tile
-constexpr int kLhRingBytes = 200 * 1024;         // stages of (hidden rows + weight tile) within this
 constexpr int kLhEpiWarps = 4;                   // one warpgroup: warp w reads TMEM lanes 32 w .. 32 w + 31
 constexpr int kLhTmaWarp = kLhEpiWarps;
 constexpr int kLhMmaWarp = kLhEpiWarps + 1;
 constexpr int kLhThreads = (kLhEpiWarps + 2) * 32;
 constexpr int kLhTmemCols = 2 * kLhMaxBN;        // two accumulators, at columns 0 and 256
-// The ring, plus slack for alignment (1 KB) and for the MMA's reads of a
-// hidden tile's unused rows past the last stage (at most a full tile).
-constexpr int kLhSmem = kLhRingBytes + kLhATile + 1024;
+// Dynamic shared memory: the ring, plus 1 KB to align it, plus slack for the
+// MMA's reads of a hidden tile's unused rows past the last stage (a full
+// tile less the rows the box brings).  kLhSmem is the most a CTA may ask for
+// (227 KB less the static barriers).
+constexpr int kLhSmem = 227 * 1024 - 1024;
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator
 // (bits 4-5 = 1), bf16 A and B (bits 7-9, 10-12 = 1), both K-major (bits 15,
@@ -550,7 +552,9 @@ dllm_status dllm_lm_head_stats(const void* hidden, int64_t T, int64_t d, int64_t
   p.d = d;
   p.n_k = static_cast<int32_t>(d / kLhBK);
   p.slabs = 1;  // two measured no faster on GB300 (the limit is the bytes in flight, not DRAM locality)
-  p.stages = std::min(kLhMaxStages, kLhRingBytes / (p.slabs * (p.a_bytes + p.b_bytes)));
+  const int32_t slack = kLhATile - p.a_bytes + 1024;
+  p.stages = std::min(kLhMaxStages, (kLhSmem - slack) / (p.slabs * (p.a_bytes + p.b_bytes)));
+  const size_t smem = static_cast<size_t>(p.stages) * p.slabs * (p.a_bytes + p.b_bytes) + slack;
   p.n_t = static_cast<int32_t>(n_t);
   p.n_v = static_cast<int32_t>((V + bn - 1) / bn);
   p.P = static_cast<int32_t>(P);
@@ -575,7 +579,7 @@ dllm_status dllm_lm_head_stats(const void* hidden, int64_t T, int64_t d, int64_t
   void* args[] = {&p};
   dllm_status st = lh_launch(gumbel ? reinterpret_cast<const void*>(&lm_head_kernel<true>)
                                     : reinterpret_cast<const void*>(&lm_head_kernel<false>),
-                             dim3(static_cast<unsigned>(P)), dim3(kLhThreads), kLhSmem, s, args);
+                             dim3(static_cast<unsigned>(P)), dim3(kLhThreads), smem, s, args);
   if (st != DLLM_OK) return st;
 
   StatsParams sp;

@@ -35,7 +35,7 @@ EXPORTS = (
     "dllm_edit_transfer", "dllm_transfer_schedule", "dllm_block_ranges", "dllm_commit_step",
     "dllm_workspace_fault", "dllm_token_stats_noalloc", "dllm_token_stats_ex", "dllm_linear_temperature",
     "dllm_uniform_canvas", "dllm_renoise", "dllm_stable_confident_stop", "dllm_block_causal_mask",
-    "dllm_lm_head_stats_workspace_size", "dllm_lm_head_stats",
+    "dllm_lm_head_stats_workspace_size", "dllm_lm_head_stats", "dllm_uniform_update",
 )
 
 
@@ -92,6 +92,7 @@ def _load() -> C.CDLL:
     lib.dllm_renoise.argtypes = [P, P, P, P, i64, i64, P, P]
     lib.dllm_stable_confident_stop.argtypes = [P, P, i64, i64, i32, f32, P, P, P, P, P]
     lib.dllm_block_causal_mask.argtypes = [i64, i64, i64, i64, i64, C.c_int, P, i64, P]
+    lib.dllm_uniform_update.argtypes = [P, P, P, P, i64, i64, i64, u64, i32, f32, P, P, P, P, P, P]
     lib.dllm_lm_head_stats_workspace_size.argtypes = [i64, i64, i64]
     lib.dllm_lm_head_stats_workspace_size.restype = sz
     lib.dllm_lm_head_stats.argtypes = [P, i64, i64, i64, P, i64, i64, f32, u64, P, i32, P, P, P, P, i64, P, sz, P]
@@ -556,3 +557,20 @@ def lm_head_stats(hidden: torch.Tensor, weight: torch.Tensor, temperature: float
                                    _ptr(prob), _ptr(ent), _ptr(logits), 0 if logits is None else logits.stride(0),
                                    _ptr(ws), ws.numel(), _stream(stream)), "dllm_lm_head_stats")
     return x0, prob, ent
+
+
+def uniform_update(sample: torch.Tensor, accepted: torch.Tensor, step_argmax: torch.Tensor, entropy: torch.Tensor,
+                   V: int, noise_key: int, stop: "StableConfidentStopping", canvas: torch.Tensor,
+                   argmax: torch.Tensor, done: torch.Tensor, stream=None) -> None:
+    """The rest of one uniform-noise step in one launch: re-noise the canvas
+    (rows not done), take the step's argmax into ``argmax`` (rows not done),
+    and update ``stop``'s state and the done flags (dllm_uniform_update)."""
+    B, N = sample.shape
+    _need_cuda(sample, accepted, step_argmax, entropy, canvas, argmax, done)
+    for t in (sample, accepted, step_argmax, entropy, canvas, argmax):
+        if t.shape != (B, N) or not t.is_contiguous():
+            raise ValueError("uniform_update takes contiguous (B, N) tensors")
+    _check(_lib.dllm_uniform_update(_ptr(sample), _ptr(accepted), _ptr(step_argmax), _ptr(entropy), B, N, V,
+                                    int(noise_key) & (2**64 - 1), stop.stability_threshold,
+                                    stop.confidence_threshold, _ptr(canvas), _ptr(argmax), _ptr(stop.prev),
+                                    _ptr(stop.count), _ptr(done), _stream(stream)), "dllm_uniform_update")

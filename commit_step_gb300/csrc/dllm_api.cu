@@ -19,6 +19,7 @@ const void* schedule_kernel_ptr();
 const void* uniform_canvas_kernel_ptr();
 const void* renoise_kernel_ptr();
 const void* stop_kernel_ptr();
+const void* uniform_update_kernel_ptr();
 const void* mask_kernel_ptr(int es);
 }  // namespace dllm
 
@@ -559,6 +560,26 @@ dllm_status dllm_stable_confident_stop(const int32_t* argmax, const float* entro
   void* args[] = {const_cast<int32_t**>(&argmax), const_cast<float**>(&entropy), &L, &stability_threshold,
                   &confidence_threshold, &prev, &count, &stop, &done};
   return launch(stop_kernel_ptr(), dim3(static_cast<unsigned>(B)), dim3(256), 0,
+                reinterpret_cast<cudaStream_t>(stream), args);
+}
+
+dllm_status dllm_uniform_update(const int32_t* sample, const uint8_t* accepted, const int32_t* step_argmax,
+                                const float* entropy, int64_t B, int64_t N, int64_t V, uint64_t noise_key,
+                                int32_t stability_threshold, float confidence_threshold, int32_t* canvas,
+                                int32_t* argmax, int32_t* prev, int32_t* count, uint8_t* done, dllm_stream_t stream) {
+  if (B < 0 || N <= 0 || N > (static_cast<int64_t>(1) << 16) || V <= 0 || V > INT32_MAX || stability_threshold < 0)
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (!(confidence_threshold >= 0.0f && confidence_threshold <= 64.0f)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (B == 0) return DLLM_OK;
+  if (B > INT32_MAX || !sample || !accepted || !step_argmax || !entropy || !canvas || !argmax || !prev || !count ||
+      !done)
+    return DLLM_ERR_INVALID_ARGUMENT;
+  PhiloxSchedule ks = philox_schedule(noise_key);
+  uint32_t v32 = static_cast<uint32_t>(V);
+  void* args[] = {&ks, const_cast<int32_t**>(&sample), const_cast<uint8_t**>(&accepted),
+                  const_cast<int32_t**>(&step_argmax), const_cast<float**>(&entropy), &N, &v32,
+                  &stability_threshold, &confidence_threshold, &canvas, &argmax, &prev, &count, &done};
+  return launch(uniform_update_kernel_ptr(), dim3(static_cast<unsigned>(B)), dim3(256), 0,
                 reinterpret_cast<cudaStream_t>(stream), args);
 }
 

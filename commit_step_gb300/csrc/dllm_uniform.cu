@@ -95,7 +95,69 @@ __global__ void __launch_bounds__(kStopThreads) stop_kernel(const int32_t* __res
   }
 }
 
+// The rest of one uniform-noise step after the statistics, one CTA per batch
+// row b, in one launch -- the same results as uniform_canvas (key), renoise
+// with the done flags as frozen rows, renoise of the argmax (accepted ==
+// nullptr, same frozen rows) and the stopping criterion, in that order:
+//   if !done[b]: canvas[b, j] = accepted ? sample : noise(j); argmax[b, j] = step_argmax[b, j]
+//   then the criterion on argmax[b, :] and entropy[b, :] (prev, count), done[b] |= stop.
+__global__ void __launch_bounds__(kStopThreads) uniform_update_kernel(
+    const __grid_constant__ PhiloxSchedule ks, const int32_t* __restrict__ sample,
+    const uint8_t* __restrict__ accepted, const int32_t* __restrict__ step_argmax, const float* __restrict__ entropy,
+    int64_t N, uint32_t V, int32_t stability, float threshold, int32_t* canvas, int32_t* argmax, int32_t* prev,
+    int32_t* count, uint8_t* done) {
+  __shared__ long long part[kStopThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t b = blockIdx.x;
+  const bool frozen = done[b] != 0;
+  const int64_t base = b * N;
+  int diff = 0;
+  long long sum = 0;
+  // thread t takes groups of four consecutive positions: one Philox call each
+  for (int64_t g = threadIdx.x; g * 4 < N; g += kStopThreads) {
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (!frozen) {
+      const uint4 r = philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(b),
+                                    static_cast<uint32_t>(static_cast<uint64_t>(b) >> 32), 1u, ks);
+      w[0] = r.x;
+      w[1] = r.y;
+      w[2] = r.z;
+      w[3] = r.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t j = 4 * g + k;
+      if (j >= N) break;
+      int32_t am = argmax[base + j];
+      if (!frozen) {
+        const int32_t noise = static_cast<int32_t>((static_cast<uint64_t>(w[k]) * V) >> 32);
+        canvas[base + j] = accepted[base + j] ? sample[base + j] : noise;
+        am = step_argmax[base + j];
+        argmax[base + j] = am;
+      }
+      diff |= am != prev[base + j] ? 1 : 0;
+      prev[base + j] = am;
+      sum += fixed_q(entropy[base + j]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = sum;
+  const int any_diff = __syncthreads_or(diff);
+  if (threadIdx.x == 0) {
+    long long total = 0;
+    for (int wi = 0; wi < kStopThreads / 32; ++wi) total += part[wi];
+    const int32_t c = count[b];
+    const int32_t nc = (c >= 0 && !any_diff) ? c + 1 : 0;
+    count[b] = nc;
+    const bool confident = total < static_cast<long long>(N) * fixed_q(threshold);
+    if (nc >= stability && confident) done[b] = 1;
+  }
+}
+
 const void* uniform_canvas_kernel_ptr() { return reinterpret_cast<const void*>(&uniform_canvas_kernel); }
+const void* uniform_update_kernel_ptr() { return reinterpret_cast<const void*>(&uniform_update_kernel); }
 const void* renoise_kernel_ptr() { return reinterpret_cast<const void*>(&renoise_kernel); }
 const void* stop_kernel_ptr() { return reinterpret_cast<const void*>(&stop_kernel); }
 

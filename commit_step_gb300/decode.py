@@ -20,7 +20,7 @@ import numpy as np
 import torch
 
 from . import (RULE_ENTROPY_BOUND, RULE_THRESHOLD, StableConfidentStopping, block_ranges, commit_step,
-               linear_temperature, renoise, uniform_canvas)
+               linear_temperature, uniform_canvas, uniform_update)
 
 _GATE_CYCLES = 1_000_000   # about 0.5 ms of SM clock: well beyond what the host needs to enqueue a step
 
@@ -103,8 +103,8 @@ def decode_uniform(model, *, batch: int, canvas_len: int, vocab_size: int, key: 
     Gumbel-max sample at temperature 1) and accepts the lowest-entropy
     positions under the entropy bound over every position; then the rest is
     re-noised, the rows that already stopped stay frozen, and the stopping
-    criterion updates the rows' done flags (one 1-byte-per-row host read per
-    step decides the loop's end).  ``model(step_index, canvas)`` returns the
+    criterion updates the rows' done flags -- all of that a second launch
+    (one 1-byte-per-row host read per step decides the loop's end).  ``model(step_index, canvas)`` returns the
     (B * N, V) logits on the device.  Returns (argmax canvas (B, N), steps).
     """
     B, N, V = batch, canvas_len, vocab_size
@@ -112,7 +112,6 @@ def decode_uniform(model, *, batch: int, canvas_len: int, vocab_size: int, key: 
     canvas = uniform_canvas(B, N, V, key, device=dev)
     argmax = canvas.clone()
     am_new = torch.empty_like(canvas)
-    noise = torch.empty_like(canvas)
     sample = torch.empty_like(canvas)
     prob = torch.empty((B, N), dtype=torch.float32, device=dev)
     ent = torch.empty_like(prob)
@@ -135,10 +134,8 @@ def decode_uniform(model, *, batch: int, canvas_len: int, vocab_size: int, key: 
         commit_step(logits, rule=RULE_ENTROPY_BOUND, gamma=entropy_bound, temperature=1.0, key=k_sample,
                     suppress_ids=suppress_ids, cand=everywhere, logit_scale=scale, argmax=am_new,
                     out=(sample, prob, ent, accepted, None))
-        uniform_canvas(B, N, V, k_noise, out=noise)
-        renoise(sample, accepted, noise, out=canvas, frozen=done)
-        renoise(am_new, None, None, out=argmax, frozen=done)
-        stop(argmax, ent, done=done)
+        # noise, re-noising, the frozen rows' argmax and the stopping update, one launch
+        uniform_update(sample, accepted, am_new, ent, V, k_noise, stop, canvas, argmax, done)
         if step_times is not None:
             e1.record()
         done_host.copy_(done)                  # the one host read of the step

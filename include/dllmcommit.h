@@ -283,6 +283,21 @@ dllm_status dllm_stable_confident_stop(const int32_t* argmax, const float* entro
                                        int32_t stability_threshold, float confidence_threshold, int32_t* prev,
                                        int32_t* count, uint8_t* stop, uint8_t* done, dllm_stream_t stream);
 
+/* The rest of one uniform-noise step after the statistics, in one launch,
+ * with the same results as these calls in this order (done as the frozen
+ * rows of both renoise calls):
+ *   dllm_uniform_canvas(B, N, V, noise_key, noise, N);
+ *   dllm_renoise(sample, accepted, noise, done, B, N, canvas);
+ *   dllm_renoise(step_argmax, NULL, NULL, done, B, N, argmax);
+ *   dllm_stable_confident_stop(argmax, entropy, B, N, stability_threshold,
+ *                              confidence_threshold, prev, count, NULL, done);
+ * All arrays device, (B, N) row-major (count and done (B)).  N <= 2^16. */
+dllm_status dllm_uniform_update(const int32_t* sample, const uint8_t* accepted, const int32_t* step_argmax,
+                                const float* entropy, int64_t B, int64_t N, int64_t V, uint64_t noise_key,
+                                int32_t stability_threshold, float confidence_threshold, int32_t* canvas,
+                                int32_t* argmax, int32_t* prev, int32_t* count, uint8_t* done,
+                                dllm_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * block_causal_mask ([ARS] "What mlx-arsenal ships": the mask block-diffusion
  * models are trained with -- bidirectional inside a block, causal across

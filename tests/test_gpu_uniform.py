@@ -68,7 +68,8 @@ def test_stopping_criterion_sequence_matches(cs, L):
         canvas[change, rng.integers(0, L)] += 1
         ent = np.where(rng.random((B, 1)) < 0.5, 1e-4, 0.05) * rng.random((B, L)) * 2
         ent = ent.astype(np.float32)
-        ent[0, :] = thr                                     # a mean at the threshold: decided alike on both sides
+        ent[0, :] = thr                                     # a mean exactly at the threshold: not confident
+        ent[1, 0] = np.nan                                  # NaN counts as 64
         want = ref(canvas, ent)
         got = gpu(torch.from_numpy(canvas).cuda(), torch.from_numpy(ent).cuda(), done=done)
         done_ref |= want
@@ -95,3 +96,37 @@ def test_uniform_loop_matches_oracle_loop(cs, dtype, B, N, V, onset):
     assert [t[1] for t in trace] == [t[2] for t in trace_ref]
     assert np.array_equal(got.cpu().numpy(), want)
     assert np.array_equal(want, gen.targets)
+
+
+def test_fused_update_equals_the_four_calls(cs):
+    """dllm_uniform_update gives what uniform_canvas, renoise (twice, done
+    rows frozen) and the stopping criterion give in that order."""
+    rng = np.random.default_rng(9)
+    B, N, V = 5, 700, 262144
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    sample = d(rng.integers(0, V, (B, N)).astype(np.int32))
+    accepted = d((rng.random((B, N)) < 0.3).astype(np.uint8))
+    step_am = d(rng.integers(0, V, (B, N)).astype(np.int32))
+    canvas0 = rng.integers(0, V, (B, N)).astype(np.int32)
+    argmax0 = rng.integers(0, V, (B, N)).astype(np.int32)
+    step_np = step_am.cpu().numpy()
+    argmax0[1] = step_np[1]                                    # row 1 will be stable
+    done0 = np.array([0, 0, 1, 0, 1], np.uint8)
+    for call in range(3):
+        ent = d(np.where(rng.random((B, 1)) < 0.5, 1e-4, 0.05).astype(np.float32) * np.ones((B, N), np.float32))
+        # the composition
+        ref_stop = cs.StableConfidentStopping(B, N, 1, 0.005)
+        c_ref, a_ref, done_ref = d(canvas0.copy()), d(argmax0.copy()), d(done0.copy())
+        ref_stop.prev.copy_(d(argmax0)); ref_stop.count.fill_(call - 1)
+        noise = cs.uniform_canvas(B, N, V, 1234 + call)
+        cs.renoise(sample, accepted, noise, out=c_ref, frozen=done_ref)
+        cs.renoise(step_am, None, None, out=a_ref, frozen=done_ref)
+        ref_stop(a_ref, ent, done=done_ref)
+        # one launch
+        stop = cs.StableConfidentStopping(B, N, 1, 0.005)
+        c, a, done = d(canvas0.copy()), d(argmax0.copy()), d(done0.copy())
+        stop.prev.copy_(d(argmax0)); stop.count.fill_(call - 1)
+        cs.uniform_update(sample, accepted, step_am, ent, V, 1234 + call, stop, c, a, done)
+        torch.cuda.synchronize()
+        for x, y in ((c, c_ref), (a, a_ref), (done, done_ref), (stop.prev, ref_stop.prev), (stop.count, ref_stop.count)):
+            assert torch.equal(x, y), call

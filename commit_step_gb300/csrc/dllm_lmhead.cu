@@ -40,10 +40,14 @@ constexpr int kLhBK = 64;                        // K per stage: one 128-byte sw
 constexpr int kLhUK = 16;                        // K of one tcgen05.mma.kind::f16
 constexpr int kLhMaxStages = 16;
 constexpr int kLhATile = kLhBM * kLhBK * 2;      // 16 KB: a full 128-row hidden tile
-constexpr int kLhEpiWarps = 4;                   // one warpgroup: warp w reads TMEM lanes 32 w .. 32 w + 31
-constexpr int kLhTmaWarp = kLhEpiWarps;
-constexpr int kLhMmaWarp = kLhEpiWarps + 1;
-constexpr int kLhThreads = (kLhEpiWarps + 2) * 32;
+constexpr int kLhEpiGroups = 2;                  // epilogue warpgroups: group g reads the chunks c = g (mod 2)
+constexpr int kLhEpiWarps = 4 * kLhEpiGroups;    // warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31
+// Warp w issues on scheduler w % 4; the warps of the tile's first 32 tokens
+// (0 and 4) are the busiest when there are few tokens, so the TMA and MMA
+// warps sit on schedulers 2 and 3 (warps 8 and 9 have no role).
+constexpr int kLhTmaWarp = kLhEpiWarps + 2;
+constexpr int kLhMmaWarp = kLhEpiWarps + 3;
+constexpr int kLhThreads = (kLhEpiWarps + 4) * 32;
 constexpr int kLhTmemCols = 2 * kLhMaxBN;        // two accumulators, at columns 0 and 256
 // Dynamic shared memory: the ring, plus 1 KB to align it, plus slack for the
 // MMA's reads of a hidden tile's unused rows past the last stage (a full
@@ -79,7 +83,7 @@ struct LmHeadParams {
   PhiloxSchedule keys;
   int32_t n_sup;
   int32_t sup[DLLM_MAX_SUPPRESS];
-  Partial* partials;       // (n_t * 128, P): token-major
+  Partial* partials;       // (n_t * 128, kLhEpiGroups P): token-major, one per CTA and epilogue group
   float* logits;           // (T, V) fp32 or nullptr
   int64_t logits_stride;
   int32_t* fault;
@@ -169,6 +173,8 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
   __shared__ __align__(8) uint64_t full_bar[kLhMaxStages], empty_bar[kLhMaxStages], accf_bar[2], acce_bar[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int32_t abort_flag_s;
+  __shared__ int32_t sup_s[DLLM_MAX_SUPPRESS];  // the suppressed ids (parameter-space reads with a
+                                                // run-time index are slow)
   volatile int32_t* abort_flag = &abort_flag_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ring = (smem_addr(lh_smem) + 1023u) & ~1023u;
@@ -189,6 +195,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
     abort_flag_s = 0;
     fence_mbar_init();
   }
+  for (int q = threadIdx.x; q < p.n_sup; q += blockDim.x) sup_s[q] = p.sup[q];
   if (warp == kLhMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_slot)),
                  "r"(kLhTmemCols)
@@ -199,32 +206,49 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
   __syncthreads();
   lh_fence_after();
   const uint32_t tmem = tmem_slot;
-  pdl_wait();
+  if (warp != kLhTmaWarp) pdl_wait();  // (the TMA warp waits once it has requested the first weight slabs)
   pdl_launch_dependents();
 
   if (warp == kLhTmaWarp) {
     if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
-      for (int i = 0; i < n_my && !*abort_flag; ++i) {
+      // Stage q holds K slabs (q mod per_tile) p.slabs .. of this CTA's tile q / per_tile.
+      const int per_tile = p.n_k / p.slabs;
+      const int total = n_my * per_tile;
+      const int pre = total < p.stages ? total : p.stages;
+      const uint32_t stage_bytes = static_cast<uint32_t>(p.slabs * (p.a_bytes + p.b_bytes));
+      const uint32_t tx = static_cast<uint32_t>(p.slabs * (p.a_rows * kLhBK * 2 + p.b_bytes));
+      auto load = [&](int q, int s, bool hidden, bool weight) {
+        const int i = q / per_tile, k = (q % per_tile) * p.slabs;
         const int tt = i / nvt, vt = vt0 + i % nvt;
-        for (int k = 0; k < p.n_k; k += p.slabs) {
-          if (!lh_wait(smem_addr(&empty_bar[s]), ph ^ 1u, abort_flag)) {
-            lh_fail(p, abort_flag, kFaultEmptyWait);
-            break;
-          }
-          const uint32_t bar = smem_addr(&full_bar[s]);
-          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.slabs * (p.a_rows * kLhBK * 2 + p.b_bytes)));
-          const uint32_t stage = ring + static_cast<uint32_t>(s * p.slabs * (p.a_bytes + p.b_bytes));
-          for (int j = 0; j < p.slabs; ++j) {
-            const uint32_t sub = stage + static_cast<uint32_t>(j * (p.a_bytes + p.b_bytes));
-            lh_tma_load(sub, &p.tm_h, (k + j) * kLhBK, tt * kLhBM, bar);
-            lh_tma_load(sub + static_cast<uint32_t>(p.a_bytes), &p.tm_w, (k + j) * kLhBK, vt * p.bn, bar);
-          }
-          if (++s == p.stages) {
-            s = 0;
-            ph ^= 1u;
-          }
+        const uint32_t bar = smem_addr(&full_bar[s]);
+        for (int j = 0; j < p.slabs; ++j) {
+          const uint32_t sub = ring + static_cast<uint32_t>(s) * stage_bytes + static_cast<uint32_t>(j * (p.a_bytes + p.b_bytes));
+          if (hidden) lh_tma_load(sub, &p.tm_h, (k + j) * kLhBK, tt * kLhBM, bar);
+          if (weight) lh_tma_load(sub + static_cast<uint32_t>(p.a_bytes), &p.tm_w, (k + j) * kLhBK, vt * p.bn, bar);
+        }
+      };
+      // The weight is not written by the preceding kernel in the stream, so
+      // the first stages' weight slabs are requested before the grid
+      // dependency resolves (the ring fills while the previous call
+      // finishes); their hidden slabs only after it.
+      for (int q = 0; q < pre; ++q) {
+        mbar_arrive_expect_tx(smem_addr(&full_bar[q]), tx);
+        load(q, q, false, true);
+      }
+      pdl_wait();
+      for (int q = 0; q < pre; ++q) load(q, q, true, false);
+      int s = pre == p.stages ? 0 : pre;
+      uint32_t ph = pre == p.stages ? 1u : 0u;
+      for (int q = pre; q < total && !*abort_flag; ++q) {
+        if (!lh_wait(smem_addr(&empty_bar[s]), ph ^ 1u, abort_flag)) {
+          lh_fail(p, abort_flag, kFaultEmptyWait);
+          break;
+        }
+        mbar_arrive_expect_tx(smem_addr(&full_bar[s]), tx);
+        load(q, s, true, true);
+        if (++s == p.stages) {
+          s = 0;
+          ph ^= 1u;
         }
       }
     }
@@ -263,9 +287,12 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
         lh_commit(smem_addr(&accf_bar[buf]));  // the accumulator is complete
       }
     }
-  } else {
-    // Epilogue: thread (warp, lane) owns token row 32 warp + lane of the tile.
+  } else if (warp < kLhEpiWarps) {
+    // Epilogue: thread (warp, lane) owns token row 32 (warp % 4) + lane of the
+    // tile, and the tile's 32-column chunks c = warp / 4 (mod kLhEpiGroups).
+    const int ew = warp & 3, half = warp >> 2;
     const float t = p.temperature;
+    const float t_ln2 = t * kLn2;
     LhAcc acc;
     for (int i = 0; i < n_my; ++i) {
       const int tt = i / nvt, vt = vt0 + i % nvt;
@@ -287,54 +314,75 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
         break;
       }
       lh_fence_after();
-      const int64_t token = static_cast<int64_t>(tt) * kLhBM + warp * 32 + lane;
+      const int64_t token = static_cast<int64_t>(tt) * kLhBM + ew * 32 + lane;
       const uint64_t row_lo_hi = static_cast<uint64_t>(token);
+      // A warp whose 32 TMEM lanes hold no token (a tile of fewer than 128
+      // tokens) only hands the accumulator back; chunks past V are skipped.
+      const int64_t ids = std::min<int64_t>(p.bn, p.V - static_cast<int64_t>(vt) * p.bn);
+      const int n_chunks = token - lane < p.T ? static_cast<int>((ids + 31) / 32) : 0;
 #pragma unroll 1
-      for (int c = 0; c * 32 < p.bn; ++c) {
+      for (int c = half; c < n_chunks; c += kLhEpiGroups) {
         uint32_t r[32];
         // (the last chunk of a tile may reach past bn: those columns are in
         // the 256-column slot but hold no id of this tile, and are masked)
-        lh_tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(buf * kLhMaxBN + c * 32), r);
+        lh_tmem_ld32(tmem + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(buf * kLhMaxBN + c * 32), r);
         const int64_t v0 = static_cast<int64_t>(vt) * p.bn + c * 32;
         const int64_t vend = std::min<int64_t>(p.V, static_cast<int64_t>(vt + 1) * p.bn);
+        const int lim = static_cast<int>(std::min<int64_t>(32, vend - v0));  // columns holding ids (1 .. 32)
         if (p.logits && token < p.T) {
           float* out = p.logits + token * p.logits_stride + v0;
-          for (int j = 0; j < 32 && v0 + j < vend; ++j) out[j] = __uint_as_float(r[j]);
-        }
-        bool any_sup = false;
-        for (int q = 0; q < p.n_sup; ++q) any_sup |= p.sup[q] >= v0 && p.sup[q] < v0 + 32;
-        float z[32];
-        float cmax = kMInit;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float x = fminf(fmaxf(__uint_as_float(r[j]), kSentinel), kTopClamp);  // NaN -> -2^100
-          if (v0 + j >= vend) x = kAbsent;
-          if (any_sup)
-            for (int q = 0; q < p.n_sup; ++q)
-              if (p.sup[q] == v0 + j) x = kAbsent;
-          z[j] = x;
-          cmax = fmaxf(cmax, x);
+          for (int j = 0; j < 32; ++j)
+            if (j < lim) out[j] = __uint_as_float(r[j]);
         }
+        // Columns with no id (past the tile or V) or a suppressed id, as bits.
+        uint32_t absent = lim >= 32 ? 0u : ~((1u << lim) - 1u);
+        for (int q = 0; q < p.n_sup; ++q) {
+          const int64_t off = sup_s[q] - v0;
+          if (off >= 0 && off < 32) absent |= 1u << off;
+        }
+        // Every index below is a compile-time constant, so z stays in registers.
+        float z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = fminf(fmaxf(__uint_as_float(r[j]), kSentinel), kTopClamp);  // NaN -> -2^100
+        if (absent != 0u) {  // warp-uniform and rare: a tile's last chunk, or a suppressed id
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if ((absent >> j) & 1u) z[j] = kAbsent;
+        }
+        float cm[4] = {kMInit, kMInit, kMInit, kMInit};
+#pragma unroll
+        for (int j = 0; j < 32; ++j) cm[j & 3] = fmaxf(cm[j & 3], z[j]);
+        const float cmax = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
         if (cmax > acc.m) {  // rescale to the new running max
           const float d = (acc.m - cmax) * kLog2e;
           const float f = ex2_approx(d);
           acc.S2 = f * fmaf(d, acc.Z, acc.S2);
           acc.Z *= f;
           acc.m = cmax;
-          int first = 0;
-          for (int j = 31; j >= 0; --j)
-            if (z[j] == cmax) first = j;
-          acc.idx = static_cast<int32_t>(v0 + first);  // strictly larger than every earlier value
-        }
+          uint32_t eq = 0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float y = (z[j] - acc.m) * kLog2e;
-          const float e = ex2_approx(y);
-          acc.Z += e;
-          acc.S2 = fmaf(e, y, acc.S2);
+          for (int j = 0; j < 32; ++j) eq |= (z[j] == cmax ? 1u : 0u) << j;
+          acc.idx = static_cast<int32_t>(v0 + (__ffs(eq) - 1));  // strictly larger than every earlier value
+        }
+        // The chunk's sums in packed pairs on two independent chains, then
+        // added to the row's: y = (z - m) log2 e, sum 2^y, sum 2^y y.
+        {
+          const uint64_t negm2 = pack2(-acc.m, -acc.m), cs2 = pack2(kLog2e, kLog2e);
+          uint64_t Za = 0, Sa = 0, Zb = 0, Sb = 0;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            acc_pair2(Za, Sa, z[j], z[j + 1], negm2, cs2);
+            acc_pair2(Zb, Sb, z[j + 2], z[j + 3], negm2, cs2);
+          }
+          float z0, z1, s0, s1;
+          unpack2(add2(Za, Zb), z0, z1);
+          unpack2(add2(Sa, Sb), s0, s1);
+          acc.Z += z0 + z1;
+          acc.S2 += s0 + s1;
         }
         if (GUMBEL) {
-#pragma unroll 1
+#pragma unroll
           for (int g = 0; g < 8; ++g) {
             const uint4 o = philox4x32_10(static_cast<uint32_t>((v0 >> 2) + g), static_cast<uint32_t>(row_lo_hi),
                                           static_cast<uint32_t>(row_lo_hi >> 32), 0u, p.keys);
@@ -342,7 +390,12 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = 4 * g + e;
-              if (z[j] <= kAbsent) continue;
+              // g = -ln(-ln u) <= -ln(1 - u): the exact score is evaluated only
+              // where this bound (with a margin for the rounding of lg2.approx
+              // and the fmaf) reaches the best score so far.
+              const float w1 = __fsub_rn(1.0f, uniform_from_bits(w4[e]));
+              const float bound = fmaf(t_ln2, -lg2_approx(w1), z[j] + fmaf(fabsf(z[j]), 1e-6f, 1e-3f));
+              if (z[j] <= kAbsent || bound < acc.best_s) continue;
               const float sc = gumbel_score(z[j], t, w4[e]);
               if (sc > acc.best_s) {
                 acc.best_s = sc;
@@ -356,7 +409,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
       lh_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&acce_bar[buf]));
-      if (vt == vt1 - 1) {
+      if (vt == vt1 - 1 && token < p.T) {
         Partial q;
         q.m = acc.m;
         q.Z = acc.Z;
@@ -366,7 +419,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
         q.best_z = acc.best_z;
         q.best_v = acc.best_v;
         q.m2 = kMInit;
-        store_partial(p.partials + token * p.P + blockIdx.x, q);
+        store_partial(p.partials + token * (kLhEpiGroups * p.P) + kLhEpiGroups * blockIdx.x + half, q);
       }
     }
   }
@@ -497,7 +550,7 @@ size_t dllm_lm_head_stats_workspace_size(int64_t T, int64_t V, int64_t d) {
   const int64_t sms = dev ? dev->sms : 1024;
   const int64_t P = std::min<int64_t>(sms, (V + 63) / 64);   // the most CTAs any tile width uses
   const int64_t n_t = (T + kLhBM - 1) / kLhBM;
-  return 256 + static_cast<size_t>(n_t * kLhBM * P) * sizeof(Partial);
+  return 256 + static_cast<size_t>(n_t * kLhBM * P * kLhEpiGroups) * sizeof(Partial);
 }
 
 dllm_status dllm_lm_head_stats(const void* hidden, int64_t T, int64_t d, int64_t hidden_stride, const void* weight,
@@ -531,7 +584,7 @@ dllm_status dllm_lm_head_stats(const void* hidden, int64_t T, int64_t d, int64_t
   const int32_t bn = lh_tile_width(dev->sms, V);
   const int64_t P = std::min<int64_t>(dev->sms, (V + bn - 1) / bn);
   const int64_t n_t = (T + kLhBM - 1) / kLhBM;
-  const size_t need = 256 + static_cast<size_t>(n_t * kLhBM * P) * sizeof(Partial);
+  const size_t need = 256 + static_cast<size_t>(n_t * kLhBM * P * kLhEpiGroups) * sizeof(Partial);
   if (!workspace || workspace_bytes < need) return DLLM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return DLLM_ERR_INVALID_ARGUMENT;
 
@@ -594,7 +647,7 @@ dllm_status dllm_lm_head_stats(const void* hidden, int64_t T, int64_t d, int64_t
   sp.prob = prob;
   sp.entropy = entropy;
   sp.fault = p.fault;
-  int32_t P32 = p.P;
+  int32_t P32 = p.P * kLhEpiGroups;  // partials per token
   const Partial* parts = p.partials;
   void* fargs[] = {&sp, &P32, &parts};
   return lh_launch(gumbel ? reinterpret_cast<const void*>(&lm_head_finish_kernel<true>)

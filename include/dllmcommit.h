@@ -336,6 +336,12 @@ dllm_status dllm_block_causal_mask(int64_t Lq, int64_t Lk, int64_t q_offset, int
  * workspace >= dllm_lm_head_stats_workspace_size(T, V, d) bytes (any
  *         contents; it holds per-CTA partials).  Other arguments as in
  *         dllm_token_stats.
+ * Ordering: the call is launched as a programmatic dependent of the kernel
+ * before it in the stream.  The hidden states (and every output) are touched
+ * only after that kernel has completed; the first slabs of the weight are
+ * read before, so the weight must not be written by the kernel launched just
+ * before this call on the same stream (write it earlier, or on another stream
+ * with an event).
  * ------------------------------------------------------------------------ */
 size_t dllm_lm_head_stats_workspace_size(int64_t T, int64_t V, int64_t d);
 

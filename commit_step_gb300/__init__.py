@@ -35,7 +35,7 @@ EXPORTS = (
     "dllm_edit_transfer", "dllm_transfer_schedule", "dllm_block_ranges", "dllm_commit_step",
     "dllm_workspace_fault", "dllm_token_stats_noalloc", "dllm_token_stats_ex", "dllm_linear_temperature",
     "dllm_uniform_canvas", "dllm_renoise", "dllm_stable_confident_stop", "dllm_block_causal_mask",
-    "dllm_lm_head_stats_workspace_size", "dllm_lm_head_stats", "dllm_uniform_update",
+    "dllm_lm_head_stats_workspace_size", "dllm_lm_head_stats", "dllm_uniform_update", "dllm_commit_step_host",
 )
 
 
@@ -76,6 +76,8 @@ def _load() -> C.CDLL:
     stats_args = [P, C.c_int, i64, i64, i64, i64, f32, u64, P, i32, P, P, P]
     lib.dllm_token_stats.argtypes = stats_args + [P, sz, P]
     lib.dllm_commit_step.argtypes = stats_args + [C.POINTER(CommitParams), P, sz, P]
+    lib.dllm_commit_step_host.argtypes = [P, P, C.c_int, i64, i64, i64, f32, u64, P, i32, C.POINTER(CommitParams),
+                                          P, P, P, sz, P]
     tail = [P, P, i64, i64, P]
     lib.dllm_threshold_transfer.argtypes = [P, P, i64, i64, f32, C.c_int, P] + tail
     lib.dllm_topk_transfer.argtypes = [P, P, i64, i64, P, P] + tail
@@ -136,8 +138,8 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def _need_cuda(*ts):
-    for t in ts:
-        if t is not None and not t.is_cuda:
+    for t in ts:  # (non-tensors, e.g. an integer k, are converted by the caller)
+        if torch.is_tensor(t) and not t.is_cuda:
             raise ValueError("device tensors are required")
 
 
@@ -338,6 +340,28 @@ def block_ranges(P: int, gen_len: int, block_len: int, align: bool = False):
     return [(buf[2 * i], buf[2 * i + 1]) for i in range(n.value)]
 
 
+def _commit_params(rule, strict, tau, factor, gamma, k, cand, mask_id, edit, tau_edit, commit, edit_mask, canvas,
+                   canvas_offset, counts, inputs_ready, ex) -> CommitParams:
+    """The dllm_commit_params of a call (device tensors or None)."""
+    p = CommitParams()
+    p.rule, p.strict, p.tau, p.factor, p.gamma = int(rule), int(bool(strict)), float(tau), float(factor), float(gamma)
+    p.k = None if k is None else k.data_ptr()
+    p.cand = None if cand is None else cand.data_ptr()
+    p.mask_id = int(mask_id)
+    p.edit, p.tau_edit = int(bool(edit)), float(tau_edit)
+    p.commit = None if commit is None else commit.data_ptr()
+    p.edit_mask = None if edit_mask is None else edit_mask.data_ptr()
+    if canvas is not None:
+        if canvas.dim() != 2 or canvas.stride(1) != 1 or canvas.dtype != torch.int32:
+            raise ValueError("canvas must be a (B, N) int32 tensor with unit column stride")
+        p.canvas, p.canvas_stride, p.canvas_offset = canvas.data_ptr(), canvas.stride(0), int(canvas_offset)
+    p.counts = None if counts is None else counts.data_ptr()
+    p.flags = FLAG_INPUTS_READY if inputs_ready else 0
+    if ex is not None:
+        p.ex = C.pointer(ex)
+    return p
+
+
 def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, suppress_ids: Sequence[int] = (),
                 cand=None, mask_id: int = -1, tau: float = 0.0, strict: bool = False, k=None, factor: float = 0.0,
                 gamma: float = 0.0, edit: bool = False, tau_edit: float = 1.0, canvas=None, canvas_offset: int = 0,
@@ -371,23 +395,9 @@ def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, su
         x0, prob, ent, commit, edit_mask = out
     if rule == RULE_TOPK and not torch.is_tensor(k):
         k = torch.full((B,), int(k), dtype=torch.int32, device=dev)
-    p = CommitParams()
-    p.rule, p.strict, p.tau, p.factor, p.gamma = int(rule), int(bool(strict)), float(tau), float(factor), float(gamma)
-    p.k = None if k is None else k.data_ptr()
-    p.cand = None if cand is None else cand.data_ptr()
-    p.mask_id = int(mask_id)
-    p.edit, p.tau_edit = int(bool(edit)), float(tau_edit)
-    p.commit = None if commit is None else commit.data_ptr()
-    p.edit_mask = None if edit_mask is None else edit_mask.data_ptr()
-    if canvas is not None:
-        if canvas.dim() != 2 or canvas.stride(1) != 1 or canvas.dtype != torch.int32:
-            raise ValueError("canvas must be a (B, N) int32 tensor with unit column stride")
-        p.canvas, p.canvas_stride, p.canvas_offset = canvas.data_ptr(), canvas.stride(0), int(canvas_offset)
-    p.counts = None if counts is None else counts.data_ptr()
-    p.flags = FLAG_INPUTS_READY if inputs_ready else 0
     ex, _, _ = _stats_ex((B, L), dev, logit_scale, margin, argmax)
-    if ex is not None:
-        p.ex = C.pointer(ex)
+    p = _commit_params(rule, strict, tau, factor, gamma, k, cand, mask_id, edit, tau_edit, commit, edit_mask, canvas,
+                       canvas_offset, counts, inputs_ready, ex)
     sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
     if ws is None:
         ws = workspace(B, L, V, dt, dev, stream)
@@ -395,6 +405,71 @@ def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, su
                                  sup, len(suppress_ids), _ptr(x0), _ptr(prob), _ptr(ent), C.byref(p), _ptr(ws),
                                  ws.numel(), _stream(stream)), "dllm_commit_step")
     return x0, prob, ent, commit, edit_mask
+
+
+class HostStep:
+    """A commit step on logits held in host memory, prepared once and queued
+    with one C call (dllm_commit_step_host) each time it is called: the copy
+    of the logits to the device, the fused statistics pass + commit rule, and
+    one copy of x0 / prob / entropy / commit back to host memory, in order on
+    one stream (fixed at construction).
+
+    ``host_logits``: a contiguous CPU tensor (B, L, V) or (T, V), bf16 or
+    fp32; pin it for the copies to run asynchronously.  Its contents are read
+    when the stream reaches the step, so a caller may refill it between
+    steps once the previous step has finished.  After the stream reaches the
+    step, ``x0``, ``prob``, ``entropy`` and ``commit`` (views of one pinned
+    host buffer) hold the results.  ``cand``, ``k``, ``canvas``, ``counts``,
+    ``margin`` and ``argmax`` are device tensors as in commit_step; an edit
+    mask, when ``edit`` is set, is written to the device tensor ``edit_mask``.
+    """
+
+    def __init__(self, host_logits: torch.Tensor, *, rule: int, temperature: float = 0.0, key: int = 0,
+                 suppress_ids: Sequence[int] = (), cand=None, mask_id: int = -1, tau: float = 0.0,
+                 strict: bool = False, k=None, factor: float = 0.0, gamma: float = 0.0, edit: bool = False,
+                 edit_mask=None, tau_edit: float = 1.0, canvas=None, canvas_offset: int = 0, counts=None,
+                 device=None, ws=None, stream=None, logit_scale: float = 1.0, margin=None, argmax=None):
+        if host_logits.is_cuda or not host_logits.is_contiguous():
+            raise ValueError("host_logits must be a contiguous CPU tensor")
+        B, L, V, _ = _logits_view(host_logits)
+        dt = _dtype_code(host_logits)
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        _need_cuda(cand, canvas, k, counts, edit_mask)
+        T = B * L
+        self.dev_logits = torch.empty(host_logits.shape, dtype=host_logits.dtype, device=dev)
+        self.dev_out = torch.empty(max(1, 13 * T), dtype=torch.uint8, device=dev)
+        self.host_out = torch.empty(max(1, 13 * T), dtype=torch.uint8).pin_memory()
+        self.x0 = self.host_out[0:4 * T].view(torch.int32).view(B, L)
+        self.prob = self.host_out[4 * T:8 * T].view(torch.float32).view(B, L)
+        self.entropy = self.host_out[8 * T:12 * T].view(torch.float32).view(B, L)
+        self.commit = self.host_out[12 * T:13 * T].view(B, L) if rule != RULE_NONE else None
+        if rule == RULE_TOPK and not torch.is_tensor(k):
+            k = torch.full((B,), int(k), dtype=torch.int32, device=dev)
+        if edit and edit_mask is None:
+            edit_mask = torch.empty((B, L), dtype=torch.uint8, device=dev)
+        self.edit_mask = edit_mask if edit else None
+        ex, _, _ = _stats_ex((B, L), dev, logit_scale, margin, argmax)
+        self._ex = ex
+        self._p = _commit_params(rule, strict, tau, factor, gamma, k, cand, mask_id, edit, tau_edit, None,
+                                 self.edit_mask, canvas, canvas_offset, counts, False, ex)
+        self._sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
+        if ws is None:
+            ws = workspace(B, L, V, dt, dev, stream)
+        self._keep = (host_logits, cand, k, canvas, counts, margin, argmax, ws)
+        self._args = (C.c_void_p(host_logits.data_ptr()), _ptr(self.dev_logits), dt, B, L, V, float(temperature),
+                      int(key) & (2**64 - 1), self._sup, len(suppress_ids), C.byref(self._p), _ptr(self.dev_out),
+                      C.c_void_p(self.host_out.data_ptr()), _ptr(ws), ws.numel(), _stream(stream))
+
+    def __call__(self):
+        _check(_lib.dllm_commit_step_host(*self._args), "dllm_commit_step_host")
+        return self.x0, self.prob, self.entropy, self.commit
+
+
+def commit_step_host(host_logits: torch.Tensor, **kw):
+    """One commit step on host-resident logits (see HostStep); returns host
+    tensors (x0, prob, entropy, commit), valid once the stream reaches the
+    step."""
+    return HostStep(host_logits, **kw)()
 
 
 def token_stats_noalloc(logits: torch.Tensor, temperature: float = 0.0, key: int = 0,

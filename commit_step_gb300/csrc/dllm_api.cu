@@ -399,6 +399,64 @@ void* noalloc_scratch(cudaError_t* err) {
   return g_noalloc[dev].ptr;
 }
 
+// The checks of dllm_commit_step, and the rule arguments and options they
+// resolve (shared by the device- and host-buffer entry points).
+struct CommitCall {
+  std::vector<int32_t> sup;
+  RuleArgs a{};
+  StatsOpts opt;
+  bool early = false;
+};
+
+dllm_status commit_check(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
+                         float temperature, const int32_t* suppress_ids, int32_t n_suppress, int32_t* x0, float* prob,
+                         float* entropy, const dllm_commit_params* cp, CommitCall& c) {
+  dllm_status st = check_stats(logits, dt, B, L, V, row_stride, temperature, suppress_ids, n_suppress, x0, prob,
+                               entropy, c.sup);
+  if (st != DLLM_OK) return st;
+  if (!cp) return DLLM_ERR_INVALID_ARGUMENT;
+  if (cp->rule < DLLM_RULE_NONE || cp->rule > DLLM_RULE_ENTROPY_BOUND) return DLLM_ERR_INVALID_ARGUMENT;
+  if (B * L == 0) return DLLM_OK;
+  if (B > INT32_MAX || L > 65535) return DLLM_ERR_UNSUPPORTED;  // per-batch-row counters are 16-bit
+  if (cp->rule != DLLM_RULE_NONE && !cp->commit) return DLLM_ERR_INVALID_ARGUMENT;
+  if (cp->rule == DLLM_RULE_TOPK && !cp->k) return DLLM_ERR_INVALID_ARGUMENT;
+  if (cp->edit && !cp->edit_mask) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!cp->cand && !cp->canvas) return DLLM_ERR_INVALID_ARGUMENT;
+  if (std::isnan(cp->tau) || std::isnan(cp->factor) || std::isnan(cp->gamma) || std::isnan(cp->tau_edit))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  const bool sorting = cp->rule == DLLM_RULE_TOPK || cp->rule == DLLM_RULE_FACTOR || cp->rule == DLLM_RULE_ENTROPY_BOUND;
+  if (sorting && L > kFusedSortCap) return DLLM_ERR_UNSUPPORTED;
+  if (cp->canvas) {
+    if (cp->canvas_offset < 0 || cp->canvas_stride < 0) return DLLM_ERR_INVALID_ARGUMENT;
+    if (B > 1 && cp->canvas_stride < cp->canvas_offset + L) return DLLM_ERR_INVALID_ARGUMENT;
+  }
+  RuleArgs& a = c.a;
+  a.rule = cp->rule;
+  a.strict = cp->strict ? 1 : 0;
+  a.tau = cp->tau;
+  a.factor = cp->factor;
+  a.gamma = cp->gamma;
+  a.k = cp->k;
+  a.conf = prob;
+  a.entropy = entropy;
+  a.cand = cp->cand;
+  a.mask_id = cp->mask_id;
+  a.edit = cp->edit ? 1 : 0;
+  a.tau_edit = cp->tau_edit;
+  a.x0 = x0;
+  a.commit = cp->commit;
+  a.edit_mask = cp->edit ? cp->edit_mask : nullptr;
+  a.canvas = cp->canvas;
+  a.canvas_stride = cp->canvas_stride;
+  a.canvas_offset = cp->canvas_offset;
+  a.counts = cp->counts;
+  a.L = L;
+  if (cp->flags & ~static_cast<int32_t>(DLLM_FLAG_INPUTS_READY)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (resolve_ex(cp->ex, c.opt) != DLLM_OK) return DLLM_ERR_INVALID_ARGUMENT;
+  c.early = (cp->flags & DLLM_FLAG_INPUTS_READY) != 0;
+  return DLLM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -628,53 +686,44 @@ dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64
                              float temperature, uint64_t key, const int32_t* suppress_ids, int32_t n_suppress,
                              int32_t* x0, float* prob, float* entropy, const dllm_commit_params* cp, void* workspace,
                              size_t workspace_bytes, dllm_stream_t stream) {
-  std::vector<int32_t> sup;
-  dllm_status st = check_stats(logits, dt, B, L, V, row_stride, temperature, suppress_ids, n_suppress, x0, prob,
-                               entropy, sup);
-  if (st != DLLM_OK) return st;
-  if (!cp) return DLLM_ERR_INVALID_ARGUMENT;
-  if (cp->rule < DLLM_RULE_NONE || cp->rule > DLLM_RULE_ENTROPY_BOUND) return DLLM_ERR_INVALID_ARGUMENT;
+  CommitCall c;
+  const dllm_status st = commit_check(logits, dt, B, L, V, row_stride, temperature, suppress_ids, n_suppress, x0, prob,
+                                      entropy, cp, c);
+  if (st != DLLM_OK || B * L == 0) return st;
+  return run_stats(logits, dt, B, L, V, row_stride, temperature, key, c.sup, x0, prob, entropy, &c.a, workspace,
+                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream), c.early, c.opt);
+}
+
+dllm_status dllm_commit_step_host(const void* host_logits, void* dev_logits, dllm_dtype dt, int64_t B, int64_t L,
+                                  int64_t V, float temperature, uint64_t key, const int32_t* suppress_ids,
+                                  int32_t n_suppress, const dllm_commit_params* cp, void* dev_out, void* host_out,
+                                  void* workspace, size_t workspace_bytes, dllm_stream_t stream) {
+  if (!cp || B < 0 || L < 0 || V < 1) return DLLM_ERR_INVALID_ARGUMENT;
   if (B * L == 0) return DLLM_OK;
-  if (B > INT32_MAX || L > 65535) return DLLM_ERR_UNSUPPORTED;  // per-batch-row counters are 16-bit
-  if (cp->rule != DLLM_RULE_NONE && !cp->commit) return DLLM_ERR_INVALID_ARGUMENT;
-  if (cp->rule == DLLM_RULE_TOPK && !cp->k) return DLLM_ERR_INVALID_ARGUMENT;
-  if (cp->edit && !cp->edit_mask) return DLLM_ERR_INVALID_ARGUMENT;
-  if (!cp->cand && !cp->canvas) return DLLM_ERR_INVALID_ARGUMENT;
-  if (std::isnan(cp->tau) || std::isnan(cp->factor) || std::isnan(cp->gamma) || std::isnan(cp->tau_edit))
-    return DLLM_ERR_INVALID_ARGUMENT;
-  const bool sorting = cp->rule == DLLM_RULE_TOPK || cp->rule == DLLM_RULE_FACTOR || cp->rule == DLLM_RULE_ENTROPY_BOUND;
-  if (sorting && L > kFusedSortCap) return DLLM_ERR_UNSUPPORTED;
-  if (cp->canvas) {
-    if (cp->canvas_offset < 0 || cp->canvas_stride < 0) return DLLM_ERR_INVALID_ARGUMENT;
-    if (B > 1 && cp->canvas_stride < cp->canvas_offset + L) return DLLM_ERR_INVALID_ARGUMENT;
-  }
-  RuleArgs a{};
-  a.rule = cp->rule;
-  a.strict = cp->strict ? 1 : 0;
-  a.tau = cp->tau;
-  a.factor = cp->factor;
-  a.gamma = cp->gamma;
-  a.k = cp->k;
-  a.conf = prob;
-  a.entropy = entropy;
-  a.cand = cp->cand;
-  a.mask_id = cp->mask_id;
-  a.edit = cp->edit ? 1 : 0;
-  a.tau_edit = cp->tau_edit;
-  a.x0 = x0;
-  a.commit = cp->commit;
-  a.edit_mask = cp->edit ? cp->edit_mask : nullptr;
-  a.canvas = cp->canvas;
-  a.canvas_stride = cp->canvas_stride;
-  a.canvas_offset = cp->canvas_offset;
-  a.counts = cp->counts;
-  a.L = L;
-  if (cp->flags & ~static_cast<int32_t>(DLLM_FLAG_INPUTS_READY)) return DLLM_ERR_INVALID_ARGUMENT;
-  StatsOpts opt;
-  if (resolve_ex(cp->ex, opt) != DLLM_OK) return DLLM_ERR_INVALID_ARGUMENT;
-  return run_stats(logits, dt, B, L, V, row_stride, temperature, key, sup, x0, prob, entropy, &a, workspace,
-                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream), (cp->flags & DLLM_FLAG_INPUTS_READY) != 0,
-                   opt);
+  if (!host_logits || !dev_logits || !dev_out || !host_out) return DLLM_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(dev_out) & 3u) != 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (dt != DLLM_F32 && dt != DLLM_BF16) return DLLM_ERR_INVALID_ARGUMENT;
+  const int64_t T = B * L;
+  if (T > INT64_MAX / V / esize_of(dt)) return DLLM_ERR_INVALID_ARGUMENT;
+  int32_t* x0 = static_cast<int32_t*>(dev_out);
+  float* prob = reinterpret_cast<float*>(x0 + T);
+  float* entropy = prob + T;
+  dllm_commit_params p = *cp;
+  if (p.rule != DLLM_RULE_NONE) p.commit = reinterpret_cast<uint8_t*>(entropy + T);
+  CommitCall c;
+  const dllm_status st = commit_check(dev_logits, dt, B, L, V, V, temperature, suppress_ids, n_suppress, x0, prob,
+                                      entropy, &p, c);
+  if (st != DLLM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dev_logits, host_logits, static_cast<size_t>(T * V * esize_of(dt)), cudaMemcpyHostToDevice,
+                      s) != cudaSuccess)
+    return DLLM_ERR_CUDA;
+  const dllm_status rs = run_stats(dev_logits, dt, B, L, V, V, temperature, key, c.sup, x0, prob, entropy, &c.a,
+                                   workspace, workspace_bytes, s, c.early, c.opt);
+  if (rs != DLLM_OK) return rs;
+  const size_t out_bytes = static_cast<size_t>(T) * (p.rule != DLLM_RULE_NONE ? 13 : 12);
+  return cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess ? DLLM_OK
+                                                                                                   : DLLM_ERR_CUDA;
 }
 
 dllm_status dllm_token_stats_noalloc(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,

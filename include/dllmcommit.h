@@ -404,6 +404,27 @@ dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64
                              const dllm_commit_params* params,
                              void* workspace, size_t workspace_bytes, dllm_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * dllm_commit_step on logits held in host memory, with its results returned
+ * to host memory: one call queues, on `stream`, the copy of the (B, L, V)
+ * logits (rows contiguous, row stride V) from host_logits into dev_logits,
+ * dllm_commit_step on them, and one copy of the per-position results back.
+ * Results, in dev_out and then host_out, back to back with T = B L:
+ *   x0 int32[T], prob fp32[T], entropy fp32[T], commit uint8[T]
+ * (12 T bytes, or 13 T when params->rule != DLLM_RULE_NONE: the commit mask
+ * is written to the packed buffer, params->commit is ignored).  The edit
+ * mask, the canvas and the counts (when requested) stay on the device.
+ * host_logits / host_out: host memory (pinned for the copies to run
+ * asynchronously), valid until the stream reaches the copies.
+ * dev_logits: device, B L V elements; dev_out: device, 4-byte aligned,
+ * >= 13 T bytes.  Other arguments and errors as in dllm_commit_step; the
+ * arguments are checked before anything is queued.
+ * ------------------------------------------------------------------------ */
+dllm_status dllm_commit_step_host(const void* host_logits, void* dev_logits, dllm_dtype dt, int64_t B, int64_t L,
+                                  int64_t V, float temperature, uint64_t key, const int32_t* suppress_ids,
+                                  int32_t n_suppress, const dllm_commit_params* params, void* dev_out,
+                                  void* host_out, void* workspace, size_t workspace_bytes, dllm_stream_t stream);
+
 /* Reads and clears the device fault word of a workspace (synchronises the
  * stream).  *fault = 0 when no kernel reported a fault; otherwise a code
  * naming the wait that gave up (the kernel stopped early; outputs of that

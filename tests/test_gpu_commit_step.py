@@ -128,6 +128,31 @@ def test_inputs_ready_pipelining_matches_plain_calls(cs):
         assert torch.allclose(prob, outs_plain[j][1], rtol=TOL["f32"][0], atol=TOL["f32"][1])
 
 
+def test_host_buffer_step_matches_device_call(cs):
+    """dllm_commit_step_host (host logits in, one packed host read out) gives
+    the device call's results bit for bit, over repeated steps whose host
+    logits are refilled between steps, for a greedy and a sampled rule."""
+    rng = np.random.default_rng(21)
+    B, L, V = 2, 24, 40_000
+    cand = torch.from_numpy((rng.random((B, L)) < 0.7).astype(np.uint8)).cuda()
+    host = torch.empty((B, L, V), dtype=torch.bfloat16).pin_memory()
+    for kw in ({"rule": 1, "tau": 0.6, "strict": True},
+               {"rule": 2, "k": 3, "temperature": 0.8, "key": 77}):
+        step = cs.HostStep(host, cand=cand, suppress_ids=[5, 17], **kw)
+        for j in range(3):
+            z = (rng.standard_normal((B * L, V)) * (2 + j)).astype(np.float32)
+            z[np.arange(B * L), rng.integers(0, V, B * L)] += 9
+            host.copy_(torch.from_numpy(z).view(B, L, V).to(torch.bfloat16))
+            x0, prob, ent, commit = step()
+            torch.cuda.synchronize()
+            dx0, dprob, dent, dcommit, _ = cs.commit_step(host.cuda(), cand=cand, suppress_ids=[5, 17], **kw)
+            torch.cuda.synchronize()
+            assert torch.equal(x0, dx0.cpu()) and torch.equal(commit, dcommit.cpu())
+            assert torch.equal(prob, dprob.cpu()) and torch.equal(ent, dent.cpu())
+    with pytest.raises(ValueError):
+        cs.HostStep(host.cuda(), rule=1, cand=cand)
+
+
 def test_repeated_fused_calls_leave_workspace_clean(cs):
     w = W.tiny()
     dev = to_device(w.logits, w.dtype)

@@ -80,3 +80,27 @@ def test_workspace_size_without_device(lib):
     a = lib.dllm_token_stats_workspace_size(1, 32, 126464, 1)
     b = lib.dllm_token_stats_workspace_size(32, 512, 126464, 0)
     assert 0 < a < b < (1 << 24)
+
+
+def test_commit_step_host_checks_arguments_before_any_device_work(lib):
+    """dllm_commit_step_host validates on the host and returns before queuing
+    anything: an empty shape is a no-op, bad pointers, dtype, alignment or
+    rule parameters are DLLM_ERR_INVALID_ARGUMENT (1)."""
+    P, i64, i32, f32, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_uint64
+    fn = lib.dllm_commit_step_host
+    fn.argtypes = [P, P, ctypes.c_int, i64, i64, i64, f32, u64, P, i32, P, P, P, P, ctypes.c_size_t, P]
+    fn.restype = ctypes.c_int
+    params = (ctypes.c_char * 256)()           # a zeroed dllm_commit_params: rule NONE, no candidates
+    cp = ctypes.cast(params, P)
+    fake = P(4096)                              # never dereferenced: every call below fails its checks
+    # empty shape: nothing to do
+    assert fn(None, None, 1, 0, 32, 1000, 0.0, 0, None, 0, cp, None, None, None, 0, None) == 0
+    # missing pointers / params
+    assert fn(None, fake, 1, 1, 32, 1000, 0.0, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1
+    assert fn(fake, fake, 1, 1, 32, 1000, 0.0, 0, None, 0, None, fake, fake, fake, 1 << 20, None) == 1
+    # bad dtype, misaligned packed output, negative temperature
+    assert fn(fake, fake, 7, 1, 32, 1000, 0.0, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1
+    assert fn(fake, fake, 1, 1, 32, 1000, 0.0, 0, None, 0, cp, P(4098), fake, fake, 1 << 20, None) == 1
+    assert fn(fake, fake, 1, 1, 32, 1000, -1.0, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1
+    # rule NONE with neither candidates nor a canvas is invalid (as for dllm_commit_step)
+    assert fn(fake, fake, 1, 1, 32, 1000, 0.0, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1

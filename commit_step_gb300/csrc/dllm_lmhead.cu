@@ -366,14 +366,15 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
           acc.idx = static_cast<int32_t>(v0 + (__ffs(eq) - 1));  // strictly larger than every earlier value
         }
         // The chunk's sums in packed pairs on two independent chains, then
-        // added to the row's: y = (z - m) log2 e, sum 2^y, sum 2^y y.
+        // added to the row's: y = z log2 e - m log2 e, sum 2^y, sum 2^y y.
         {
-          const uint64_t negm2 = pack2(-acc.m, -acc.m), cs2 = pack2(kLog2e, kLog2e);
+          const float nmc = -acc.m * kLog2e;
+          const uint64_t nmc2 = pack2(nmc, nmc), cs2 = pack2(kLog2e, kLog2e);
           uint64_t Za = 0, Sa = 0, Zb = 0, Sb = 0;
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
-            acc_pair2(Za, Sa, z[j], z[j + 1], negm2, cs2);
-            acc_pair2(Zb, Sb, z[j + 2], z[j + 3], negm2, cs2);
+            acc_pair2(Za, Sa, z[j], z[j + 1], nmc2, cs2);
+            acc_pair2(Zb, Sb, z[j + 2], z[j + 3], nmc2, cs2);
           }
           float z0, z1, s0, s1;
           unpack2(add2(Za, Zb), z0, z1);

@@ -117,12 +117,13 @@ __device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Adds two sanitized logits (<= the running max) to the sums (Z2, S2).
-// Adds two sanitized logits (<= m) to the sums: y = (z - m) cs, cs = s log2 e.
-__device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, float z1, uint64_t negm2,
+// Adds two sanitized logits (<= m) to the sums (Z2, S2): y = z cs - m cs in
+// one fused multiply-add per pair (cs = s log2 e; nmc2 holds fp32(-m cs)
+// twice), 2^y and 2^y y.  The rounding of m cs shifts every y of the row's
+// current running max alike, which cancels in prob and entropy.
+__device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, float z1, uint64_t nmc2,
                                           uint64_t cs2) {
-  const uint64_t d2 = add2(pack2(z0, z1), negm2);
-  const uint64_t y2 = mul2(d2, cs2);
+  const uint64_t y2 = fma2(pack2(z0, z1), cs2, nmc2);
   float y0, y1;
   unpack2(y2, y0, y1);
   const uint64_t e2 = pack2(ex2_approx(y0), ex2_approx(y1));
@@ -592,15 +593,16 @@ struct Consumer {
       acc.m = mnew;
       acc.negm = -mnew;
     }
-    const uint64_t negm2 = pack2(acc.negm, acc.negm);
+    const float nmc = acc.negm * cs;
+    const uint64_t nmc2 = pack2(nmc, nmc);
     uint64_t Zb = 0, Sb = 0;
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
       if (!FULL && !valid[j]) continue;
 #pragma unroll
       for (int e = 0; e < EPV; e += 4) {
-        acc_pair2(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), negm2, cs2);
-        acc_pair2(Zb, Sb, elem(w[j], e + 2), elem(w[j], e + 3), negm2, cs2);
+        acc_pair2(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), nmc2, cs2);
+        acc_pair2(Zb, Sb, elem(w[j], e + 2), elem(w[j], e + 3), nmc2, cs2);
       }
     }
     acc.Z2 = add2(acc.Z2, Zb);

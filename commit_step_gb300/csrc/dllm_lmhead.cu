@@ -3,18 +3,20 @@
 // mlx-arsenal "dLLM block decoding" (the statistics of the logits) and
 // mojo-dllm manual, "The GPU path": the LM head's output rows are only ever
 // consumed by the row statistics, so the logits z = h W^T need not reach
-// HBM.  logits tile = hidden tile (128 tokens x d) x weight tile (128 ids x
+// HBM.  logits tile = hidden tile (128 tokens x d) x weight tile (bn ids x
 // d)^T on the 5th-generation tensor cores: TMA brings 64-wide K slabs of both
 // into a shared-memory ring of up to 16 stages filling the CTA's shared memory
 // (128-byte swizzle), one thread issues
 // tcgen05.mma (kind::f16, bf16 in, fp32 accumulate) into one of two TMEM
-// accumulators (128 lanes x 128 columns each), and four epilogue warps read
-// each finished accumulator back with tcgen05.ld -- thread i of warp w holds
-// token 32 w + i's 128 logits of the tile -- and fold them into that token's running
-// statistics (max, sum 2^y, sum 2^y y, first argmax, best Gumbel score), the
-// same state the statistics kernels keep.  CTA c owns a contiguous range of
-// vocabulary tiles for every token tile; a finish kernel combines the CTAs'
-// per-token partials and writes x0, prob and entropy.
+// accumulators (128 lanes x 256 columns each, bn of them used), and two
+// warpgroups of epilogue warps read each finished accumulator back with
+// tcgen05.ld -- thread i of warp w holds token 32 (w % 4) + i, warpgroup g the
+// tile's 32-column chunks c = g (mod 2) -- and fold the logits into that
+// token's running statistics (max, sum 2^y, sum 2^y y, first argmax, best
+// Gumbel score), the same state the statistics kernels keep.  CTA c owns a
+// contiguous range of vocabulary tiles for every token tile; a finish kernel
+// combines the per-token partials (one per CTA and warpgroup) and writes x0,
+// prob and entropy.
 //
 // Waits are bounded (a clock64 deadline of about a second, then a fault code
 // in the workspace), the TMEM allocation is released before every exit, and

@@ -465,7 +465,7 @@ const char* dllm_status_string(dllm_status status) {
   switch (status) {
     case DLLM_OK: return "DLLM_OK";
     case DLLM_ERR_INVALID_ARGUMENT: return "DLLM_ERR_INVALID_ARGUMENT: a shape, pointer, value or alignment is wrong";
-    case DLLM_ERR_UNSUPPORTED: return "DLLM_ERR_UNSUPPORTED: valid, but outside what this build handles";
+    case DLLM_ERR_UNSUPPORTED: return "DLLM_ERR_UNSUPPORTED: valid, but outside what this library version handles";
     case DLLM_ERR_WORKSPACE: return "DLLM_ERR_WORKSPACE: workspace missing or too small";
     case DLLM_ERR_CUDA: return "DLLM_ERR_CUDA: a CUDA launch or query failed";
     case DLLM_ERR_DEVICE: return "DLLM_ERR_DEVICE: a kernel reported a fault";
@@ -481,7 +481,7 @@ size_t dllm_token_stats_workspace_size(int64_t B, int64_t L, int64_t V, dllm_dty
   if (B < 0 || L < 0) return 0;
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 160;  // no device: size for the largest part this build targets
+    sms = 160;  // no device: size for the largest part the library targets
   return ws_layout(B, L, sms).total;
 }
 

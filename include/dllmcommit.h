@@ -45,7 +45,7 @@ typedef struct CUstream_st* dllm_stream_t; /* a cudaStream_t */
 typedef enum {
   DLLM_OK = 0,
   DLLM_ERR_INVALID_ARGUMENT = 1, /* a shape, pointer, value or alignment is wrong */
-  DLLM_ERR_UNSUPPORTED = 2,      /* valid, but outside what this build handles */
+  DLLM_ERR_UNSUPPORTED = 2,      /* valid, but outside what this library version handles */
   DLLM_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
   DLLM_ERR_CUDA = 4,             /* a CUDA launch or query failed */
   DLLM_ERR_DEVICE = 5            /* a kernel reported a fault through the workspace */

@@ -189,12 +189,23 @@ dllm_status launch(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaS
 
 int esize_of(dllm_dtype dt) { return dt == DLLM_BF16 ? 2 : 4; }
 
+// a * b for a, b >= 0, or -1 when the product does not fit in int64 (such a
+// shape cannot describe memory; the entry points reject it before any other
+// arithmetic on it).
+int64_t checked_mul(int64_t a, int64_t b) {
+  if (a < 0 || b < 0) return -1;
+  if (a == 0 || b == 0) return 0;
+  return a > INT64_MAX / b ? -1 : a * b;
+}
+
 // Shared validation of the statistics arguments; fills the suppress list.
 dllm_status check_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
                         float temperature, const int32_t* sup, int32_t n_sup, const int32_t* x0, const float* prob,
                         const float* entropy, std::vector<int32_t>& sorted_sup) {
   if (B < 0 || L < 0 || V < 1 || V > INT32_MAX || row_stride < V) return DLLM_ERR_INVALID_ARGUMENT;
   if (dt != DLLM_F32 && dt != DLLM_BF16) return DLLM_ERR_INVALID_ARGUMENT;
+  // the logits' byte extent T * row_stride * size must be representable
+  if (checked_mul(checked_mul(checked_mul(B, L), row_stride), 4) < 0) return DLLM_ERR_INVALID_ARGUMENT;
   if (!(temperature >= 0.0f) || std::isinf(temperature)) return DLLM_ERR_INVALID_ARGUMENT;
   if (n_sup < 0 || (n_sup > 0 && !sup)) return DLLM_ERR_INVALID_ARGUMENT;
   if (n_sup > DLLM_MAX_SUPPRESS) return DLLM_ERR_UNSUPPORTED;
@@ -479,6 +490,8 @@ size_t dllm_token_stats_workspace_size(int64_t B, int64_t L, int64_t V, dllm_dty
   (void)V;
   (void)dt;
   if (B < 0 || L < 0) return 0;
+  const int64_t T = checked_mul(B, L);
+  if (T < 0 || T > (static_cast<int64_t>(1) << 56) || B > (static_cast<int64_t>(1) << 56)) return 0;
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 160;  // no device: size for the largest part the library targets
@@ -543,7 +556,8 @@ dllm_status dllm_entropy_bound_transfer(const float* entropy, const uint8_t* can
 dllm_status dllm_edit_transfer(const int32_t* x0, const float* prob, const int32_t* tokens, const uint8_t* editable,
                                int64_t B, int64_t L, float tau_edit, uint8_t* edit, dllm_stream_t stream) {
   if (B < 0 || L < 0 || std::isnan(tau_edit)) return DLLM_ERR_INVALID_ARGUMENT;
-  const int64_t n = B * L;
+  const int64_t n = checked_mul(B, L);
+  if (n < 0) return DLLM_ERR_INVALID_ARGUMENT;
   if (n == 0) return DLLM_OK;
   if (!x0 || !prob || !tokens || !editable || !edit) return DLLM_ERR_INVALID_ARGUMENT;
   const DeviceInfo* d = device_info();
@@ -581,6 +595,7 @@ dllm_status dllm_linear_temperature(int32_t remaining, int32_t num_steps, float 
 dllm_status dllm_uniform_canvas(int64_t B, int64_t N, int64_t V, uint64_t key, int32_t* canvas,
                                 int64_t canvas_stride, dllm_stream_t stream) {
   if (B < 0 || N < 0 || V <= 0 || V > INT32_MAX || canvas_stride < N) return DLLM_ERR_INVALID_ARGUMENT;
+  if (checked_mul(B, canvas_stride) < 0) return DLLM_ERR_INVALID_ARGUMENT;
   if (B * N == 0) return DLLM_OK;
   if (!canvas) return DLLM_ERR_INVALID_ARGUMENT;
   const DeviceInfo* d = device_info();
@@ -596,7 +611,7 @@ dllm_status dllm_uniform_canvas(int64_t B, int64_t N, int64_t V, uint64_t key, i
 
 dllm_status dllm_renoise(const int32_t* sample, const uint8_t* accepted, const int32_t* noise, const uint8_t* frozen,
                          int64_t B, int64_t N, int32_t* out, dllm_stream_t stream) {
-  if (B < 0 || N < 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (B < 0 || N < 0 || checked_mul(B, N) < 0) return DLLM_ERR_INVALID_ARGUMENT;
   if (B * N == 0) return DLLM_OK;
   if (!sample || !out || (accepted && !noise)) return DLLM_ERR_INVALID_ARGUMENT;
   const DeviceInfo* d = device_info();
@@ -698,7 +713,7 @@ dllm_status dllm_commit_step_host(const void* host_logits, void* dev_logits, dll
                                   int64_t V, float temperature, uint64_t key, const int32_t* suppress_ids,
                                   int32_t n_suppress, const dllm_commit_params* cp, void* dev_out, void* host_out,
                                   void* workspace, size_t workspace_bytes, dllm_stream_t stream) {
-  if (!cp || B < 0 || L < 0 || V < 1) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!cp || B < 0 || L < 0 || V < 1 || checked_mul(B, L) < 0) return DLLM_ERR_INVALID_ARGUMENT;
   if (B * L == 0) return DLLM_OK;
   if (!host_logits || !dev_logits || !dev_out || !host_out) return DLLM_ERR_INVALID_ARGUMENT;
   if ((reinterpret_cast<uintptr_t>(dev_out) & 3u) != 0) return DLLM_ERR_INVALID_ARGUMENT;

@@ -87,7 +87,10 @@ const char* dllm_version(void);
  * x0, prob, entropy   device outputs, T entries each.
  * workspace     device, >= dllm_token_stats_workspace_size(B, L, V, dt)
  *               bytes, zero-filled before its first use; every call leaves it
- *               zeroed again (the library resets what it uses).
+ *               zeroed again (the library resets what it uses).  The size
+ *               query returns 0 for a negative shape or one beyond 2^56 rows.
+ * Errors: DLLM_ERR_INVALID_ARGUMENT also when T * row_stride * 4 does not fit
+ * in int64 (no such buffer exists); nothing is launched on any error.
  * ------------------------------------------------------------------------ */
 size_t dllm_token_stats_workspace_size(int64_t B, int64_t L, int64_t V, dllm_dtype dt);
 

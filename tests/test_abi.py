@@ -104,3 +104,45 @@ def test_commit_step_host_checks_arguments_before_any_device_work(lib):
     assert fn(fake, fake, 1, 1, 32, 1000, -1.0, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1
     # rule NONE with neither candidates nor a canvas is invalid (as for dllm_commit_step)
     assert fn(fake, fake, 1, 1, 32, 1000, 0.0, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1
+
+
+def test_overflowing_shapes_are_rejected_on_the_host(lib):
+    """Shapes whose row count, element count or byte count does not fit in
+    int64 describe no buffer: the entry points return
+    DLLM_ERR_INVALID_ARGUMENT (1) before any other arithmetic on them (a
+    wrapped product could otherwise pass as an empty shape).  Nothing is
+    launched, so no device is needed."""
+    P, i64, i32, f32, u64, c_int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                    ctypes.c_uint64, ctypes.c_int)
+    fake = P(4096)                              # never dereferenced
+    big = 1 << 40                               # big * big wraps to 0 in int64
+    ts = lib.dllm_token_stats
+    ts.argtypes = [P, c_int, i64, i64, i64, i64, f32, u64, P, i32, P, P, P, P, ctypes.c_size_t, P]
+    ts.restype = c_int
+    assert ts(fake, 1, big, big, 1000, 1000, 0.0, 0, None, 0, fake, fake, fake, fake, 1 << 20, None) == 1
+    # rows fit, elements do not: 2^41 rows of stride 2^30
+    assert ts(fake, 0, 1 << 31, 1 << 10, 1000, 1 << 30, 0.0, 0, None, 0, fake, fake, fake, fake, 1 << 20, None) == 1
+    ws = lib.dllm_token_stats_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [i64, i64, i64, c_int]
+    assert ws(big, big, 1000, 1) == 0
+    assert ws(1 << 60, 0, 1000, 1) == 0
+    assert ws(1, 32, 1000, 1) > 0
+    edit = lib.dllm_edit_transfer
+    edit.argtypes = [P, P, P, P, i64, i64, f32, P, P]
+    edit.restype = c_int
+    assert edit(fake, fake, fake, fake, big, big, 0.5, fake, None) == 1
+    ren = lib.dllm_renoise
+    ren.argtypes = [P, P, P, P, i64, i64, P, P]
+    ren.restype = c_int
+    assert ren(fake, None, None, None, big, big, fake, None) == 1
+    uc = lib.dllm_uniform_canvas
+    uc.argtypes = [i64, i64, i64, u64, P, i64, P]
+    uc.restype = c_int
+    assert uc(big, 10, 1000, 0, fake, big, None) == 1
+    host = lib.dllm_commit_step_host
+    host.argtypes = [P, P, c_int, i64, i64, i64, f32, u64, P, i32, P, P, P, P, ctypes.c_size_t, P]
+    host.restype = c_int
+    params = (ctypes.c_char * 256)()
+    assert host(fake, fake, 1, big, big, 1000, 0.0, 0, None, 0, ctypes.cast(params, P), fake, fake, fake,
+                1 << 20, None) == 1

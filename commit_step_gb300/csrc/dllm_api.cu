@@ -571,7 +571,7 @@ dllm_status dllm_edit_transfer(const int32_t* x0, const float* prob, const int32
 
 dllm_status dllm_transfer_schedule(const int32_t* counts, int64_t B, int32_t steps, int32_t* quotas,
                                    dllm_stream_t stream) {
-  if (B < 0 || steps <= 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (B < 0 || steps <= 0 || checked_mul(B, steps) < 0) return DLLM_ERR_INVALID_ARGUMENT;
   if (B == 0) return DLLM_OK;
   if (!counts || !quotas) return DLLM_ERR_INVALID_ARGUMENT;
   const DeviceInfo* d = device_info();
@@ -663,6 +663,7 @@ dllm_status dllm_block_causal_mask(int64_t Lq, int64_t Lk, int64_t q_offset, int
   if (kind != DLLM_MASK_F32 && kind != DLLM_MASK_BF16 && kind != DLLM_MASK_KEEP_U8) return DLLM_ERR_INVALID_ARGUMENT;
   if (q_offset > INT64_MAX / 2 - Lq || k_offset > INT64_MAX / 2 - Lk || block_len > INT64_MAX / 4)
     return DLLM_ERR_INVALID_ARGUMENT;
+  if (checked_mul(checked_mul(Lq, row_stride), 4) < 0) return DLLM_ERR_INVALID_ARGUMENT;  // byte extent
   if (Lq * Lk == 0) return DLLM_OK;
   if (!out) return DLLM_ERR_INVALID_ARGUMENT;
   const DeviceInfo* d = device_info();

@@ -140,6 +140,14 @@ def test_overflowing_shapes_are_rejected_on_the_host(lib):
     uc.argtypes = [i64, i64, i64, u64, P, i64, P]
     uc.restype = c_int
     assert uc(big, 10, 1000, 0, fake, big, None) == 1
+    sched = lib.dllm_transfer_schedule
+    sched.argtypes = [P, i64, i32, P, P]
+    sched.restype = c_int
+    assert sched(fake, 1 << 40, 1 << 30, fake, None) == 1
+    mask = lib.dllm_block_causal_mask
+    mask.argtypes = [i64, i64, i64, i64, i64, c_int, P, i64, P]
+    mask.restype = c_int
+    assert mask(big, big, 0, 0, 32, 0, fake, big, None) == 1
     host = lib.dllm_commit_step_host
     host.argtypes = [P, P, c_int, i64, i64, i64, f32, u64, P, i32, P, P, P, P, ctypes.c_size_t, P]
     host.restype = c_int

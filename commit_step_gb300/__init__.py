@@ -143,6 +143,47 @@ def _need_cuda(*ts):
             raise ValueError("device tensors are required")
 
 
+_I32, _F32, _MASK = (torch.int32,), (torch.float32,), (torch.uint8, torch.bool)
+
+
+def _arg(t, name: str, numel: int, dtypes, device) -> None:
+    """Checks a tensor the library reads or writes through a raw pointer: on
+    ``device``, contiguous, ``numel`` elements of one of ``dtypes`` (the
+    kernels index it by row, so anything else would be read or written out
+    of bounds).  None passes: the argument is optional."""
+    if t is None:
+        return
+    if not torch.is_tensor(t):
+        raise TypeError(f"{name} must be a tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}; the call runs on {device}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must be {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+    if t.numel() != numel or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor of {numel} elements, got shape {tuple(t.shape)}")
+
+
+def _canvas_check(canvas, B: int, L: int, canvas_offset: int, device) -> None:
+    """A canvas updated at columns canvas_offset .. canvas_offset + L - 1 of
+    its first B rows."""
+    if canvas is None:
+        return
+    if not torch.is_tensor(canvas) or canvas.device != device:
+        raise ValueError(f"canvas must be a tensor on {device}")
+    if canvas.dim() != 2 or canvas.stride(1) != 1 or canvas.dtype != torch.int32:
+        raise ValueError("canvas must be a (B, N) int32 tensor with unit column stride")
+    off = int(canvas_offset)
+    if canvas.shape[0] < B or off < 0 or canvas.shape[1] < off + L:
+        raise ValueError(f"canvas {tuple(canvas.shape)} does not hold {B} rows of columns {off} .. {off + L - 1}")
+
+
+def _stats_out(out, T: int, device) -> None:
+    x0, prob, ent = out[:3]
+    _arg(x0, "x0", T, _I32, device)
+    _arg(prob, "prob", T, _F32, device)
+    _arg(ent, "entropy", T, _F32, device)
+
+
 _WS = {}
 
 
@@ -186,6 +227,7 @@ def token_stats(logits: torch.Tensor, temperature: float = 0.0, key: int = 0, su
         ent = torch.empty(shape, dtype=torch.float32, device=logits.device)
     else:
         x0, prob, ent = out
+        _stats_out(out, B * L, logits.device)
     sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
     if ws is None:
         ws = workspace(B, L, V, dt, logits.device, stream)
@@ -205,7 +247,11 @@ def _stats_ex(shape, device, logit_scale, margin, argmax):
         argmax = torch.empty(shape, dtype=torch.int32, device=device)
     margin = margin if torch.is_tensor(margin) else None
     argmax = argmax if torch.is_tensor(argmax) else None
-    _need_cuda(margin, argmax)
+    n = 1
+    for d in shape:
+        n *= int(d)
+    _arg(margin, "margin", n, _F32, device)
+    _arg(argmax, "argmax", n, _I32, device)
     if float(logit_scale) == 1.0 and margin is None and argmax is None:
         return None, None, None
     ex = StatsEx()
@@ -232,6 +278,7 @@ def token_stats_ex(logits: torch.Tensor, temperature: float = 0.0, key: int = 0,
         ent = torch.empty(shape, dtype=torch.float32, device=logits.device)
     else:
         x0, prob, ent = out
+        _stats_out(out, B * L, logits.device)
     ex, margin, argmax = _stats_ex(shape, logits.device, logit_scale, margin, argmax)
     sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
     if ws is None:
@@ -243,13 +290,13 @@ def token_stats_ex(logits: torch.Tensor, temperature: float = 0.0, key: int = 0,
     return x0, prob, ent, margin, argmax
 
 
-def _canvas_args(x0, canvas, canvas_offset):
+def _canvas_args(x0, canvas, canvas_offset, B: int, L: int, device):
     if canvas is None:
         return None, None, 0, 0
     if x0 is None:
         raise ValueError("a canvas update needs x0")
-    if canvas.dim() != 2 or canvas.stride(1) != 1 or canvas.dtype != torch.int32:
-        raise ValueError("canvas must be a (B, N) int32 tensor with unit column stride")
+    _arg(x0, "x0", B * L, _I32, device)
+    _canvas_check(canvas, B, L, canvas_offset, device)
     return _ptr(x0), _ptr(canvas), canvas.stride(0), int(canvas_offset)
 
 
@@ -259,15 +306,18 @@ def _rule_io(conf, cand, commit):
         raise ValueError("scores must be a contiguous (B, L) float32 tensor")
     if cand.shape != conf.shape or cand.dtype not in (torch.uint8, torch.bool) or not cand.is_contiguous():
         raise ValueError("candidates must be a contiguous (B, L) bool/uint8 tensor")
+    if cand.device != conf.device:
+        raise ValueError("scores and candidates must be on one device")
     if commit is None:
         commit = torch.empty(conf.shape, dtype=torch.uint8, device=conf.device)
+    _arg(commit, "commit", conf.numel(), _MASK, conf.device)
     return conf.shape[0], conf.shape[1], commit
 
 
 def threshold_transfer(conf, cand, tau: float, strict: bool = False, commit=None, x0=None, canvas=None,
                        canvas_offset: int = 0, stream=None):
     B, L, commit = _rule_io(conf, cand, commit)
-    a = _canvas_args(x0, canvas, canvas_offset)
+    a = _canvas_args(x0, canvas, canvas_offset, B, L, commit.device)
     _check(_lib.dllm_threshold_transfer(_ptr(conf), _ptr(cand), B, L, float(tau), int(bool(strict)), _ptr(commit),
                                         *a, _stream(stream)), "dllm_threshold_transfer")
     return commit
@@ -277,9 +327,8 @@ def topk_transfer(conf, cand, k, commit=None, x0=None, canvas=None, canvas_offse
     B, L, commit = _rule_io(conf, cand, commit)
     if not torch.is_tensor(k):
         k = torch.full((B,), int(k), dtype=torch.int32, device=conf.device)
-    if k.dtype != torch.int32 or k.numel() != B or not k.is_cuda:
-        raise ValueError("k must be a (B,) int32 device tensor")
-    a = _canvas_args(x0, canvas, canvas_offset)
+    _arg(k, "k", B, _I32, conf.device)
+    a = _canvas_args(x0, canvas, canvas_offset, B, L, commit.device)
     _check(_lib.dllm_topk_transfer(_ptr(conf), _ptr(cand), B, L, _ptr(k), _ptr(commit), *a, _stream(stream)),
            "dllm_topk_transfer")
     return commit
@@ -287,7 +336,7 @@ def topk_transfer(conf, cand, k, commit=None, x0=None, canvas=None, canvas_offse
 
 def factor_transfer(conf, cand, factor: float, commit=None, x0=None, canvas=None, canvas_offset: int = 0, stream=None):
     B, L, commit = _rule_io(conf, cand, commit)
-    a = _canvas_args(x0, canvas, canvas_offset)
+    a = _canvas_args(x0, canvas, canvas_offset, B, L, commit.device)
     _check(_lib.dllm_factor_transfer(_ptr(conf), _ptr(cand), B, L, float(factor), _ptr(commit), *a, _stream(stream)),
            "dllm_factor_transfer")
     return commit
@@ -296,7 +345,7 @@ def factor_transfer(conf, cand, factor: float, commit=None, x0=None, canvas=None
 def entropy_bound_transfer(entropy, cand, gamma: float, commit=None, x0=None, canvas=None, canvas_offset: int = 0,
                            stream=None):
     B, L, commit = _rule_io(entropy, cand, commit)
-    a = _canvas_args(x0, canvas, canvas_offset)
+    a = _canvas_args(x0, canvas, canvas_offset, B, L, commit.device)
     _check(_lib.dllm_entropy_bound_transfer(_ptr(entropy), _ptr(cand), B, L, float(gamma), _ptr(commit), *a,
                                             _stream(stream)), "dllm_entropy_bound_transfer")
     return commit
@@ -309,8 +358,13 @@ def edit_transfer(x0, prob, tokens, editable, tau_edit: float, edit=None, stream
     for t, dt in ((x0, torch.int32), (prob, torch.float32), (tokens, torch.int32)):
         if t.dtype != dt or not t.is_contiguous():
             raise ValueError("edit_transfer: x0/tokens int32, prob float32, all contiguous")
+    _arg(editable, "editable", x0.numel(), _MASK, x0.device)
+    for t in (prob, tokens):
+        if t.device != x0.device:
+            raise ValueError("edit_transfer inputs must be on one device")
     if edit is None:
         edit = torch.empty(x0.shape, dtype=torch.uint8, device=x0.device)
+    _arg(edit, "edit", x0.numel(), _MASK, x0.device)
     B, L = x0.shape
     _check(_lib.dllm_edit_transfer(_ptr(x0), _ptr(prob), _ptr(tokens), _ptr(editable), B, L, float(tau_edit),
                                    _ptr(edit), _stream(stream)), "dllm_edit_transfer")
@@ -324,6 +378,7 @@ def transfer_schedule(counts, steps: int, quotas=None, stream=None):
     B = counts.numel()
     if quotas is None:
         quotas = torch.empty((B, max(int(steps), 0)), dtype=torch.int32, device=counts.device)
+    _arg(quotas, "quotas", B * max(int(steps), 0), _I32, counts.device)
     _check(_lib.dllm_transfer_schedule(_ptr(counts), B, int(steps), _ptr(quotas), _stream(stream)),
            "dllm_transfer_schedule")
     return quotas
@@ -340,6 +395,25 @@ def block_ranges(P: int, gen_len: int, block_len: int, align: bool = False):
     return [(buf[2 * i], buf[2 * i + 1]) for i in range(n.value)]
 
 
+def _fused_args(B: int, L: int, device, rule, edit, k, cand, canvas, canvas_offset, counts, commit=None,
+                edit_mask=None, check_commit=False) -> None:
+    """Checks the device tensors of a fused step (dllm_commit_step and its
+    host-buffer form)."""
+    T = B * L
+    _arg(cand, "cand", T, _MASK, device)
+    _arg(k, "k", B, _I32, device)
+    _arg(counts, "counts", 3 * B, _I32, device)
+    _canvas_check(canvas, B, L, canvas_offset, device)
+    if check_commit and rule != RULE_NONE:
+        if commit is None:
+            raise ValueError("a commit rule needs a commit mask")
+        _arg(commit, "commit", T, _MASK, device)
+    if edit:
+        if edit_mask is None:
+            raise ValueError("the edit rule needs an edit mask")
+        _arg(edit_mask, "edit_mask", T, _MASK, device)
+
+
 def _commit_params(rule, strict, tau, factor, gamma, k, cand, mask_id, edit, tau_edit, commit, edit_mask, canvas,
                    canvas_offset, counts, inputs_ready, ex) -> CommitParams:
     """The dllm_commit_params of a call (device tensors or None)."""
@@ -351,9 +425,7 @@ def _commit_params(rule, strict, tau, factor, gamma, k, cand, mask_id, edit, tau
     p.edit, p.tau_edit = int(bool(edit)), float(tau_edit)
     p.commit = None if commit is None else commit.data_ptr()
     p.edit_mask = None if edit_mask is None else edit_mask.data_ptr()
-    if canvas is not None:
-        if canvas.dim() != 2 or canvas.stride(1) != 1 or canvas.dtype != torch.int32:
-            raise ValueError("canvas must be a (B, N) int32 tensor with unit column stride")
+    if canvas is not None:   # checked by the caller (_fused_args)
         p.canvas, p.canvas_stride, p.canvas_offset = canvas.data_ptr(), canvas.stride(0), int(canvas_offset)
     p.counts = None if counts is None else counts.data_ptr()
     p.flags = FLAG_INPUTS_READY if inputs_ready else 0
@@ -393,8 +465,10 @@ def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, su
         edit_mask = torch.empty((B, L), dtype=torch.uint8, device=dev) if edit else None
     else:
         x0, prob, ent, commit, edit_mask = out
+        _stats_out(out, B * L, dev)
     if rule == RULE_TOPK and not torch.is_tensor(k):
         k = torch.full((B,), int(k), dtype=torch.int32, device=dev)
+    _fused_args(B, L, dev, rule, edit, k, cand, canvas, canvas_offset, counts, commit, edit_mask, check_commit=True)
     ex, _, _ = _stats_ex((B, L), dev, logit_scale, margin, argmax)
     p = _commit_params(rule, strict, tau, factor, gamma, k, cand, mask_id, edit, tau_edit, commit, edit_mask, canvas,
                        canvas_offset, counts, inputs_ready, ex)
@@ -434,6 +508,8 @@ class HostStep:
         B, L, V, _ = _logits_view(host_logits)
         dt = _dtype_code(host_logits)
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        if dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
         _need_cuda(cand, canvas, k, counts, edit_mask)
         T = B * L
         self.dev_logits = torch.empty(host_logits.shape, dtype=host_logits.dtype, device=dev)
@@ -448,6 +524,7 @@ class HostStep:
         if edit and edit_mask is None:
             edit_mask = torch.empty((B, L), dtype=torch.uint8, device=dev)
         self.edit_mask = edit_mask if edit else None
+        _fused_args(B, L, dev, rule, edit, k, cand, canvas, canvas_offset, counts, None, self.edit_mask)
         ex, _, _ = _stats_ex((B, L), dev, logit_scale, margin, argmax)
         self._ex = ex
         self._p = _commit_params(rule, strict, tau, factor, gamma, k, cand, mask_id, edit, tau_edit, None,
@@ -485,6 +562,7 @@ def token_stats_noalloc(logits: torch.Tensor, temperature: float = 0.0, key: int
                torch.empty(shape, dtype=torch.float32, device=logits.device),
                torch.empty(shape, dtype=torch.float32, device=logits.device))
     x0, prob, ent = out
+    _stats_out(out, B * L, logits.device)
     sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
     _check(_lib.dllm_token_stats_noalloc(_ptr(logits), dt, B, L, V, stride, float(temperature),
                                          int(key) & (2**64 - 1), sup, len(suppress_ids), _ptr(x0), _ptr(prob),

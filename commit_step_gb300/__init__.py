@@ -615,10 +615,13 @@ def renoise(sample: torch.Tensor, accepted: Optional[torch.Tensor], noise: Optio
     for t, dt in ((accepted, (torch.uint8, torch.bool)), (noise, (torch.int32,))):
         if t is not None and (t.shape != sample.shape or t.dtype not in dt or not t.is_contiguous()):
             raise ValueError("accepted / noise must be contiguous and shaped like sample")
+    for t in (accepted, noise):
+        if t is not None and t.device != sample.device:
+            raise ValueError("renoise inputs must be on one device")
+    _arg(frozen, "frozen", B, _MASK, sample.device)
     if out is None:
         out = torch.empty_like(sample)
-    if out.shape != sample.shape or out.dtype != torch.int32 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous (B, N) int32 tensor")
+    _arg(out, "out", B * N, _I32, sample.device)
     _check(_lib.dllm_renoise(_ptr(sample), _ptr(accepted), _ptr(noise), _ptr(frozen), B, N, _ptr(out),
                              _stream(stream)), "dllm_renoise")
     return out
@@ -643,8 +646,13 @@ class StableConfidentStopping:
         if argmax.shape != (B, L) or entropy.shape != (B, L) or not argmax.is_contiguous() or \
                 not entropy.is_contiguous() or argmax.dtype != torch.int32 or entropy.dtype != torch.float32:
             raise ValueError("argmax / entropy must be contiguous (B, L) int32 / float32 tensors")
+        dev = self.prev.device
+        if argmax.device != dev or entropy.device != dev:
+            raise ValueError(f"argmax / entropy must be on the criterion's device {dev}")
+        _arg(done, "done", B, _MASK, dev)
         if stop is None:
-            stop = torch.empty((B,), dtype=torch.uint8, device=argmax.device)
+            stop = torch.empty((B,), dtype=torch.uint8, device=dev)
+        _arg(stop, "stop", B, _MASK, dev)
         _check(_lib.dllm_stable_confident_stop(_ptr(argmax), _ptr(entropy), B, L, self.stability_threshold,
                                                self.confidence_threshold, _ptr(self.prev), _ptr(self.count),
                                                _ptr(stop), _ptr(done), _stream(stream)),
@@ -690,11 +698,14 @@ def lm_head_stats(hidden: torch.Tensor, weight: torch.Tensor, temperature: float
         raise ValueError("hidden (T, d) and weight (V, d) need unit column stride and the same d")
     T, d = hidden.shape
     V = weight.shape[0]
+    if weight.device != hidden.device or (logits is not None and logits.device != hidden.device):
+        raise ValueError("hidden, weight and logits must be on one device")
     if out is None:
         out = (torch.empty((T,), dtype=torch.int32, device=hidden.device),
                torch.empty((T,), dtype=torch.float32, device=hidden.device),
                torch.empty((T,), dtype=torch.float32, device=hidden.device))
     x0, prob, ent = out
+    _stats_out(out, T, hidden.device)
     if logits is not None and (logits.dtype != torch.float32 or logits.shape != (T, V) or logits.stride(1) != 1):
         raise ValueError("logits must be a (T, V) float32 tensor with unit column stride")
     if ws is None:
@@ -720,9 +731,15 @@ def uniform_update(sample: torch.Tensor, accepted: torch.Tensor, step_argmax: to
     and update ``stop``'s state and the done flags (dllm_uniform_update)."""
     B, N = sample.shape
     _need_cuda(sample, accepted, step_argmax, entropy, canvas, argmax, done)
-    for t in (sample, accepted, step_argmax, entropy, canvas, argmax):
-        if t.shape != (B, N) or not t.is_contiguous():
+    dev = sample.device
+    for t, name, dts in ((sample, "sample", _I32), (accepted, "accepted", _MASK), (step_argmax, "step_argmax", _I32),
+                         (entropy, "entropy", _F32), (canvas, "canvas", _I32), (argmax, "argmax", _I32)):
+        if t.shape != (B, N):
             raise ValueError("uniform_update takes contiguous (B, N) tensors")
+        _arg(t, name, B * N, dts, dev)
+    _arg(done, "done", B, _MASK, dev)
+    if stop.prev.shape != (B, N) or stop.prev.device != dev:
+        raise ValueError("the stopping criterion's state must be (B, N) on the same device")
     _check(_lib.dllm_uniform_update(_ptr(sample), _ptr(accepted), _ptr(step_argmax), _ptr(entropy), B, N, V,
                                     int(noise_key) & (2**64 - 1), stop.stability_threshold,
                                     stop.confidence_threshold, _ptr(canvas), _ptr(argmax), _ptr(stop.prev),

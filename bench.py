@@ -767,7 +767,8 @@ def main():
         return 0
     res, w = run_ours(args, rank, world)
     if rank == 0:
-        if not args.no_cpu_baseline and not args.profile:
+        # the oracle baseline is timed at N=1 only (one replica's host cores)
+        if world == 1 and not args.no_cpu_baseline and not args.profile:
             res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
         print(json.dumps(res))
     if world > 1:

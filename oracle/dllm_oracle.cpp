@@ -19,7 +19,7 @@
 //
 // Parity pins (the tests): worked examples per rule, closed forms for the
 // statistics, invariants, brute force on tiny inputs, Philox against
-// PyTorch's and cuRAND's implementations, ln_p against the true logarithm
+// PyTorch's independent header-only engine, ln_p against the true logarithm
 // within its derived bound, and a chi-square check of Gumbel-max sampling.
 
 #include "dllm_oracle.h"

@@ -151,8 +151,9 @@ dllm_status dllm_token_stats_ex(const void* logits, dllm_dtype dt, int64_t B, in
  * workspace.  The scratch memory is one fixed device array inside the
  * library, DLLM_NOALLOC_SCRATCH_BYTES per GPU, held by every GPU that loads
  * the library until the process exits.  A shape whose scratch does not fit
- * (about (B*L + B) * 4 bytes plus a fixed part, so B*L up to roughly 250,000
- * rows) returns DLLM_ERR_UNSUPPORTED without launching anything.
+ * (4 bytes per row and 16 per batch row, plus about 40 KB for the partial
+ * reductions, so B*L up to roughly 250,000 rows) returns
+ * DLLM_ERR_UNSUPPORTED without launching anything.
  *   - The first call on each device looks the array's device address up
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.

@@ -571,8 +571,14 @@ def token_stats_noalloc(logits: torch.Tensor, temperature: float = 0.0, key: int
 
 
 def workspace_fault(ws: torch.Tensor, stream=None) -> int:
+    """The fault code a kernel left in ``ws`` (0: none).  After a fault the
+    workspace's counters may be left non-zero, so the whole tensor is zeroed
+    here, on the same stream, before it can be used again."""
     f = C.c_int32(0)
     _check(_lib.dllm_workspace_fault(_ptr(ws), _stream(stream), C.byref(f)), "dllm_workspace_fault")
+    if f.value != 0:
+        with torch.cuda.stream(torch.cuda.current_stream(ws.device) if stream is None else stream):
+            ws.zero_()
     return f.value
 
 

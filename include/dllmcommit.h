@@ -432,7 +432,11 @@ dllm_status dllm_commit_step_host(const void* host_logits, void* dev_logits, dll
 /* Reads and clears the device fault word of a workspace (synchronises the
  * stream).  *fault = 0 when no kernel reported a fault; otherwise a code
  * naming the wait that gave up (the kernel stopped early; outputs of that
- * call are undefined).  Returns DLLM_ERR_CUDA if the copy fails. */
+ * call are undefined).  A faulted call can also leave the workspace's
+ * per-row and per-batch-row counters non-zero: zero the whole workspace
+ * before its next use (only the fault word is cleared here, since the call
+ * does not know the workspace's size).  Returns DLLM_ERR_CUDA if the copy
+ * fails. */
 dllm_status dllm_workspace_fault(void* workspace, dllm_stream_t stream, int32_t* fault);
 
 #ifdef __cplusplus

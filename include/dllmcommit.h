@@ -19,7 +19,9 @@
  *   - Every device-side call is asynchronous on the given stream (0 = the
  *     legacy default stream) and is launched with programmatic dependent
  *     launch, so its prologue may overlap the previous kernel in the stream;
- *     it reads no input before that kernel has finished.
+ *     it reads no input before that kernel has finished, except where a
+ *     declaration says so (DLLM_FLAG_INPUTS_READY of dllm_commit_step; the
+ *     first weight slabs of dllm_lm_head_stats).
  *   - Arguments are validated on the host first; on any error nothing is
  *     launched and the status says why.  A failed launch returns
  *     DLLM_ERR_CUDA (the CUDA error is left for cudaGetLastError).
@@ -48,7 +50,8 @@ typedef enum {
   DLLM_ERR_UNSUPPORTED = 2,      /* valid, but outside what this library version handles */
   DLLM_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
   DLLM_ERR_CUDA = 4,             /* a CUDA launch or query failed */
-  DLLM_ERR_DEVICE = 5            /* a kernel reported a fault through the workspace */
+  DLLM_ERR_DEVICE = 5            /* reserved: calls are asynchronous, so a kernel's fault is
+                                    reported by dllm_workspace_fault, not by the call */
 } dllm_status;
 
 typedef enum { DLLM_F32 = 0, DLLM_BF16 = 1 } dllm_dtype;

@@ -74,6 +74,27 @@ def test_block_ranges_errors(lib):
     assert lib.dllm_block_ranges(5, 10, 4, 0, None, 0, ctypes.byref(n)) == 3 and n.value == 3
 
 
+def test_linear_temperature_matches_oracle(lib):
+    """dllm_linear_temperature is host-only: the library's value equals the
+    oracle's bit for bit, and bad schedules are rejected."""
+    import numpy as np
+
+    f = lib.dllm_linear_temperature
+    f.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float, ctypes.POINTER(ctypes.c_float)]
+    f.restype = ctypes.c_int
+    out = ctypes.c_float(0.0)
+    for num_steps in (1, 7, 48, 1000):
+        for remaining in sorted({0, 1, num_steps // 3, num_steps - 1, num_steps}):
+            for t_min, t_max in ((0.4, 0.8), (0.05, 3.0), (1.0, 1.0)):
+                assert f(remaining, num_steps, t_min, t_max, ctypes.byref(out)) == 0
+                assert np.float32(out.value) == oracle.linear_temperature(remaining, num_steps, t_min, t_max)
+    assert f(5, 4, 0.4, 0.8, ctypes.byref(out)) == 1       # remaining > num_steps
+    assert f(1, 0, 0.4, 0.8, ctypes.byref(out)) == 1       # num_steps <= 0
+    assert f(1, 4, 0.0, 0.8, ctypes.byref(out)) == 1       # t_min <= 0
+    assert f(1, 4, 0.9, 0.8, ctypes.byref(out)) == 1       # t_max < t_min
+    assert f(1, 4, 0.4, 0.8, None) == 1                    # no output
+
+
 def test_workspace_size_without_device(lib):
     lib.dllm_token_stats_workspace_size.restype = ctypes.c_size_t
     lib.dllm_token_stats_workspace_size.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int]

@@ -737,7 +737,9 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": n, "warmup": warmup, "ms_per_step": dt * 1e3 / n, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator, dllm_workloads.py)",
-        "config": {"workload": describe(w), "sample": f"{sub.logits.shape[0]} rows per step"},
+        "config": {"workload": describe(w), "global_batch": w.B * world, "seq_len": w.L, "vocab": w.V,
+                   "parallelism": f"replicas x{world} (batch rows shard, no collective)",
+                   "sample": f"{sub.logits.shape[0]} rows per step"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.default_threads(), "kind": "oracle",
                          "sample": f"{n} steps over {sub.logits.shape[0]} rows of the {w.name} workload"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -36,9 +36,6 @@
 
 namespace {
 
-constexpr float kNegInfThreshold = -0x1p+100f;  // -2^100
-constexpr float kPosClamp = 0x1p+100f;          // 2^100
-
 // ---------------------------------------------------------------------------
 // Philox4x32-10, from its definition in Salmon et al., "Parallel random
 // numbers: as easy as 1, 2, 3" (SC'11): ten rounds of two 32x32->64
@@ -123,10 +120,11 @@ float gumbel_score(float z, float t, uint64_t key, int64_t row, int64_t v) {
   return std::fma(t, g, z);
 }
 
-// A logit as the statistics see it: bf16 widens exactly to fp32; NaN and
-// anything at or below -2^100 count as -inf (no probability mass); anything
-// at or above 2^100 (+inf included) counts as 2^100, so the largest entries
-// share the mass equally.
+// A logit as the statistics see it: bf16 widens exactly to fp32 and a NaN
+// counts as -inf (no probability mass, [ARS] token_stats "NaN-safe").  Every
+// other value, however large, is the logit itself: finite logits go through
+// the ordinary softmax, and +inf entries (if any) share the mass (the limit
+// of the softmax as those logits grow together).
 inline float load_logit(const void* base, int dtype, int64_t idx) {
   float z;
   if (dtype == 1) {
@@ -135,8 +133,7 @@ inline float load_logit(const void* base, int dtype, int64_t idx) {
   } else {
     z = static_cast<const float*>(base)[idx];
   }
-  if (std::isnan(z) || z <= kNegInfThreshold) return -std::numeric_limits<float>::infinity();
-  if (z >= kPosClamp) return kPosClamp;
+  if (std::isnan(z)) return -std::numeric_limits<float>::infinity();
   return z;
 }
 
@@ -149,11 +146,11 @@ struct RowOut {
 };
 
 // The logit of id v as the statistics see it: sanitised (load_logit), then
-// scaled by the caller's fp32 factor s in one fp32 multiplication (a logit
-// with no mass keeps none).  s = 1 leaves the logit as it is; s = 1/T gives
-// the temperature-scaled logits the uniform-noise loop of "dLLM block
-// decoding" (section "Uniform-noise decoding (DiffusionGemma)") measures its
-// entropy on and samples from.
+// scaled by the caller's fp32 factor s in one fp32 multiplication (a product
+// beyond the fp32 range is +-inf; a logit with no mass keeps none).  s = 1
+// leaves the logit as it is; s = 1/T gives the temperature-scaled logits the
+// uniform-noise loop of "dLLM block decoding" (section "Uniform-noise
+// decoding (DiffusionGemma)") measures its entropy on and samples from.
 inline float scaled_logit(const void* logits, int dtype, int64_t idx, float s) {
   const float z = load_logit(logits, dtype, idx);
   if (z == -std::numeric_limits<float>::infinity()) return z;
@@ -206,11 +203,23 @@ RowOut stats_row(const void* logits, int dtype, int64_t row_off, int64_t V, int6
     have_r = true;
   }
   RowOut out{static_cast<int32_t>(x0), 0.0, 0.0, 0.0, static_cast<int32_t>(first_max)};
+  const double log_veff = std::log(static_cast<double>(v_eff));
   if (m == -std::numeric_limits<float>::infinity()) {
-    // No finite mass anywhere: the uniform limit over A.
+    // No mass anywhere (every logit NaN or -inf): the uniform limit over A.
     out.prob = 1.0 / static_cast<double>(v_eff);
-    out.entropy = std::log(static_cast<double>(v_eff));
+    out.entropy = log_veff;
     out.margin = out.prob - (have_r ? out.prob : 0.0);
+    return out;
+  }
+  if (m == std::numeric_limits<float>::infinity()) {
+    // The +inf entries share the mass equally; every finite logit has none.
+    int64_t n_inf = 0;
+    for (int64_t v = 0; v < V; ++v)
+      if (!absent[v] && zl(v) == m) ++n_inf;
+    const double share = 1.0 / static_cast<double>(n_inf);
+    out.prob = zl(x0) == m ? share : 0.0;
+    out.margin = out.prob - ((have_r && r == m) ? share : 0.0);
+    out.entropy = std::min(std::log(static_cast<double>(n_inf)), log_veff);
     return out;
   }
   // Pass 2: Z = sum exp(z - m), S = sum exp(z - m)(z - m); -inf terms add 0.
@@ -231,7 +240,7 @@ RowOut stats_row(const void* logits, int dtype, int64_t row_off, int64_t V, int6
   out.margin = out.prob - p_r;
   // H = -sum p log p = log Z - S / Z, clamped to its range [0, log |A|].
   double H = std::log(Z) - S / Z;
-  H = std::min(std::max(H, 0.0), std::log(static_cast<double>(v_eff)));
+  H = std::min(std::max(H, 0.0), log_veff);
   out.entropy = H;
   return out;
 }

@@ -28,10 +28,9 @@ def test_margin_worked_examples(golden):
 
 
 def _sanitised(z):
-    """The readings of a logit: NaN and <= -2^100 carry no mass (-inf); >= 2^100 counts as 2^100."""
+    """The reading of a logit: NaN carries no mass (-inf); every other value is itself."""
     z = np.asarray(z, dtype=np.float32).copy()
-    z[np.isnan(z) | (z <= np.float32(-2.0**100))] = -np.inf
-    z[z >= np.float32(2.0**100)] = np.float32(2.0**100)
+    z[np.isnan(z)] = -np.inf
     return z
 
 
@@ -39,11 +38,14 @@ def _brute(z, s, sup):
     """x0, prob, margin, argmax of one row from its probability vector."""
     V = z.size
     A = [v for v in range(V) if v not in sup]
-    zs = _sanitised(z) * np.float32(s)              # one fp32 multiplication per logit
+    with np.errstate(over="ignore", invalid="ignore"):
+        zs = _sanitised(z) * np.float32(s)          # one fp32 multiplication per logit (may overflow to inf)
     zs[np.isinf(zs) & (zs < 0)] = -np.inf
     za = zs[A].astype(np.float64)
     if np.all(za == -np.inf):
         p = np.full(len(A), 1.0 / len(A))
+    elif za.max() == np.inf:
+        p = (za == np.inf) / np.count_nonzero(za == np.inf)   # the +inf entries share the mass
     else:
         p = np.exp(za - za.max())
         p /= p.sum()
@@ -56,7 +58,8 @@ def _brute(z, s, sup):
 
 def test_margin_bruteforce_tiny_rows():
     rng = np.random.default_rng(2024)
-    specials = [np.nan, np.inf, -np.inf, np.float32(2.0**101), np.float32(-2.0**105)]
+    specials = [np.nan, np.inf, -np.inf, np.float32(2.0**101), np.float32(-2.0**105), np.float32(3e38),
+                np.float32(-1e31)]
     for trial in range(400):
         V = int(rng.integers(1, 9))
         if trial % 3 == 0:

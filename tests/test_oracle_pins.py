@@ -103,12 +103,53 @@ def test_all_masked_row_is_uniform_limit():
 
 
 def test_positive_infinity_shares_mass():
-    # +inf and values >= 2^100 count as 2^100: the top entries share the mass
+    # +inf entries share the mass equally; finite logits, however large, get none
     z = np.array([[0.0, np.inf, 5.0, 2.0**101, np.inf, 1.0]], dtype=np.float32)
     x0, p, h = oracle.token_stats(z)
-    assert x0[0] == 1 and p[0] == pytest.approx(1 / 3) and h[0] == pytest.approx(math.log(3))
+    assert x0[0] == 1 and p[0] == pytest.approx(1 / 2) and h[0] == pytest.approx(math.log(2))
     x0, p, h = oracle.token_stats(z, temperature=0.5, key=3)
-    assert x0[0] in (1, 3, 4) and p[0] == pytest.approx(1 / 3)
+    assert x0[0] in (1, 4) and p[0] == pytest.approx(1 / 2)
+
+
+def test_huge_finite_logits_take_the_plain_softmax():
+    """Finite logits beyond any clamp are ordinary logits ("dLLM block
+    decoding", What mlx-arsenal ships: token_stats is NaN-safe; nothing else
+    is special).  exp(1e37 - 1e38) is 0 in double, so the larger takes all."""
+    z = np.array([[1e38, 1e37]], dtype=np.float32)
+    x0, p, h = oracle.token_stats(z)
+    assert x0[0] == 0 and p[0] == 1.0 and h[0] == 0.0
+    # a single finite logit among NaNs is certain, however negative it is
+    z = np.array([[-1e31, np.nan, np.nan]], dtype=np.float32)
+    x0, p, h = oracle.token_stats(z)
+    assert x0[0] == 0 and p[0] == 1.0 and h[0] == 0.0
+    # three equal maxima at the top of the fp32 range share the mass
+    top = np.float32(3.4e38)
+    z = np.array([[5.0, top, -top, top, 1e30, top]], dtype=np.float32)
+    x0, p, h = oracle.token_stats(z)
+    assert x0[0] == 1 and p[0] == pytest.approx(1 / 3, rel=1e-15) and h[0] == pytest.approx(math.log(3), rel=1e-15)
+    # the same row sampled: one of the maxima, with its share
+    x0, p, h = oracle.token_stats(z, temperature=0.8, key=11)
+    assert x0[0] in (1, 3, 5) and p[0] == pytest.approx(1 / 3, rel=1e-15)
+
+
+@pytest.mark.parametrize("level", [0.0, 1e3, -1e3, 2.0**20, -(2.0**20), 1e9, -1e9])
+def test_two_level_rows_at_any_offset(level):
+    """Closed form of a row with a entries at x and b entries at x - d:
+    p = 1 / (a + b e^-d) for an entry at x, H = ln(a + b e^-d) + b d e^-d / (a + b e^-d).
+    Softmax is shift invariant, so the answer does not depend on x: the
+    oracle must give it at every offset, up to the fp32 spacing of x."""
+    x = np.float32(level)
+    ulp = float(np.spacing(np.abs(x))) if x != 0 else 2.0**-149
+    d = float(np.float32(max(1.5, ulp)))          # an exact fp32 gap at this offset
+    lo = np.float32(x - np.float32(d))
+    d = float(x) - float(lo)
+    a, b = 3, 5
+    z = np.array([[lo] * b + [x] * a], dtype=np.float32)
+    x0, p, h = oracle.token_stats(z)
+    Z = a + b * math.exp(-d)
+    assert x0[0] == b
+    assert p[0] == pytest.approx(1 / Z, rel=1e-12)
+    assert h[0] == pytest.approx(math.log(Z) + b * d * math.exp(-d) / Z, rel=1e-10, abs=1e-15)
 
 
 def test_bf16_widening_matches_torch():

@@ -28,6 +28,7 @@ MAX_SUPPRESS = 64
 MAX_SORT_L = 16384
 FUSED_SORT_CAP = 1024
 FLAG_INPUTS_READY = 1
+FLAG_TEST_DROP_COPY = 2   # tests only: see DLLM_FLAG_TEST_DROP_COPY
 
 EXPORTS = (
     "dllm_status_string", "dllm_version", "dllm_token_stats_workspace_size", "dllm_token_stats",
@@ -36,6 +37,7 @@ EXPORTS = (
     "dllm_workspace_fault", "dllm_token_stats_noalloc", "dllm_token_stats_ex", "dllm_linear_temperature",
     "dllm_uniform_canvas", "dllm_renoise", "dllm_stable_confident_stop", "dllm_block_causal_mask",
     "dllm_lm_head_stats_workspace_size", "dllm_lm_head_stats", "dllm_uniform_update", "dllm_commit_step_host",
+    "dllm_noalloc_fault",
 )
 
 
@@ -88,6 +90,7 @@ def _load() -> C.CDLL:
     lib.dllm_block_ranges.argtypes = [i64, i64, i64, C.c_int, P, i64, P]
     lib.dllm_workspace_fault.argtypes = [P, P, C.POINTER(C.c_int32)]
     lib.dllm_token_stats_noalloc.argtypes = stats_args + [P]
+    lib.dllm_noalloc_fault.argtypes = [P, C.POINTER(C.c_int32)]
     lib.dllm_token_stats_ex.argtypes = stats_args[:10] + [C.POINTER(StatsEx)] + stats_args[10:] + [P, sz, P]
     lib.dllm_linear_temperature.argtypes = [i32, i32, f32, f32, C.POINTER(C.c_float)]
     lib.dllm_uniform_canvas.argtypes = [i64, i64, i64, u64, P, i64, P]
@@ -439,7 +442,7 @@ def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, su
                 gamma: float = 0.0, edit: bool = False, tau_edit: float = 1.0, canvas=None, canvas_offset: int = 0,
                 out=None, counts=None, ws=None, stream=None, inputs_ready: bool = False,
                 logit_scale: float = 1.0, margin: Optional[torch.Tensor] = None,
-                argmax: Optional[torch.Tensor] = None):
+                argmax: Optional[torch.Tensor] = None, _test_flags: int = 0):
     """Fused statistics pass + commit rule (+ edit rule and canvas update) in one launch.
 
     ``logit_scale``, ``margin`` and ``argmax`` (preallocated (B, L) float32 /
@@ -472,6 +475,7 @@ def commit_step(logits, *, rule: int, temperature: float = 0.0, key: int = 0, su
     ex, _, _ = _stats_ex((B, L), dev, logit_scale, margin, argmax)
     p = _commit_params(rule, strict, tau, factor, gamma, k, cand, mask_id, edit, tau_edit, commit, edit_mask, canvas,
                        canvas_offset, counts, inputs_ready, ex)
+    p.flags |= int(_test_flags)
     sup = (C.c_int32 * max(1, len(suppress_ids)))(*[int(v) for v in suppress_ids])
     if ws is None:
         ws = workspace(B, L, V, dt, dev, stream)
@@ -549,11 +553,26 @@ def commit_step_host(host_logits: torch.Tensor, **kw):
     return HostStep(host_logits, **kw)()
 
 
+def _on_current_device(device: torch.device, current: int, stream_device=None) -> None:
+    """The allocation-free entry takes its scratch array, the device's launch
+    limits and (without a stream) the default stream from the current CUDA
+    device, so its tensors (and a given stream) must be on that device."""
+    if device.type != "cuda" or device.index != current:
+        raise ValueError(f"tensors on {device} but the current CUDA device is cuda:{current}: "
+                         "make their device current first")
+    if stream_device is not None and stream_device != current:
+        raise ValueError(f"stream on cuda:{stream_device} but the current CUDA device is cuda:{current}")
+
+
 def token_stats_noalloc(logits: torch.Tensor, temperature: float = 0.0, key: int = 0,
                         suppress_ids: Sequence[int] = (), out=None, stream=None):
     """token_stats without a workspace: the library's fixed scratch array is
-    used instead (see dllm_token_stats_noalloc); calls must not overlap."""
+    used instead (see dllm_token_stats_noalloc); calls must not overlap.  The
+    tensors must be on the current CUDA device.  A kernel fault of the call
+    is read with noalloc_fault() before the next call."""
     _need_cuda(logits)
+    _on_current_device(logits.device, torch.cuda.current_device(),
+                       None if stream is None else stream.device.index)
     B, L, V, stride = _logits_view(logits)
     dt = _dtype_code(logits)
     shape = logits.shape[:-1]
@@ -568,6 +587,15 @@ def token_stats_noalloc(logits: torch.Tensor, temperature: float = 0.0, key: int
                                          int(key) & (2**64 - 1), sup, len(suppress_ids), _ptr(x0), _ptr(prob),
                                          _ptr(ent), _stream(stream)), "dllm_token_stats_noalloc")
     return x0, prob, ent
+
+
+def noalloc_fault(stream=None) -> int:
+    """The fault code the last token_stats_noalloc call on the current device
+    left in the library's array (0: none); synchronises the stream and clears
+    the code."""
+    f = C.c_int32(0)
+    _check(_lib.dllm_noalloc_fault(_stream(stream), C.byref(f)), "dllm_noalloc_fault")
+    return f.value
 
 
 def workspace_fault(ws: torch.Tensor, stream=None) -> int:

@@ -206,7 +206,9 @@ dllm_status check_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L,
   if (dt != DLLM_F32 && dt != DLLM_BF16) return DLLM_ERR_INVALID_ARGUMENT;
   // the logits' byte extent T * row_stride * size must be representable
   if (checked_mul(checked_mul(checked_mul(B, L), row_stride), 4) < 0) return DLLM_ERR_INVALID_ARGUMENT;
-  if (!(temperature >= 0.0f) || std::isinf(temperature)) return DLLM_ERR_INVALID_ARGUMENT;
+  // (0, 2^64]: the streaming pass reads NaN as -2^100, and at these
+  // temperatures no noise lifts such an entry above a real logit's score.
+  if (!(temperature >= 0.0f) || !(temperature <= 0x1p+64f)) return DLLM_ERR_INVALID_ARGUMENT;
   if (n_sup < 0 || (n_sup > 0 && !sup)) return DLLM_ERR_INVALID_ARGUMENT;
   if (n_sup > DLLM_MAX_SUPPRESS) return DLLM_ERR_UNSUPPORTED;
   sorted_sup.assign(sup, sup + n_sup);
@@ -256,7 +258,7 @@ dllm_status resolve_ex(const dllm_stats_ex* ex, StatsOpts& o) {
 dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
                       float temperature, uint64_t key, const std::vector<int32_t>& sup, int32_t* x0, float* prob,
                       float* entropy, const RuleArgs* rule, void* ws, size_t ws_bytes, cudaStream_t s,
-                      bool early = false, const StatsOpts& opt = StatsOpts()) {
+                      bool early = false, const StatsOpts& opt = StatsOpts(), bool test_drop = false) {
   const DeviceInfo* d = device_info();
   if (!d) return DLLM_ERR_CUDA;
   const bool bf16 = dt == DLLM_BF16, gumbel = temperature > 0.0f;
@@ -278,6 +280,7 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   p.logits = static_cast<const uint8_t*>(logits);
   p.cluster = pl.cluster;
   p.early = early ? 1 : 0;
+  p.test_drop = test_drop ? 1 : 0;
   p.row_bytes = row_stride * es;
   p.T = T;
   p.V = V;
@@ -291,7 +294,6 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   p.stages = pl.stages;
   p.temperature = temperature;
   p.scale = opt.scale;
-  p.cs = opt.scale * kLog2e;
   p.keys = philox_schedule(key);
   p.n_sup = static_cast<int32_t>(sup.size());
   for (size_t i = 0; i < sup.size(); ++i) p.sup[i] = sup[i];
@@ -417,6 +419,7 @@ struct CommitCall {
   RuleArgs a{};
   StatsOpts opt;
   bool early = false;
+  bool test_drop = false;
 };
 
 dllm_status commit_check(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V, int64_t row_stride,
@@ -462,9 +465,11 @@ dllm_status commit_check(const void* logits, dllm_dtype dt, int64_t B, int64_t L
   a.canvas_offset = cp->canvas_offset;
   a.counts = cp->counts;
   a.L = L;
-  if (cp->flags & ~static_cast<int32_t>(DLLM_FLAG_INPUTS_READY)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (cp->flags & ~static_cast<int32_t>(DLLM_FLAG_INPUTS_READY | DLLM_FLAG_TEST_DROP_COPY))
+    return DLLM_ERR_INVALID_ARGUMENT;
   if (resolve_ex(cp->ex, c.opt) != DLLM_OK) return DLLM_ERR_INVALID_ARGUMENT;
   c.early = (cp->flags & DLLM_FLAG_INPUTS_READY) != 0;
+  c.test_drop = (cp->flags & DLLM_FLAG_TEST_DROP_COPY) != 0;
   return DLLM_OK;
 }
 
@@ -707,7 +712,7 @@ dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64
                                       entropy, cp, c);
   if (st != DLLM_OK || B * L == 0) return st;
   return run_stats(logits, dt, B, L, V, row_stride, temperature, key, c.sup, x0, prob, entropy, &c.a, workspace,
-                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream), c.early, c.opt);
+                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream), c.early, c.opt, c.test_drop);
 }
 
 dllm_status dllm_commit_step_host(const void* host_logits, void* dev_logits, dllm_dtype dt, int64_t B, int64_t L,
@@ -763,6 +768,20 @@ dllm_status dllm_token_stats_noalloc(const void* logits, dllm_dtype dt, int64_t 
   if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) return DLLM_ERR_CUDA;
   return run_stats(logits, dt, B, L, V, row_stride, temperature, key, sup, x0, prob, entropy, nullptr, scratch,
                    DLLM_NOALLOC_SCRATCH_BYTES, s);
+}
+
+dllm_status dllm_noalloc_fault(dllm_stream_t stream, int32_t* fault) {
+  if (!fault) return DLLM_ERR_INVALID_ARGUMENT;
+  cudaError_t err = cudaSuccess;
+  void* scratch = noalloc_scratch(&err);
+  if (!scratch) return DLLM_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return DLLM_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DLLM_ERR_CUDA;
+  if (v != 0 && cudaMemsetAsync(scratch, 0, sizeof(int32_t), s) != cudaSuccess) return DLLM_ERR_CUDA;
+  *fault = v;
+  return DLLM_OK;
 }
 
 dllm_status dllm_workspace_fault(void* workspace, dllm_stream_t stream, int32_t* fault) {

@@ -185,10 +185,16 @@ __device__ __forceinline__ long long fixed_bound(float bound) {
   return __float2ll_rz(fminf(bound, 0x1p+22f) * 0x1p+40f);
 }
 
-constexpr float kSentinel = -0x1p+100f;   // NaN and values <= -2^100 become this
-constexpr float kAbsent = -0x1p+120f;     // suppressed ids become this (no mass, never chosen)
+// The streaming statistics read NaN and values <= -2^100 as this sentinel and
+// clamp values above 2^100 to 2^100; in every row they finish themselves
+// (maximum within about 1.8e8 of zero) that reading equals the plain softmax,
+// and other rows are recomputed from the logits as they are.
+constexpr float kSentinel = -0x1p+100f;
+// Suppressed ids become this (no mass, never chosen).  Its product with the
+// largest exponent scale (256 log2 e) stays finite, so 2^y y is 0, not NaN.
+constexpr float kAbsent = -0x1p+110f;
 constexpr uint32_t kSentinelBf16x2 = 0xF180F180u;  // two bf16 -2^100
-constexpr uint32_t kAbsentBf16 = 0xFB80u;           // bf16 -2^120
+constexpr uint32_t kAbsentBf16 = 0xF680u;           // bf16 -2^110
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

@@ -356,8 +356,8 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
 #pragma unroll
         for (int j = 0; j < 32; ++j) cm[j & 3] = fmaxf(cm[j & 3], z[j]);
         const float cmax = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
-        if (cmax > acc.m) {  // rescale to the new running max
-          const float d = (acc.m - cmax) * kLog2e;
+        if (cmax > acc.m) {  // rescale to the new running max (shift between exponent references)
+          const float d = ref_shift(exp_ref(acc.m), exp_ref(cmax));
           const float f = ex2_approx(d);
           acc.S2 = f * fmaf(d, acc.Z, acc.S2);
           acc.Z *= f;
@@ -368,15 +368,16 @@ __global__ void __launch_bounds__(kLhThreads, 1) lm_head_kernel(const __grid_con
           acc.idx = static_cast<int32_t>(v0 + (__ffs(eq) - 1));  // strictly larger than every earlier value
         }
         // The chunk's sums in packed pairs on two independent chains, then
-        // added to the row's: y = z log2 e - m log2 e, sum 2^y, sum 2^y y.
+        // added to the row's: y = z log2 e - ref, ref = RU(m log2 e), sum 2^y,
+        // sum 2^y y.
         {
-          const float nmc = -acc.m * kLog2e;
-          const uint64_t nmc2 = pack2(nmc, nmc), cs2 = pack2(kLog2e, kLog2e);
+          const float nmc = -exp_ref(acc.m);
+          const uint64_t nmc2 = pack2(nmc, nmc), l2e2 = pack2(kLog2e, kLog2e);
           uint64_t Za = 0, Sa = 0, Zb = 0, Sb = 0;
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
-            acc_pair2(Za, Sa, z[j], z[j + 1], nmc2, cs2);
-            acc_pair2(Zb, Sb, z[j + 2], z[j + 3], nmc2, cs2);
+            acc_pair2<false>(Za, Sa, z[j], z[j + 1], nmc2, l2e2, 0);
+            acc_pair2<false>(Zb, Sb, z[j + 2], z[j + 3], nmc2, l2e2, 0);
           }
           float z0, z1, s0, s1;
           unpack2(add2(Za, Zb), z0, z1);
@@ -447,8 +448,8 @@ __global__ void __launch_bounds__(256) lm_head_finish_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
   if (token >= sp.T) return;
   Partial tot = empty_partial();
-  for (int k = lane; k < P; k += 32) part_combine<MODE>(tot, load_partial(partials + token * P + k), 1.0f, kLog2e);
-  tot = warp_combine<MODE>(tot, 1.0f, kLog2e);
+  for (int k = lane; k < P; k += 32) part_combine<MODE>(tot, load_partial(partials + token * P + k), 1.0f);
+  tot = warp_combine<MODE>(tot, 1.0f);
   if (lane == 0) finish_row(sp, token, row_out<MODE>(sp, tot), RowPre());
 }
 
@@ -562,7 +563,7 @@ dllm_status dllm_lm_head_stats(const void* hidden, int64_t T, int64_t d, int64_t
                                float* entropy, float* logits, int64_t logits_stride, void* workspace,
                                size_t workspace_bytes, dllm_stream_t stream) {
   if (T < 0 || V < 1 || V > INT32_MAX || d < 1) return DLLM_ERR_INVALID_ARGUMENT;
-  if (!(temperature >= 0.0f) || std::isinf(temperature)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!(temperature >= 0.0f) || !(temperature <= 0x1p+64f)) return DLLM_ERR_INVALID_ARGUMENT;
   if (hidden_stride < d || weight_stride < d || (logits && logits_stride < V)) return DLLM_ERR_INVALID_ARGUMENT;
   if (n_suppress < 0 || (n_suppress > 0 && !suppress_ids)) return DLLM_ERR_INVALID_ARGUMENT;
   if (n_suppress > DLLM_MAX_SUPPRESS) return DLLM_ERR_UNSUPPORTED;
@@ -644,7 +645,6 @@ dllm_status dllm_lm_head_stats(const void* hidden, int64_t T, int64_t d, int64_t
   sp.V = V;
   sp.L = T;
   sp.scale = 1.0f;
-  sp.cs = kLog2e;
   sp.ln_veff = static_cast<float>(std::log(static_cast<double>(V - static_cast<int64_t>(sup.size()))));
   sp.x0 = x0;
   sp.prob = prob;

@@ -55,6 +55,7 @@ struct StatsParams {
   const uint8_t* logits;
   int32_t cluster;          // CTAs per row in the cluster kernel (0: persistent kernel)
   int32_t early;            // logits are ready before the previous kernel ends: load before the grid dependency
+  int32_t test_drop;        // test only: CTA 0 does not issue its first unit's copy (its consumers' wait runs out)
   int64_t row_bytes;        // row stride in bytes (multiple of 16)
   int64_t T, V, L;
   int64_t nvec;             // full 16-byte vectors per row
@@ -65,7 +66,6 @@ struct StatsParams {
   int32_t stages;           // ring stages
   float temperature;
   float scale;              // logit scale s: every statistic is of z' = fp32(z s)
-  float cs;                 // fp32(s log2 e): the exponent scale of the sums (log2 e when s = 1)
   PhiloxSchedule keys;      // Philox round keys of the caller's key
   int32_t n_sup;
   int32_t sup[DLLM_MAX_SUPPRESS];  // sorted, distinct

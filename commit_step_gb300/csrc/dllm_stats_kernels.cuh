@@ -13,11 +13,15 @@
 //     cp.async.bulk (TMA bulk copies), one mbarrier per stage; eight consumer
 //     warps read each unit from shared memory.
 //   * Each consumer thread keeps an online softmax state of the scaled logits
-//     z' = z s (s = 1 unless the caller scales them): running max m of the
-//     raw logits, Z = sum 2^y and S2 = sum 2^y y with y = (z - m) c,
-//     c = s log2 e (packed fp32x2 accumulators), rescaled when the max grows;
-//     entropy = ln Z - S2 ln 2 / Z.  Decisions (argmax, ties, Gumbel scores)
-//     compare the scaled values fp32(z s) themselves.
+//     z' = fp32(z s) (s = 1 unless the caller scales them): running max m of
+//     the raw logits, Z = sum 2^y and S2 = sum 2^y y with y = z' log2 e - ref
+//     and ref = RU(m' log2 e), the product rounded up (packed fp32x2
+//     accumulators, one fused multiply-add per pair), rescaled when the max
+//     grows; entropy = ln Z - S2 ln 2 / Z.  Decisions (argmax, ties, Gumbel
+//     scores) compare the scaled values z' themselves.
+//   * Rows whose maximum the streaming pass cannot resolve exactly (|ref| >=
+//     2^28, or no logit above the no-mass sentinel -2^100) are recomputed by
+//     one warp from the logits as they are (exotic_row).
 //     The first index of the max is located once per row, from the first
 //     vector that holds the thread's max; the largest value outside that
 //     element (the runner-up of the margin confidence) comes with it.
@@ -49,7 +53,7 @@ struct Acc {
   float m;          // running max of the raw logits
   uint64_t Z2;      // two partial sums of 2^y
   uint64_t S2;      // two partial sums of 2^y y
-  float negm;
+  float nref;       // -ref, ref = RU(m' log2 e): minus the exponent reference of m
   int32_t idx;      // first index of m among the tail elements (greedy)
   float vm;         // max of z' over the thread's full vectors (greedy)
   int32_t vv;       // first id of the first vector holding vm, -1 if none
@@ -68,7 +72,10 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   return d;
 }
 
-constexpr float kMInit = -0x1p+121f;  // below every sanitized value
+// Below every sanitized value (kAbsent is -2^110), and finite after scaling
+// by the largest logit scale (256): -2^120.
+constexpr float kMInit = -0x1p+112f;
+constexpr float kExoticRef = 0x1p+28f;  // rows whose |ref| reaches this take exotic_row
 constexpr float kTopClamp = 0x1p+100f;
 constexpr uint32_t kTopBf16x2 = 0x71807180u;  // two bf16 2^100
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -77,7 +84,7 @@ __device__ __forceinline__ void acc_init(Acc& a) {
   a.m = kMInit;
   a.Z2 = 0;
   a.S2 = 0;
-  a.negm = -kMInit;
+  a.nref = 0x1.fffffep+127f;   // the reference of "no max yet": every rescale from it gives 0
   a.idx = 0x7FFFFFFF;
   a.vm = kMInit;
   a.vv = -1;
@@ -88,16 +95,38 @@ __device__ __forceinline__ void acc_init(Acc& a) {
   a.best_z = 0.0f;
 }
 
+// The exponent reference of a running max m' (a scaled logit): ref =
+// RU(m' log2 e), the product rounded up.  A term is 2^(z' log2 e - ref) with
+// z' log2 e - ref formed exactly and rounded once (one fused multiply-add),
+// so every term is at most 1 and the sums stay finite for any logit; the
+// max's own term is 2^(m' log2 e - ref), in (2^-ulp(ref), 1].  Rescales and
+// combines shift by differences of these references, so sums built against
+// different maxima agree on their scale.
+__device__ __forceinline__ float exp_ref(float ms) { return __fmul_ru(ms, kLog2e); }
+
+// z' = fp32(z s) in the scaled modes, z itself otherwise.
+template <bool SCALED>
+__device__ __forceinline__ float scaled(float z, float s) { return SCALED ? __fmul_rn(z, s) : z; }
+
+// The shift from reference `from` to reference `to` (>= from), clamped to
+// [-256, 0] (2^-256 is 0 in fp32): the clamp keeps it finite when a
+// reference sits at the end of the fp32 range.
+__device__ __forceinline__ float ref_shift(float from, float to) {
+  return fminf(fmaxf(from - to, -256.0f), 0.0f);
+}
+
 // Raise the running max to mnew (> a.m): Z' = f Z, S2' = f (S2 + d Z),
-// f = 2^d, d = (m - mnew) cs, cs = s log2 e.
-__device__ __forceinline__ void acc_rescale(Acc& a, float mnew, float cs) {
-  const float d = (a.m - mnew) * cs;
+// f = 2^d, d = ref(m) - ref(mnew).
+template <bool SCALED>
+__device__ __forceinline__ void acc_rescale(Acc& a, float mnew, float s) {
+  const float rn = exp_ref(scaled<SCALED>(mnew, s));
+  const float d = ref_shift(-a.nref, rn);
   const float c = ex2_approx(d);
   const uint64_t d2 = pack2(d, d), c2 = pack2(c, c);
   a.S2 = mul2(c2, fma2(d2, a.Z2, a.S2));
   a.Z2 = mul2(a.Z2, c2);
   a.m = mnew;
-  a.negm = -mnew;
+  a.nref = -rn;
 }
 
 __device__ __forceinline__ float sanitize(float z) {
@@ -117,13 +146,15 @@ __device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Adds two sanitized logits (<= m) to the sums (Z2, S2): y = z cs - m cs in
-// one fused multiply-add per pair (cs = s log2 e; nmc2 holds fp32(-m cs)
-// twice), 2^y and 2^y y.  The rounding of m cs shifts every y of the row's
-// current running max alike, which cancels in prob and entropy.
-__device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, float z1, uint64_t nmc2,
-                                          uint64_t cs2) {
-  const uint64_t y2 = fma2(pack2(z0, z1), cs2, nmc2);
+// Adds two sanitized logits (<= m) to the sums (Z2, S2): z' = fp32(z s) in
+// the scaled modes (one packed multiply; s2 holds s twice), y = z' log2 e -
+// ref in one fused multiply-add per pair (l2e2 holds log2 e twice, nref2
+// holds -ref twice, ref = exp_ref(m')), 2^y and 2^y y.
+template <bool SCALED>
+__device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, float z1, uint64_t nref2,
+                                          uint64_t l2e2, uint64_t s2) {
+  const uint64_t zz = SCALED ? mul2(pack2(z0, z1), s2) : pack2(z0, z1);
+  const uint64_t y2 = fma2(zz, l2e2, nref2);
   float y0, y1;
   unpack2(y2, y0, y1);
   const uint64_t e2 = pack2(ex2_approx(y0), ex2_approx(y1));
@@ -136,15 +167,15 @@ __device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, 
 // The runner-up of the union is the larger of the winner's runner-up and the
 // loser's (scaled) max.
 template <int MODE>
-__device__ __forceinline__ void part_combine(Partial& a, const Partial& b, float s, float cs) {
+__device__ __forceinline__ void part_combine(Partial& a, const Partial& b, float s) {
   constexpr bool GUMBEL = mode_sample(MODE), RUNNER = mode_runner(MODE), SCALED = mode_scaled(MODE);
-  if (!SCALED) cs = kLog2e;
   const float m = fmaxf(a.m, b.m);
-  const float da = (a.m - m) * cs, db = (b.m - m) * cs;
+  const float sa = scaled<SCALED>(a.m, s), sb = scaled<SCALED>(b.m, s);
+  const float ra = exp_ref(sa), rb = exp_ref(sb), r = fmaxf(ra, rb);   // r = exp_ref(m')
+  const float da = ref_shift(ra, r), db = ref_shift(rb, r);
   const float ca = ex2_approx(da), cb = ex2_approx(db);
   const float Z = ca * a.Z + cb * b.Z;
   const float S2 = ca * fmaf(da, a.Z, a.S2) + cb * fmaf(db, b.Z, b.S2);
-  const float sa = SCALED ? __fmul_rn(a.m, s) : a.m, sb = SCALED ? __fmul_rn(b.m, s) : b.m;
   const bool b_wins = sb > sa || (sb == sa && b.idx < a.idx);
   if (RUNNER) a.m2 = b_wins ? fmaxf(b.m2, sa) : fmaxf(a.m2, sb);
   a.m = m;
@@ -214,11 +245,11 @@ __device__ __forceinline__ Partial shfl_partial(const Partial& p, int o) {
 }
 
 template <int MODE>
-__device__ __forceinline__ Partial warp_combine(Partial part, float s, float cs) {
+__device__ __forceinline__ Partial warp_combine(Partial part, float s) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const Partial q = shfl_partial<MODE>(part, o);
-    part_combine<MODE>(part, q, s, cs);
+    part_combine<MODE>(part, q, s);
   }
   return part;
 }
@@ -292,29 +323,184 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long lon
   return old;
 }
 
-// x0, prob and entropy of one row from its full reduction.
+// x0, prob and entropy of one row from its full reduction.  exotic: the
+// row's maximum is outside what the streaming pass resolves (see exotic_row).
 struct RowOut {
   int32_t x0, argmax;
   float prob, H, margin;
+  bool exotic;
 };
 
-// The margin's runner-up is the largest z' without x0: the row's runner-up
-// when x0 is the argmax, else the max itself.
+// prob = x0's term over Z (its exponent formed exactly as the sums formed
+// it); entropy = ln Z - S2 ln 2 / Z clamped to [0, ln |A|].  The margin's
+// runner-up is the largest z' without x0: the row's runner-up when x0 is the
+// argmax, else the max itself.
 template <int MODE>
 __device__ __forceinline__ RowOut row_out(const StatsParams& p, const Partial& r) {
   constexpr bool GUMBEL = mode_sample(MODE), RUNNER = mode_runner(MODE), SCALED = mode_scaled(MODE);
   RowOut o;
   o.x0 = GUMBEL ? r.best_v : r.idx;
   o.argmax = r.idx;
-  const float ms = SCALED ? __fmul_rn(r.m, p.scale) : r.m;   // the scaled max
-  const float zx = GUMBEL ? r.best_z : ms;
-  o.prob = ex2_approx((zx - ms) * kLog2e) / r.Z;
+  const float ms = scaled<SCALED>(r.m, p.scale);                // the scaled max m'
+  const float ref = exp_ref(ms);
+  o.exotic = !(fabsf(ref) < kExoticRef);
+  const float ytop = fmaf(ms, kLog2e, -ref);                      // the max's own exponent
+  // best_z is the raw logit of x0: its exponent as the sums formed it
+  const float yx = GUMBEL ? fmaf(scaled<SCALED>(r.best_z, p.scale), kLog2e, -ref) : ytop;
+  o.prob = ex2_approx(yx) / r.Z;
   const float H = logf(r.Z) - r.S2 * kLn2 / r.Z;
   o.H = fminf(fmaxf(H, 0.0f), p.ln_veff);
   o.margin = 0.0f;
   if (RUNNER) {
-    const float r2 = (!GUMBEL || r.best_v == r.idx) ? r.m2 : ms;
-    o.margin = o.prob - ex2_approx((r2 - ms) * kLog2e) / r.Z;
+    const float r2 = (!GUMBEL || r.best_v == r.idx) ? r.m2 : ms;   // a scaled logit
+    o.margin = o.prob - ex2_approx(fmaf(r2, kLog2e, -ref)) / r.Z;
+  }
+  return o;
+}
+
+// The statistics of a row whose maximum the streaming pass does not resolve
+// exactly: |RU(m' log2 e)| >= 2^28 (logits beyond about 1.8e8 / s in magnitude,
+// +inf included, where the fp32 spacing of the reference exceeds 16), or no
+// logit above the no-mass sentinel (NaN, -inf or finite values <= -2^100
+// only).  One warp recomputes the row from the logits as they are, reading
+// them again: a NaN has no mass, +inf entries share the mass equally, every
+// finite logit takes the ordinary softmax ("dLLM block decoding", What
+// mlx-arsenal ships: token_stats is NaN-safe), and a row with no mass at all
+// gives the uniform limit.  Model output never holds such rows; this path
+// costs two or three extra reads of the row by one warp.
+template <bool BF16, int MODE>
+__device__ __noinline__ RowOut exotic_row(const StatsParams& p, int64_t row, int lane) {
+  constexpr bool GUMBEL = mode_sample(MODE), RUNNER = mode_runner(MODE), SCALED = mode_scaled(MODE);
+  constexpr int32_t kNone = 0x7FFFFFFF;
+  const float s = SCALED ? p.scale : 1.0f;
+  const float t = p.temperature;
+  const uint8_t* rowp = p.logits + row * p.row_bytes;
+  const int32_t V = static_cast<int32_t>(p.V);
+  const int32_t n_sup = p.n_sup;
+  // z' of id v: NaN -> -inf, else fp32(z s)
+  auto zl = [&](int32_t v) -> float {
+    float z;
+    if (BF16)
+      z = __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t*>(rowp) + v)) << 16);
+    else
+      z = __ldg(reinterpret_cast<const float*>(rowp) + v);
+    if (isnan(z)) return kNegInf;
+    return SCALED ? __fmul_rn(z, s) : z;
+  };
+  // Walks this lane's ids v = lane, lane + 32, ... of the token set (the
+  // sorted suppress list is stepped through alongside, one read per id it holds).
+  auto for_each = [&](auto&& fn) {
+    int32_t si = 0;
+    int32_t next = n_sup > 0 ? p.sup[0] : kNone;
+    for (int64_t vv = lane; vv < V; vv += 32) {
+      const int32_t v = static_cast<int32_t>(vv);
+      while (next < v) next = (++si < n_sup) ? p.sup[si] : kNone;
+      if (next == v) continue;
+      fn(v, zl(v));
+    }
+  };
+  // Pass 1: the max M of z' over the token set and its first id (with no
+  // mass anywhere, M = -inf and the id is the set's first).
+  float M = kNegInf;
+  int32_t am = kNone;
+  for_each([&](int32_t v, float z) {
+    if (am == kNone || z > M) {
+      M = z;
+      am = v;
+    }
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float M2 = __shfl_xor_sync(0xFFFFFFFFu, M, o);
+    const int32_t a2 = __shfl_xor_sync(0xFFFFFFFFu, am, o);
+    if (a2 != kNone && (am == kNone || M2 > M || (M2 == M && a2 < am))) {
+      M = M2;
+      am = a2;
+    }
+  }
+  const float veff = static_cast<float>(p.V - n_sup);
+  RowOut o;
+  o.exotic = false;
+  o.argmax = am;
+  o.x0 = am;
+  o.margin = 0.0f;
+  if (M == kNegInf) {  // the uniform limit; every Gumbel score is -inf, so x0 is the first id too
+    o.prob = 1.0f / veff;
+    o.H = p.ln_veff;
+    if (RUNNER) o.margin = veff >= 2.0f ? 0.0f : o.prob;
+    return o;
+  }
+  if (M == -kNegInf) {  // the +inf entries share the mass; the first of them is x0 and has the top score
+    int32_t n_inf = 0;
+    for_each([&](int32_t, float z) { n_inf += z == M ? 1 : 0; });
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) n_inf += __shfl_xor_sync(0xFFFFFFFFu, n_inf, k);
+    o.prob = 1.0f / static_cast<float>(n_inf);
+    o.H = fminf(static_cast<float>(log(static_cast<double>(n_inf))), p.ln_veff);
+    if (RUNNER) o.margin = n_inf >= 2 ? 0.0f : o.prob;
+    return o;
+  }
+  // Finite M.  Pass 2: Z = sum 2^y, S2 = sum 2^y y, y = (z' - M) log2 e
+  // (accumulated in double), and the Gumbel-max sample: an id can beat the
+  // argmax's score only if z' + 17 t >= M - 3 t (every noise value g of the
+  // sampler lies in [-3, 17]), so only those ids get a score.
+  const uint32_t row_lo = static_cast<uint32_t>(row);
+  const uint32_t row_hi = static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32);
+  const float floor_s = fmaf(t, -3.0f, M);
+  double Z = 0.0, S2 = 0.0;
+  float bs = kNegInf, bz = 0.0f;
+  int32_t bv = kNone;
+  for_each([&](int32_t v, float z) {
+    const float y = (z - M) * kLog2e;
+    if (y > -200.0f) {
+      const float e = ex2_approx(y);
+      Z += static_cast<double>(e);
+      S2 += static_cast<double>(e) * static_cast<double>(y);
+    }
+    if (GUMBEL && fmaf(t, 17.0f, z) >= floor_s) {
+      const uint4 w4 = philox4x32_10(static_cast<uint32_t>(v >> 2), row_lo, row_hi, 0u, p.keys);
+      const int k = v & 3;
+      const uint32_t word = k == 0 ? w4.x : (k == 1 ? w4.y : (k == 2 ? w4.z : w4.w));
+      const float sc = gumbel_score(z, t, word);
+      if (bv == kNone || sc > bs) {   // ids rise in a lane: a strict > keeps the first of equal scores
+        bs = sc;
+        bv = v;
+        bz = z;
+      }
+    }
+  });
+#pragma unroll
+  for (int k = 16; k > 0; k >>= 1) {
+    Z += __shfl_xor_sync(0xFFFFFFFFu, Z, k);
+    S2 += __shfl_xor_sync(0xFFFFFFFFu, S2, k);
+    if (GUMBEL) {
+      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, bs, k);
+      const int32_t v2 = __shfl_xor_sync(0xFFFFFFFFu, bv, k);
+      const float z2 = __shfl_xor_sync(0xFFFFFFFFu, bz, k);
+      if (v2 != kNone && (bv == kNone || s2 > bs || (s2 == bs && v2 < bv))) {
+        bs = s2;
+        bv = v2;
+        bz = z2;
+      }
+    }
+  }
+  if (GUMBEL) o.x0 = bv;
+  const float zx = GUMBEL ? bz : M;
+  o.prob = static_cast<float>(static_cast<double>(ex2_approx((zx - M) * kLog2e)) / Z);
+  const double H = log(Z) - S2 * 0.6931471805599453 / Z;
+  o.H = fminf(fmaxf(static_cast<float>(H), 0.0f), p.ln_veff);
+  if (RUNNER) {
+    // Pass 3: the runner-up, the largest z' over the token set without x0.
+    float r2 = kNegInf;
+    const int32_t x0 = o.x0;
+    for_each([&](int32_t v, float z) {
+      if (v != x0) r2 = fmaxf(r2, z);
+    });
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) r2 = fmaxf(r2, __shfl_xor_sync(0xFFFFFFFFu, r2, k));
+    const float y2 = (r2 - M) * kLog2e;
+    const double p2 = y2 > -200.0f ? static_cast<double>(ex2_approx(y2)) / Z : 0.0;
+    o.margin = static_cast<float>(static_cast<double>(o.prob) - p2);
   }
   return o;
 }
@@ -417,7 +603,7 @@ struct GumbelWords {
 struct GumbelBest {
   float s;
   int32_t v;
-  float z;
+  float z;   // the raw (unscaled) logit of v
 };
 
 // Exact Gumbel scores of the elements of one vector that can still beat
@@ -431,7 +617,8 @@ __device__ __noinline__ GumbelBest gumbel_exact(GumbelBest best, VecWords vw, Gu
 #pragma unroll 1
   for (int e = 0; e < EPV; ++e) {
     const uint32_t word = vw.w[BF16 ? (e >> 1) : e];
-    const float z = __fmul_rn(BF16 ? ((e & 1) ? bf16hi(word) : bf16lo(word)) : __uint_as_float(word), s);
+    const float zr = BF16 ? ((e & 1) ? bf16hi(word) : bf16lo(word)) : __uint_as_float(word);
+    const float z = __fmul_rn(zr, s);
     const uint32_t re = r.w[e];
     const float w1 = __fsub_rn(1.0f, uniform_from_bits(re));
     const float bound = fmaf(t_ln2, -lg2_approx(w1), z + fmaf(fabsf(z), 1e-6f, 1e-3f));
@@ -440,7 +627,7 @@ __device__ __noinline__ GumbelBest gumbel_exact(GumbelBest best, VecWords vw, Gu
     if (sc > best.s) {
       best.s = sc;
       best.v = v0 + e;
-      best.z = z;
+      best.z = zr;   // the raw logit
     }
   }
   return best;
@@ -460,8 +647,8 @@ struct Consumer {
   int tid, warp, lane;
   float t, t_ln2;
   float s;          // logit scale
-  float cs;         // s log2 e
-  uint64_t cs2;     // (cs, cs)
+  uint64_t s2;      // (s, s)
+  uint64_t l2e2;    // (log2 e, log2 e)
   Acc acc;
   float warp_best;
 
@@ -473,8 +660,8 @@ struct Consumer {
     t = p.temperature;
     t_ln2 = t * kLn2;
     s = SCALED ? p.scale : 1.0f;
-    cs = p.cs;   // log2 e when unscaled; read from the parameters in every mode (it schedules better)
-    cs2 = pack2(cs, cs);
+    s2 = pack2(s, s);
+    l2e2 = pack2(kLog2e, kLog2e);
     reset();
   }
 
@@ -487,7 +674,7 @@ struct Consumer {
   }
 
   static constexpr int kVPT = 1024 / kConsumers;  // vectors per thread in the largest unit
-  static constexpr uint32_t kAbsentWord = BF16 ? 0xFB80FB80u : 0xFB800000u;  // -2^120 in every lane
+  static constexpr uint32_t kAbsentWord = BF16 ? 0xF680F680u : 0xF6800000u;  // -2^110 in every lane
 
   // Reduces one unit: nv (<= 1024) vectors in the ring stage at shared
   // address `base`, the first being vector v_unit of global row `row`.
@@ -585,24 +772,24 @@ struct Consumer {
     // Branch-free rescale to the new running max (factor 1 when it did not grow).
     {
       const float mnew = fmaxf(acc.m, umax);
-      const float d = (acc.m - mnew) * cs;
+      const float rn = exp_ref(scaled<SCALED>(mnew, s));
+      const float d = ref_shift(-acc.nref, rn);
       const float c = ex2_approx(d);
       const uint64_t d2 = pack2(d, d), c2 = pack2(c, c);
       acc.S2 = mul2(c2, fma2(d2, acc.Z2, acc.S2));
       acc.Z2 = mul2(acc.Z2, c2);
       acc.m = mnew;
-      acc.negm = -mnew;
+      acc.nref = -rn;
     }
-    const float nmc = acc.negm * cs;
-    const uint64_t nmc2 = pack2(nmc, nmc);
+    const uint64_t nmc2 = pack2(acc.nref, acc.nref);
     uint64_t Zb = 0, Sb = 0;
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
       if (!FULL && !valid[j]) continue;
 #pragma unroll
       for (int e = 0; e < EPV; e += 4) {
-        acc_pair2(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), nmc2, cs2);
-        acc_pair2(Zb, Sb, elem(w[j], e + 2), elem(w[j], e + 3), nmc2, cs2);
+        acc_pair2<SCALED>(acc.Z2, acc.S2, elem(w[j], e), elem(w[j], e + 1), nmc2, l2e2, s2);
+        acc_pair2<SCALED>(Zb, Sb, elem(w[j], e + 2), elem(w[j], e + 3), nmc2, l2e2, s2);
       }
     }
     acc.Z2 = add2(acc.Z2, Zb);
@@ -712,10 +899,10 @@ struct Consumer {
     for (int i = 0; i < p.n_sup; ++i)
       if (p.sup[i] == v) z = kAbsent;
     const float zs = SCALED ? __fmul_rn(z, s) : z;
-    if (z > acc.m) acc_rescale(acc, z, cs);
+    if (z > acc.m) acc_rescale<SCALED>(acc, z, s);
     acc.idx = static_cast<int32_t>(v);  // one tail element per thread
     acc.vm_tail = zs;
-    const float y = (z - acc.m) * cs;
+    const float y = fmaf(zs, kLog2e, acc.nref);
     const float e = ex2_approx(y);
     acc.Z2 = add2(acc.Z2, pack2(e, 0.0f));
     acc.S2 = fma2(pack2(e, 0.0f), pack2(y, 0.0f), acc.S2);
@@ -728,7 +915,7 @@ struct Consumer {
       if (sc > acc.best_s) {
         acc.best_s = sc;
         acc.best_v = static_cast<int32_t>(v);
-        acc.best_z = zs;
+        acc.best_z = z;   // the raw logit (prob forms its exponent as the sums did)
       }
     }
   }
@@ -773,7 +960,7 @@ struct Consumer {
 
   // The CTA's reduction of all consumer states; valid in thread 0.
   __device__ Partial cta_reduce() {
-    Partial part = warp_combine<MODE>(acc_to_partial<RUNNER>(acc), s, cs);
+    Partial part = warp_combine<MODE>(acc_to_partial<RUNNER>(acc), s);
     if (lane == 0) ctl.warp_part[warp] = part;
     named_sync(1, kConsumers);
     Partial r = empty_partial();
@@ -782,7 +969,7 @@ struct Consumer {
 #pragma unroll
       for (int o = kConsumerWarps / 2; o > 0; o >>= 1) {
         const Partial q = shfl_partial<MODE>(r, o);
-        part_combine<MODE>(r, q, s, cs);
+        part_combine<MODE>(r, q, s);
       }
     }
     return r;
@@ -817,9 +1004,11 @@ struct RingPos {
 // Producer: issues the bulk copies of this CTA's n units in order; next(src,
 // bytes) yields each unit's global address and size.  Returns when every
 // issued copy has landed (or, after a fault, when the drain deadline passes).
+// drop_first (tests only): the first unit's copy is not issued and its stage
+// not arrived on, so the consumers' bounded wait for it runs out.
 template <typename Next>
 __device__ void produce(const StatsParams& p, SharedCtl& ctl, uint32_t ring, uint32_t chunk_bytes, int64_t n,
-                        Next next) {
+                        Next next, bool drop_first = false) {
   volatile int32_t* abort_flag = &ctl.abort_flag;
   const int stages = p.stages;
   RingPos r;
@@ -838,7 +1027,9 @@ __device__ void produce(const StatsParams& p, SharedCtl& ctl, uint32_t ring, uin
     uint32_t bytes;
     next(src, bytes);
     const uint32_t bar = smem_addr(&ctl.full[r.slot]);
-    if (bytes > 0) {
+    if (i == 0 && drop_first) {
+      // nothing issued, nothing arrived: this stage never completes
+    } else if (bytes > 0) {
       mbar_arrive_expect_tx(bar, bytes);
       bulk_copy_g2s(ring + r.slot * chunk_bytes, src, bytes, bar);
     } else {
@@ -850,6 +1041,7 @@ __device__ void produce(const StatsParams& p, SharedCtl& ctl, uint32_t ring, uin
   // Drain: the last (up to `stages`) issued copies must land before exit.
   const long long t0 = clock64();
   for (int64_t i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+    if (i == 0 && drop_first) continue;   // never issued
     const int slot = static_cast<int>(i % stages);
     const uint32_t par = static_cast<uint32_t>((i / stages) & 1);
     while (!mbar_try_wait_sleep(smem_addr(&ctl.full[slot]), par, kSleepHintNs)) {
@@ -925,7 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
           puk = 0;
           ++prow;
         }
-      });
+      }, p.test_drop != 0 && blockIdx.x == 0);
     }
     return;
   }
@@ -975,17 +1167,26 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
         const int64_t cc = cb + lane;
         Partial q = empty_partial();
         if (cc <= c1) q = load_partial(p.partials + 2 * cc + ((cc == c0 && c0_tail) ? 1 : 0));
-        part_combine<MODE>(tot, q, p.scale, p.cs);
+        part_combine<MODE>(tot, q, p.scale);
       }
-      tot = warp_combine<MODE>(tot, p.scale, p.cs);
+      tot = warp_combine<MODE>(tot, p.scale);
       if (lane == 0) {
         p.row_count[row] = 0;
         ctl.result = tot;
       }
     }
-    if (tid == 0) {
-      ctl.flag2 = action != 0 ? finish_row(p, row, row_out<MODE>(p, ctl.result), RowPre()) : -1;
-      ctl.cta_best = float_key(kNegInf);  // the next row starts with no pruning floor
+    if (warp == 0) {
+      __syncwarp();   // ctl.result, when lane 0 of this warp wrote it
+      int32_t rule_b = -1;
+      if (action != 0) {
+        RowOut o = row_out<MODE>(p, ctl.result);
+        if (__shfl_sync(0xFFFFFFFFu, o.exotic ? 1 : 0, 0)) o = exotic_row<BF16, MODE>(p, row, lane);
+        if (lane == 0) rule_b = finish_row(p, row, o, RowPre());
+      }
+      if (lane == 0) {
+        ctl.flag2 = rule_b;
+        ctl.cta_best = float_key(kNegInf);  // the next row starts with no pruning floor
+      }
     }
     named_sync(1, kConsumers);
     con.rule_if_needed(ctl.flag2, rule_smem);
@@ -1054,7 +1255,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
         src = p.logits + row * p.row_bytes + pv * 16;
         bytes = static_cast<uint32_t>(nv) * 16u;
         pv += p.chunk_vec;
-      });
+      }, p.test_drop != 0 && blockIdx.x == 0);
     }
     __syncwarp();
     cluster_sync_all();  // partials published
@@ -1097,11 +1298,14 @@ __global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid
     // exit and free their SM slots while rank 0 finishes the row).
     Partial tot = empty_partial();
     if (warp == 0)
-      for (int k = lane; k < S; k += 32) part_combine<MODE>(tot, load_partial_dsmem(&ctl.result, k), p.scale, p.cs);
+      for (int k = lane; k < S; k += 32) part_combine<MODE>(tot, load_partial_dsmem(&ctl.result, k), p.scale);
     __syncwarp();
     cluster_arrive();
     RowOut o{};
-    if (warp == 0) o = row_out<MODE>(p, warp_combine<MODE>(tot, p.scale, p.cs));
+    if (warp == 0) {
+      o = row_out<MODE>(p, warp_combine<MODE>(tot, p.scale));
+      if (__shfl_sync(0xFFFFFFFFu, o.exotic ? 1 : 0, 0)) o = exotic_row<BF16, MODE>(p, row, lane);
+    }
     // Everything above touched only this cluster's own memory.  In early mode
     // the wait for the previous kernel comes here, so that only the row's
     // writes (outputs, canvas, batch-row counters) follow that kernel's end.

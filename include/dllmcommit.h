@@ -77,10 +77,17 @@ const char* dllm_version(void);
  *           v & 3, u = (2 (r >> 9) + 1) 2^-24; row = b*L + l.
  *   prob    exp(z_x0 - m) / sum_A exp(z - m) of the untempered softmax.
  *   entropy ln Z - S / Z of the same softmax, clamped to [0, ln |A|].
- * bf16 logits widen exactly to fp32; NaN and values <= -2^100 carry no
- * mass; a row whose every entry carries none yields the uniform limit
- * (x0 = min A, prob = 1/|A|, entropy = ln |A|); +inf entries share all the
- * mass equally.  Sums are accumulated in fp32.
+ * bf16 logits widen exactly to fp32.  A NaN carries no mass; every other
+ * value is the logit itself: finite logits of any size take the ordinary
+ * softmax, +inf entries share all the mass equally, and a row whose every
+ * entry carries no mass (NaN or -inf) yields the uniform limit (x0 = min A,
+ * prob = 1/|A|, entropy = ln |A|).  Sums are accumulated in fp32.  Rows
+ * whose largest logit exceeds about 1.8e8 in magnitude (1.8e8 / s for
+ * scaled logits), or that hold no logit above -2^100, are recomputed by a
+ * slower exact path inside the same launch (one warp, two or three extra
+ * reads of the row); model logits never reach it.
+ * temperature   0 (greedy) or a Gumbel temperature in (0, 2^64]; NaN,
+ *               negative, infinite or larger values: DLLM_ERR_INVALID_ARGUMENT.
  *
  * logits        device, T rows of row_stride elements (dtype dt); the base
  *               pointer and row_stride * sizeof(element) must be multiples of
@@ -157,15 +164,26 @@ dllm_status dllm_token_stats_ex(const void* logits, dllm_dtype dt, int64_t B, in
  * (4 bytes per row and 16 per batch row, plus about 40 KB for the partial
  * reductions, so B*L up to roughly 250,000 rows) returns
  * DLLM_ERR_UNSUPPORTED without launching anything.
+ *   - The logits and outputs must be on the current CUDA device: the call
+ *     takes the array, the device's launch limits and (stream 0) the
+ *     default stream from it.
  *   - The first call on each device looks the array's device address up
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  With CUDA's lazy module loading (the
+ *     default), the driver reserves the array on a device only when the
+ *     library's kernels are first loaded there, which can be that first
+ *     call: make one call of any entry point on each device during warm-up,
+ *     before a section that must not allocate.
  *   - Every call first clears the part of the array it uses
  *     (cudaMemsetAsync on the stream), then launches the kernel; nothing is
  *     allocated or freed.
  *   - All calls share the one array and it keeps the last call's contents:
  *     calls that can overlap on the GPU (other streams, other host threads)
  *     race with each other and give wrong results.  Serialise them.
+ *   - A kernel fault (a bounded wait that ran out; see dllm_workspace_fault)
+ *     is recorded in the array's first word.  dllm_noalloc_fault reads it;
+ *     the next dllm_token_stats_noalloc call clears it, so read it after a
+ *     call and before the next one.
  * ------------------------------------------------------------------------ */
 #define DLLM_NOALLOC_SCRATCH_BYTES (1u << 20)
 
@@ -173,6 +191,13 @@ dllm_status dllm_token_stats_noalloc(const void* logits, dllm_dtype dt, int64_t 
                                      int64_t row_stride, float temperature, uint64_t key,
                                      const int32_t* suppress_ids, int32_t n_suppress,
                                      int32_t* x0, float* prob, float* entropy, dllm_stream_t stream);
+
+/* The fault word of the allocation-free entry's array on the current device,
+ * as dllm_workspace_fault reads a workspace's: synchronises `stream`, stores
+ * the code in *fault (0: none) and clears the word if it was set.  Errors:
+ * DLLM_ERR_INVALID_ARGUMENT for a NULL fault, DLLM_ERR_CUDA if the copy or
+ * the synchronisation fails. */
+dllm_status dllm_noalloc_fault(dllm_stream_t stream, int32_t* fault);
 
 /* ------------------------------------------------------------------------
  * Commit rules.  One batch row b of L positions; cand (device, (B, L)) marks
@@ -343,6 +368,10 @@ dllm_status dllm_block_causal_mask(int64_t Lq, int64_t Lk, int64_t q_offset, int
  * workspace >= dllm_lm_head_stats_workspace_size(T, V, d) bytes (any
  *         contents; it holds per-CTA partials).  Other arguments as in
  *         dllm_token_stats.
+ * Range: the logits this call never stores cannot be read back, so it has
+ * no exact path for exotic rows: the products must stay below 1.8e8 in
+ * magnitude and must not be NaN (rows beyond that get unspecified
+ * statistics; no fault).
  * Ordering: the call is launched as a programmatic dependent of the kernel
  * before it in the stream.  The hidden states (and every output) are touched
  * only after that kernel has completed; the first slabs of the weight are
@@ -391,7 +420,7 @@ typedef struct {
   int64_t canvas_stride;    /* elements between batch rows of the canvas */
   int64_t canvas_offset;    /* canvas column of position l = 0 */
   int32_t* counts;          /* device (B, 3) or NULL: per batch row [candidates, commits, edits] */
-  int32_t flags;            /* 0, or DLLM_FLAG_INPUTS_READY */
+  int32_t flags;            /* 0, or DLLM_FLAG_INPUTS_READY (| DLLM_FLAG_TEST_DROP_COPY in tests) */
   const dllm_stats_ex* ex;  /* NULL, or the extended statistics options (scale, margin, argmax);
                                the rules then decide on the scaled statistics */
 } dllm_commit_params;
@@ -403,6 +432,15 @@ typedef struct {
  * Lets back-to-back steps over independent inputs overlap.  Never set it when
  * the previous kernel produces the logits or the mask (an LM-head GEMM, say). */
 #define DLLM_FLAG_INPUTS_READY 1
+
+/* Test only, never set in use: the first CTA of the statistics kernel does
+ * not issue the bulk copy of its first unit, so that its consumers' bounded
+ * wait (about one second) runs out.  The call then takes a second or two,
+ * records fault 1 (a consumer gave up waiting for a copy) or 2 (the copy
+ * issuer gave up waiting for a free stage) in the workspace, leaves outputs
+ * unwritten and workspace counters set.  It exists to exercise the fault path
+ * (dllm_workspace_fault, then zeroing the workspace) without a real fault. */
+#define DLLM_FLAG_TEST_DROP_COPY 2
 
 dllm_status dllm_commit_step(const void* logits, dllm_dtype dt, int64_t B, int64_t L, int64_t V,
                              int64_t row_stride, float temperature, uint64_t key,

@@ -123,6 +123,9 @@ def test_commit_step_host_checks_arguments_before_any_device_work(lib):
     assert fn(fake, fake, 7, 1, 32, 1000, 0.0, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1
     assert fn(fake, fake, 1, 1, 32, 1000, 0.0, 0, None, 0, cp, P(4098), fake, fake, 1 << 20, None) == 1
     assert fn(fake, fake, 1, 1, 32, 1000, -1.0, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1
+    # temperatures above 2^64 (and inf, NaN) are outside the range the statistics accept
+    for t in (2.0 ** 65, float("inf"), float("nan")):
+        assert fn(fake, fake, 1, 1, 32, 1000, t, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1
     # rule NONE with neither candidates nor a canvas is invalid (as for dllm_commit_step)
     assert fn(fake, fake, 1, 1, 32, 1000, 0.0, 0, None, 0, cp, fake, fake, fake, 1 << 20, None) == 1
 

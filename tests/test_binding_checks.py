@@ -85,3 +85,16 @@ def test_stats_outputs():
         cs._stats_out((good[0], torch.zeros(T, dtype=torch.float64), good[2]), T, CPU)
     with pytest.raises(ValueError):   # x0 one short
         cs._stats_out((torch.zeros(T - 1, dtype=torch.int32), good[1], good[2]), T, CPU)
+
+
+def test_noalloc_tensors_must_be_on_the_current_device():
+    """dllm_token_stats_noalloc takes its scratch address and launch limits
+    from the current device: the binding refuses tensors or a stream elsewhere."""
+    cs._on_current_device(torch.device("cuda", 1), 1)
+    cs._on_current_device(torch.device("cuda", 0), 0, stream_device=0)
+    with pytest.raises(ValueError):
+        cs._on_current_device(torch.device("cuda", 1), 0)
+    with pytest.raises(ValueError):
+        cs._on_current_device(torch.device("cpu"), 0)
+    with pytest.raises(ValueError):
+        cs._on_current_device(torch.device("cuda", 0), 0, stream_device=1)

@@ -1082,11 +1082,16 @@ __device__ __forceinline__ void release_unit(SharedCtl& ctl, const RingPos& r, i
   if (lane == 0 && !ctl.abort_flag) mbar_arrive(smem_addr(&ctl.empty[r.slot]));
 }
 
+// CTAs per SM each kernel is compiled for: three for the plain greedy mode
+// (its per-thread state fits 72 registers without spilling, and three rings
+// of 64 KB fit the SM's shared memory), two for the modes that track more.
+__host__ __device__ constexpr int min_ctas_per_sm(int mode) { return mode == 0 ? 3 : 2; }
+
 // ---------------------------------------------------------------------------
 // Persistent kernel: many rows.  CTA c owns units [c U / P, (c+1) U / P).
 // ---------------------------------------------------------------------------
 template <bool BF16, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constant__ StatsParams p) {
+__global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_kernel(const __grid_constant__ StatsParams p) {
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ SharedCtl ctl;
   const int tid = threadIdx.x;
@@ -1226,7 +1231,7 @@ __global__ void __launch_bounds__(kThreads, 2) stats_kernel(const __grid_constan
 // memory and finishes the row.
 // ---------------------------------------------------------------------------
 template <bool BF16, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) stats_cluster_kernel(const __grid_constant__ StatsParams p) {
+__global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_cluster_kernel(const __grid_constant__ StatsParams p) {
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ SharedCtl ctl;
   const int tid = threadIdx.x;

@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
                     help="eager steps only (no graph, e2e or CPU leg): the command the ncu captures use")
+    ap.add_argument("--ready", action="store_true",
+                    help="with --profile: launch the steps with DLLM_FLAG_INPUTS_READY (the launch the "
+                         "timed graph uses) instead of as a dependent chain")
     ap.add_argument("--batch-rows", type=int, default=None,
                     help="with --profile: only the first N batch rows of the workload (a capture small "
                          "enough for a full ncu section set)")
@@ -508,7 +511,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     if args.profile:
         for i in range(warmup + steps):
-            runner.step(i)
+            runner.step(i, args.ready)
         torch.cuda.synchronize()
         return {"profile": w.name, "steps": warmup + steps, "workspace_fault": cs.workspace_fault(runner.ws)}, w
 

@@ -37,6 +37,7 @@ struct DeviceInfo {
   // cluster size 1, 2, 4, 8, 16.
   int occ[2 * kModeSlots] = {};
   int clusters[2 * kModeSlots][5] = {};
+  int batch_clusters[2 * kModeSlots][5] = {};   // co-resident clusters of stats_batch_kernel per size
   cudaError_t err = cudaSuccess;
 };
 
@@ -51,37 +52,39 @@ const DeviceInfo* device_info() {
     d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     for (int v = 0; v < 2 * kModeSlots && d.err == cudaSuccess; ++v) {
       if (!mode_built(v % kModeSlots)) continue;
-      const void* k = stats_kernel_ptr(v >= kModeSlots, v % kModeSlots, false);
+      const void* k = stats_kernel_ptr(v >= kModeSlots, v % kModeSlots, kGridPersistent);
       d.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmemMax));
       if (d.err != cudaSuccess) break;
       int n = 0;
       d.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kThreads, kStatsSmemMax);
       d.occ[v] = std::max(1, std::min(n, kMaxCtasPerSm));
     }
-    for (int v = 0; v < 2 * kModeSlots && d.err == cudaSuccess; ++v) {
-      if (!mode_built(v % kModeSlots)) continue;
-      const void* k = stats_kernel_ptr(v >= kModeSlots, v % kModeSlots, true);
-      d.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmemMax));
-      if (d.err == cudaSuccess) d.err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      for (int e = 0; e < 5 && d.err == cudaSuccess; ++e) {
-        const int S = 1 << e;
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(S * 64);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kStatsSmemMax;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = S;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
-          (void)cudaGetLastError();  // an unsupported size only rules that size out
-          n = 0;
+    for (int kind : {kGridCluster, kGridBatch}) {
+      for (int v = 0; v < 2 * kModeSlots && d.err == cudaSuccess; ++v) {
+        if (!mode_built(v % kModeSlots)) continue;
+        const void* k = stats_kernel_ptr(v >= kModeSlots, v % kModeSlots, kind);
+        d.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmemMax));
+        if (d.err == cudaSuccess) d.err = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        for (int e = 0; e < 5 && d.err == cudaSuccess; ++e) {
+          const int S = 1 << e;
+          cudaLaunchConfig_t cfg{};
+          cfg.gridDim = dim3(S * 64);
+          cfg.blockDim = dim3(kThreads);
+          cfg.dynamicSmemBytes = kStatsSmemMax;
+          cudaLaunchAttribute attr[1];
+          attr[0].id = cudaLaunchAttributeClusterDimension;
+          attr[0].val.clusterDim.x = S;
+          attr[0].val.clusterDim.y = 1;
+          attr[0].val.clusterDim.z = 1;
+          cfg.attrs = attr;
+          cfg.numAttrs = 1;
+          int n = 0;
+          if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();  // an unsupported size only rules that size out
+            n = 0;
+          }
+          (kind == kGridCluster ? d.clusters : d.batch_clusters)[v][e] = n;
         }
-        d.clusters[v][e] = n;
       }
     }
     for (int nt : {128, 256, 512, 1024}) {
@@ -118,6 +121,7 @@ WsLayout ws_layout(int64_t B, int64_t L, int sms) {
 struct StatsPlan {
   int64_t nvec, K, U;
   int32_t tail, chunk_vec, P, stages, cluster;
+  int32_t kind;   // kGridPersistent, kGridCluster or kGridBatch
 };
 
 int chunk_for(int64_t vectors_per_cta) {
@@ -145,6 +149,7 @@ StatsPlan plan_stats(const DeviceInfo& d, int variant, int64_t T, int64_t V, int
     const int S = 1 << e;
     if (T <= d.clusters[variant][e] && T * S <= budgets[bi] && pl.nvec >= static_cast<int64_t>(S) * 128) {
       pl.cluster = S;
+      pl.kind = kGridCluster;
       // slices are equal by construction: favour few, large copies
       const int64_t slice = pl.nvec / S;
       pl.chunk_vec = slice >= 768 ? 1024 : (slice >= 384 ? 512 : 256);
@@ -157,12 +162,35 @@ StatsPlan plan_stats(const DeviceInfo& d, int variant, int64_t T, int64_t V, int
   }
   const int64_t total_vec = T * std::max<int64_t>(pl.nvec, 1);
   pl.cluster = 0;
+  pl.kind = kGridPersistent;
   pl.chunk_vec = chunk_for(total_vec / std::max(ctas, 1));
   pl.stages = std::min(kMaxStages, kRingBytes / (pl.chunk_vec * 16));
   pl.K = pl.nvec > 0 ? (pl.nvec + pl.chunk_vec - 1) / pl.chunk_vec : 1;
   pl.U = T * pl.K;
   pl.P = static_cast<int32_t>(std::min<int64_t>(pl.U, ctas));
   return pl;
+}
+
+// The fused step on few short batch rows whose inputs are ready early
+// (where the few-rows plan took a cluster per row): one cluster of S CTAs
+// per batch row, S the largest power of two <= min(16, L) whose clusters can
+// be resident, each CTA taking at most kBatchMaxRowsPerCta whole rows.
+bool plan_batch(const DeviceInfo& d, int variant, int64_t B, int64_t L, StatsPlan& pl) {
+  if (L > kBatchMaxL || B > INT32_MAX / 16) return false;
+  for (int e = 4; e >= 0; --e) {
+    const int S = 1 << e;
+    if (S > L || d.batch_clusters[variant][e] <= 0) continue;
+    if ((L + S - 1) / S > kBatchMaxRowsPerCta) return false;
+    pl.kind = kGridBatch;
+    pl.cluster = S;
+    pl.chunk_vec = pl.nvec >= 3 * 1024 ? 1024 : (pl.nvec >= 3 * 512 ? 512 : 256);
+    pl.stages = std::min(kMaxStages, kRingBytes / (pl.chunk_vec * 16));
+    pl.K = pl.nvec > 0 ? (pl.nvec + pl.chunk_vec - 1) / pl.chunk_vec : 1;
+    pl.U = 0;
+    pl.P = static_cast<int32_t>(B * S);
+    return true;
+  }
+  return false;
 }
 
 dllm_status launch(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
@@ -274,7 +302,18 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   if (!ws || ws_bytes < lay.total) return DLLM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0) return DLLM_ERR_INVALID_ARGUMENT;
   const int variant = (bf16 ? kModeSlots : 0) + mode;
-  const StatsPlan pl = plan_stats(*d, variant, T, V, es, early);
+  StatsPlan pl = plan_stats(*d, variant, T, V, es, early);
+  // Inputs ready early, a rule to run and short batch rows: one cluster per
+  // batch row, so the step's rule needs no global atomics after the wait.
+  // Taken where the plan was a cluster per row (few rows), or where each of
+  // its CTAs would stream at most 1 MiB (a small step, whose serial chain
+  // matters more than how many CTAs stream it).
+  if (early && rule) {
+    StatsPlan bp = pl;
+    if (plan_batch(*d, variant, B, L, bp) &&
+        (pl.kind == kGridCluster || T * V * es <= static_cast<int64_t>(bp.P) * (1 << 20)))
+      pl = bp;
+  }
 
   StatsParams p{};
   p.logits = static_cast<const uint8_t*>(logits);
@@ -313,9 +352,9 @@ dllm_status run_stats(const void* logits, dllm_dtype dt, int64_t B, int64_t L, i
   if (rule) p.rule = *rule;
   const size_t smem = static_cast<size_t>(pl.stages) * pl.chunk_vec * 16 + (rule ? kFusedSortCap * 9 : 0);
   void* args[] = {&p};
-  if (pl.cluster > 0)
-    return launch(stats_kernel_ptr(bf16, mode, true), dim3(pl.P), dim3(kThreads), smem, s, args, pl.cluster);
-  return launch(stats_kernel_ptr(bf16, mode, false), dim3(pl.P), dim3(kThreads), smem, s, args);
+  if (pl.kind != kGridPersistent)
+    return launch(stats_kernel_ptr(bf16, mode, pl.kind), dim3(pl.P), dim3(kThreads), smem, s, args, pl.cluster);
+  return launch(stats_kernel_ptr(bf16, mode, kGridPersistent), dim3(pl.P), dim3(kThreads), smem, s, args);
 }
 
 int next_pow2(int64_t x) {

@@ -192,10 +192,42 @@ __device__ __forceinline__ long long rule_excl_scan(long long v, const RuleScrat
   return off + x - v;
 }
 
-// Runs the rule of batch row b.  All NT threads must call it.  Inputs written
-// by other CTAs of the same kernel are read through L2 (ld.global.cg).
-template <int NT, int BAR>
-__device__ void run_rule(const RuleArgs& a, int64_t b, const RuleScratch& s, int tid) {
+// The inputs of one batch row's rule as global memory holds them (written by
+// other CTAs of the same kernel, so read through L2 with ld.global.cg).
+struct GlobalRowSrc {
+  const RuleArgs& a;
+  int64_t b;
+  __device__ bool cand(int64_t l, int32_t* tok) const { return is_candidate(a, b, l, tok); }
+  __device__ float conf(int64_t l) const { return __ldcg(a.conf + b * a.L + l); }
+  __device__ float entropy(int64_t l) const { return __ldcg(a.entropy + b * a.L + l); }
+  __device__ int32_t x0(int64_t l) const { return a.x0 ? __ldcg(a.x0 + b * a.L + l) : 0; }
+};
+
+// Where a rule's decisions go: the masks, the canvas and the counts of
+// RuleArgs in global memory.
+struct GlobalEmit {
+  const RuleArgs& a;
+  int64_t b;
+  __device__ void operator()(int64_t l, bool commit, bool edit, int32_t x0) const {
+    const int64_t i = b * a.L + l;
+    if (a.commit) a.commit[i] = commit ? 1 : 0;
+    if (a.edit_mask) a.edit_mask[i] = edit ? 1 : 0;
+    if ((commit || edit) && a.canvas && a.x0) a.canvas[b * a.canvas_stride + a.canvas_offset + l] = x0;
+  }
+  __device__ void counts(int n_cand, int n_commit, int n_edit) const {
+    a.counts[3 * b + 0] = n_cand;
+    a.counts[3 * b + 1] = n_commit;
+    a.counts[3 * b + 2] = n_edit;
+  }
+};
+
+// Runs the rule of batch row b on the inputs `src` gives (candidate flag and
+// canvas token, confidence, entropy, proposal per position) and hands each
+// position's commit / edit decision, and (when RuleArgs asks for counts) the
+// batch row's counts from thread 0, to `emit`.  All NT threads must call it.
+template <int NT, int BAR, typename Src, typename Emit>
+__device__ void run_rule_src(const RuleArgs& a, int64_t b, const RuleScratch& s, int tid, const Src& src,
+                             const Emit& emit) {
   const int64_t L = a.L;
   const int64_t base = b * L;
   int32_t n_commit_forced = 0;
@@ -208,10 +240,10 @@ __device__ void run_rule(const RuleArgs& a, int64_t b, const RuleScratch& s, int
     uint64_t best = kNoKey;
     for (int64_t l = tid; l < L; l += NT) {
       int32_t tok;
-      if (!is_candidate(a, b, l, &tok)) continue;
+      if (!src.cand(l, &tok)) continue;
       ++n_cand;
       if (a.rule == kRuleThreshold) {
-        const float c = nan_to(__ldcg(a.conf + base + l), -__int_as_float(0x7F800000));
+        const float c = nan_to(src.conf(l), -__int_as_float(0x7F800000));
         const bool pass = a.strict ? (c > a.tau) : (c >= a.tau);
         any_pass |= pass ? 1 : 0;
         const uint64_t key = desc_key(c, l);
@@ -233,10 +265,9 @@ __device__ void run_rule(const RuleArgs& a, int64_t b, const RuleScratch& s, int
       uint64_t key = kNoKey;
       if (l < L) {
         int32_t tok;
-        if (is_candidate(a, b, l, &tok)) {
+        if (src.cand(l, &tok)) {
           ++n_cand;
-          key = (a.rule == kRuleEntropyBound) ? asc_key(__ldcg(a.entropy + base + l), l)
-                                              : desc_key(__ldcg(a.conf + base + l), l);
+          key = (a.rule == kRuleEntropyBound) ? asc_key(src.entropy(l), l) : desc_key(src.conf(l), l);
         }
       }
       s.keys[l] = key;
@@ -251,7 +282,7 @@ __device__ void run_rule(const RuleArgs& a, int64_t b, const RuleScratch& s, int
       uint64_t first_fail = static_cast<uint64_t>(n_cand_total);
       for (int i = tid; i < n_cand_total; i += NT) {
         const int64_t l = static_cast<int64_t>(s.keys[i] & 0xFFFFFFFFu);
-        const double c = nan_to(__ldcg(a.conf + base + l), -__int_as_float(0x7F800000));
+        const double c = nan_to(src.conf(l), -__int_as_float(0x7F800000));
         const double lhs = __dmul_rn(static_cast<double>(i + 1), __dsub_rn(1.0, c));
         if (!(lhs <= static_cast<double>(a.factor))) {
           first_fail = static_cast<uint64_t>(i) < first_fail ? static_cast<uint64_t>(i) : first_fail;
@@ -284,15 +315,15 @@ __device__ void run_rule(const RuleArgs& a, int64_t b, const RuleScratch& s, int
     rsync<NT, BAR>();
   }
 
-  // Write the masks and update the canvas.
+  // The masks and the canvas update.
   int n_commit = 0, n_edit = 0;
   for (int64_t l = tid; l < L; l += NT) {
     int32_t tok;
-    const bool cand = is_candidate(a, b, l, &tok);
+    const bool cand = src.cand(l, &tok);
     bool commit = false;
     if (a.rule == kRuleThreshold) {
       if (cand) {
-        const float c = nan_to(__ldcg(a.conf + base + l), -__int_as_float(0x7F800000));
+        const float c = nan_to(src.conf(l), -__int_as_float(0x7F800000));
         commit = a.strict ? (c > a.tau) : (c >= a.tau);
         if (forced != kNoKey && static_cast<int64_t>(forced & 0xFFFFFFFFu) == l) commit = true;
       }
@@ -300,28 +331,27 @@ __device__ void run_rule(const RuleArgs& a, int64_t b, const RuleScratch& s, int
       commit = s.flags[l] != 0;
     }
     bool edit = false;
-    int32_t x0 = 0;
-    if (a.x0) x0 = __ldcg(a.x0 + base + l);
+    const int32_t x0 = src.x0(l);
     if (a.edit && !cand) {
-      const float p = nan_to(__ldcg(a.conf + base + l), -__int_as_float(0x7F800000));
+      const float p = nan_to(src.conf(l), -__int_as_float(0x7F800000));
       edit = (x0 != tok) && (p > a.tau_edit);
     }
-    if (a.commit) a.commit[base + l] = commit ? 1 : 0;
-    if (a.edit_mask) a.edit_mask[base + l] = edit ? 1 : 0;
-    if ((commit || edit) && a.canvas && a.x0) a.canvas[b * a.canvas_stride + a.canvas_offset + l] = x0;
+    emit(l, commit, edit, x0);
     n_commit += commit ? 1 : 0;
     n_edit += edit ? 1 : 0;
   }
   (void)n_commit_forced;
   if (a.counts) {
     const int4 t = rule_sum4<NT, BAR>(make_int4(n_commit, n_edit, 0, 0), s, tid);
-    if (tid == 0) {
-      a.counts[3 * b + 0] = n_cand_total;
-      a.counts[3 * b + 1] = t.x;
-      a.counts[3 * b + 2] = t.y;
-    }
+    if (tid == 0) emit.counts(n_cand_total, t.x, t.y);
   }
   rsync<NT, BAR>();
+}
+
+// The rule of batch row b on its inputs in global memory, written there.
+template <int NT, int BAR>
+__device__ void run_rule(const RuleArgs& a, int64_t b, const RuleScratch& s, int tid) {
+  run_rule_src<NT, BAR>(a, b, s, tid, GlobalRowSrc{a, b}, GlobalEmit{a, b});
 }
 
 }  // namespace dllm

@@ -17,6 +17,8 @@ constexpr int kMaxStages = 16;
 constexpr int kRingBytes = 64 * 1024;
 constexpr int kFusedSortCap = 1024;              // largest L the fused sorting rules take
 constexpr int kMaxCtasPerSm = 4;
+constexpr int kBatchMaxL = 256;            // L the batch-row kernel takes (one consumer thread per row)
+constexpr int kBatchMaxRowsPerCta = 16;    // rows one of its CTAs reduces (L <= 16 S)
 
 // What a row's pass tracks, as bits: kModeSample, a Gumbel-max sample
 // (else the greedy argmax); kModeArgmax, the first argmax beside a sample;
@@ -35,9 +37,14 @@ __host__ __device__ constexpr bool mode_built(int m) {
   return (m & 7) == 0 || (m & 7) == 4 || (m & 7) == 1 || (m & 7) == 3 || (m & 7) == 7;
 }
 
+// Grid kinds of the statistics kernel: the persistent grid (many rows), a
+// cluster per row (few rows), a cluster per batch row (few short batch rows
+// whose inputs are ready early).
+enum : int { kGridPersistent = 0, kGridCluster = 1, kGridBatch = 2 };
+
 // Launchable statistics kernels, one per (dtype, mode, grid kind); defined
 // in dllm_stats_{greedy,sample,margin}{,_scaled}.cu.
-const void* stats_kernel_ptr(bool bf16, int mode, bool cluster);
+const void* stats_kernel_ptr(bool bf16, int mode, int kind);
 
 // Partial reduction of one row segment, in scaled logits z' = z s: max m,
 // Z = sum 2^y and S2 = sum 2^y y with y = (z' - m) log2(e), the first index

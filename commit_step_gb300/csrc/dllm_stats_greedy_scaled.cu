@@ -6,17 +6,21 @@ namespace dllm {
 
 template __global__ void stats_kernel<false, 8>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<false, 8>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<false, 8>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<true, 8>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<true, 8>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<true, 8>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<false, 12>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<false, 12>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<false, 12>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<true, 12>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<true, 12>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<true, 12>(const __grid_constant__ StatsParams);
 
-const void* stats_kernel_ptr_greedy_scaled(bool bf16, int mode, bool cluster) {
+const void* stats_kernel_ptr_greedy_scaled(bool bf16, int mode, int kind) {
   switch (mode) {
-    case 8: return bf16 ? stats_entry<true, 8>(cluster) : stats_entry<false, 8>(cluster);
-    case 12: return bf16 ? stats_entry<true, 12>(cluster) : stats_entry<false, 12>(cluster);
+    case 8: return bf16 ? stats_entry<true, 8>(kind) : stats_entry<false, 8>(kind);
+    case 12: return bf16 ? stats_entry<true, 12>(kind) : stats_entry<false, 12>(kind);
     default: return nullptr;
   }
 }

@@ -671,6 +671,7 @@ struct Consumer {
     acc_init(acc);
     if (RUNNER) acc.m2o = kMInit;
     warp_best = kNegInf;
+    sup_restart();
   }
 
   static constexpr int kVPT = 1024 / kConsumers;  // vectors per thread in the largest unit
@@ -734,41 +735,81 @@ struct Consumer {
         }
       }
     }
+    // The plain greedy mode on a full unit needs only the unit's max: one
+    // max tree over all its words; the first vector holding the thread's
+    // max is looked for only when the unit raises it (rare after the first
+    // units).  The other modes keep every vector's max (the Gumbel bound,
+    // the runner-up).
+    constexpr bool LEAN = GREEDY && !RUNNER && !GUMBEL && FULL;
     float vmax[NPT];
+    float umax;
+    if (LEAN) {
+      umax = unit_max(w);
+    } else {
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) vmax[j] = valid[j] ? vector_max(w[j]) : kMInit;
-    float umax = vmax[0];
+      for (int j = 0; j < NPT; ++j) vmax[j] = valid[j] ? vector_max(w[j]) : kMInit;
+      umax = vmax[0];
 #pragma unroll
-    for (int j = 1; j < NPT; ++j) umax = fmaxf(umax, vmax[j]);
+      for (int j = 1; j < NPT; ++j) umax = fmaxf(umax, vmax[j]);
+    }
     if (umax > kTopClamp) {  // rare: +inf or huge logits count as 2^100
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) w[j][k] = BF16 ? bmin2(w[j][k], kTopBf16x2) : clamp_top_bits(w[j][k]);
-        vmax[j] = fminf(vmax[j], kTopClamp);
+        if (!LEAN) vmax[j] = fminf(vmax[j], kTopClamp);
       }
       umax = kTopClamp;
     }
-    // Maxima of the scaled logits z' = z s (the scaling is monotone, so the
-    // max of the scaled elements is the scaled max, bit for bit).
     float vms[NPT];
+    if (LEAN) {
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) vms[j] = !SCALED ? vmax[j] : ((FULL || valid[j]) ? __fmul_rn(vmax[j], s) : kMInit);
-    if (GREEDY) {
+      for (int j = 0; j < NPT; ++j) vms[j] = 0.0f;   // unused: no per-vector bound in this mode
+      const float ums = SCALED ? __fmul_rn(umax, s) : umax;   // the scaling is monotone
+      if (ums > acc.vm) {
+        bool found = false;
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+          const float vm = vector_max(w[j]);
+          const bool hit = !found && (SCALED ? __fmul_rn(vm, s) : vm) == ums;
+          if (hit) {
+            found = true;
+            acc.vm = ums;
+            acc.vv = id0 + j * kConsumers * EPV;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc.bw[k] = w[j][k];
+          }
+        }
+      }
+    } else {
+      // Maxima of the scaled logits z' = z s (the scaling is monotone, so the
+      // max of the scaled elements is the scaled max, bit for bit).
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) vms[j] = !SCALED ? vmax[j] : ((FULL || valid[j]) ? __fmul_rn(vmax[j], s) : kMInit);
+      if (GREEDY) {
       // The first vector holding this thread's max (ids increase with j and
       // from unit to unit, so a strict > keeps the earliest), kept with its
       // words; the element inside it is located once per row.  Every other
       // vector's max feeds the runner-up.
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        const bool better = vms[j] > acc.vm;
-        if (RUNNER) acc.m2o = fmaxf(acc.m2o, better ? acc.vm : vms[j]);
-        acc.vm = better ? vms[j] : acc.vm;
-        acc.vv = better ? id0 + j * kConsumers * EPV : acc.vv;
+        for (int j = 0; j < NPT; ++j) {
+          const bool better = vms[j] > acc.vm;
+          if (RUNNER) acc.m2o = fmaxf(acc.m2o, better ? acc.vm : vms[j]);
+          acc.vm = better ? vms[j] : acc.vm;
+          acc.vv = better ? id0 + j * kConsumers * EPV : acc.vv;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc.bw[k] = better ? w[j][k] : acc.bw[k];
+          for (int k = 0; k < 4; ++k) acc.bw[k] = better ? w[j][k] : acc.bw[k];
+        }
       }
     }
+    gumbel_and_sums<NPT, FULL>(w, valid, vms, umax, row, id0);
+  }
+
+  // The rescale, the sums and (Gumbel modes) the samples of one unit's
+  // vectors; vms[j] is vector j's scaled max (unused in the lean mode).
+  template <int NPT, bool FULL>
+  __device__ __forceinline__ void gumbel_and_sums(uint32_t (&w)[NPT][4], const bool (&valid)[NPT],
+                                                  const float (&vms)[NPT], float umax, int64_t row, int32_t id0) {
     // Branch-free rescale to the new running max (factor 1 when it did not grow).
     {
       const float mnew = fmaxf(acc.m, umax);
@@ -873,6 +914,30 @@ struct Consumer {
     return __uint_as_float(v[e]);
   }
 
+  // The max of all elements of a unit's vectors (sanitized words).
+  template <int NPT>
+  __device__ __forceinline__ static float unit_max(const uint32_t (&w)[NPT][4]) {
+    if (BF16) {
+      uint32_t m[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m[k] = w[0][k];
+#pragma unroll
+      for (int j = 1; j < NPT; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m[k] = bmax2(m[k], w[j][k]);
+      const uint32_t t = bmax2(bmax2(m[0], m[1]), bmax2(m[2], m[3]));
+      return fmaxf(bf16lo(t), bf16hi(t));
+    }
+    float m[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m[k] = __uint_as_float(w[0][k]);
+#pragma unroll
+    for (int j = 1; j < NPT; ++j)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], __uint_as_float(w[j][k]));
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+  }
+
   __device__ __forceinline__ static float vector_max(const uint32_t (&v)[4]) {
     if (BF16) {
       const uint32_t m = bmax2(bmax2(v[0], v[1]), bmax2(v[2], v[3]));
@@ -951,11 +1016,20 @@ struct Consumer {
     acc.m2o = r2;
   }
 
-  // Whether suppressed ids fall in [lo, hi) (the same answer in every thread).
-  __device__ bool has_sup(int64_t lo, int64_t hi) const {
-    bool any = false;
-    for (int i = 0; i < p.n_sup; ++i) any |= (p.sup[i] >= lo && p.sup[i] < hi);
-    return any;
+  // Whether suppressed ids fall in [lo, hi) (the same answer in every
+  // thread).  The loops ask for ranges of one row in increasing order, so a
+  // cursor walks the sorted list: one parameter read per suppressed id per
+  // row, not one per range (an indexed parameter read costs hundreds of
+  // cycles).  reset() restarts it for the next row.
+  int32_t sup_i;
+  int64_t sup_next;
+  __device__ void sup_restart() {
+    sup_i = 0;
+    sup_next = p.n_sup > 0 ? p.sup[0] : INT64_MAX;
+  }
+  __device__ bool has_sup(int64_t lo, int64_t hi) {
+    while (sup_next < lo) sup_next = (++sup_i < p.n_sup) ? p.sup[sup_i] : INT64_MAX;
+    return sup_next < hi;
   }
 
   // The CTA's reduction of all consumer states; valid in thread 0.
@@ -1331,11 +1405,230 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_cluster
   }
 }
 
+// ---------------------------------------------------------------------------
+// Batch-row kernel: the fused step when the inputs are ready before the
+// previous kernel ends (DLLM_FLAG_INPUTS_READY) and batch rows are short.
+// Cluster b of p.cluster CTAs takes batch row b; CTA rank k reduces rows
+// [k L / S, (k+1) L / S) of it, each whole, one after the other, and keeps
+// their partials in shared memory.  Rank 0 gathers the L partials through
+// distributed shared memory, finishes every row and runs the batch row's
+// rule on shared-memory copies of the statistics, so that no CTA depends on
+// another through global memory: after the grid dependency it only loads
+// the canvas (when a rule needs it) and stores.  (The row-cluster kernel
+// instead publishes each row with a release-acquire atomic, which puts two
+// L2 round trips into every step's serial chain.)
+// ---------------------------------------------------------------------------
+// A row's inputs to the rule, as rank 0 holds them in shared memory.
+struct SharedRowSrc {
+  const float* c;
+  const float* h;
+  const int32_t* x;
+  const uint8_t* cd;
+  const int32_t* tk;
+  __device__ bool cand(int64_t l, int32_t* tok) const {
+    *tok = tk[l];
+    return cd[l] != 0;
+  }
+  __device__ float conf(int64_t l) const { return c[l]; }
+  __device__ float entropy(int64_t l) const { return h[l]; }
+  __device__ int32_t x0(int64_t l) const { return x[l]; }
+};
+
+// The rule's decisions kept in shared memory (bit 0 commit, bit 1 edit; the
+// counts in three ints), to be stored once the grid dependency allows.
+struct SharedEmit {
+  uint8_t* flags;
+  int32_t* cnt;
+  __device__ void operator()(int64_t l, bool commit, bool edit, int32_t) const {
+    flags[l] = static_cast<uint8_t>((commit ? 1 : 0) | (edit ? 2 : 0));
+  }
+  __device__ void counts(int n_cand, int n_commit, int n_edit) const {
+    cnt[0] = n_cand;
+    cnt[1] = n_commit;
+    cnt[2] = n_edit;
+  }
+};
+
+template <bool BF16, int MODE>
+__global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_batch_kernel(const __grid_constant__ StatsParams p) {
+  extern __shared__ __align__(128) uint8_t dsmem[];
+  __shared__ SharedCtl ctl;
+  __shared__ Partial row_part[kBatchMaxRowsPerCta];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int S = p.cluster;
+  const uint32_t rank = cluster_rank();
+  const int64_t b = blockIdx.x / S;
+  const int64_t L = p.L;
+  const int64_t l0 = (static_cast<int64_t>(rank) * L) / S;
+  const int64_t l1 = (static_cast<int64_t>(rank + 1) * L) / S;
+  const int64_t n_units = (l1 - l0) * p.K;
+  const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
+  const uint32_t ring = smem_addr(dsmem);
+
+  init_barriers(ctl, p.stages);
+  __syncthreads();
+  if (!p.early) pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      int64_t prow = b * L + l0, puk = 0;
+      produce(p, ctl, ring, chunk_bytes, n_units, [&](const uint8_t*& src, uint32_t& bytes) {
+        const int64_t v0 = puk * p.chunk_vec;
+        int64_t nv = p.nvec - v0;
+        nv = nv < p.chunk_vec ? nv : p.chunk_vec;
+        nv = nv > 0 ? nv : 0;
+        src = p.logits + prow * p.row_bytes + v0 * 16;
+        bytes = static_cast<uint32_t>(nv) * 16u;
+        if (++puk == p.K) {
+          puk = 0;
+          ++prow;
+        }
+      }, p.test_drop != 0 && blockIdx.x == 0);
+    }
+    __syncwarp();
+    cluster_sync_all();  // row partials published
+    if (rank == 0)
+      cluster_arrive();
+    else
+      cluster_sync_all();  // rank 0 has read them
+    return;
+  }
+
+  Consumer<BF16, MODE> con(p, ctl, ring, chunk_bytes);
+  volatile int32_t* abort_flag = &ctl.abort_flag;
+  RingPos rc;
+  for (int64_t j = 0; j < l1 - l0; ++j) {
+    const int64_t row = b * L + l0 + j;
+    con.reset();
+    for (int64_t uk = 0; uk < p.K; ++uk) {
+      const int64_t v_unit = uk * p.chunk_vec;
+      int64_t nv = p.nvec - v_unit;
+      nv = nv < p.chunk_vec ? nv : p.chunk_vec;
+      nv = nv > 0 ? nv : 0;
+      const bool sup = con.has_sup(v_unit * con.EPV, (uk == p.K - 1) ? p.V : (v_unit + nv) * con.EPV);
+      wait_unit(p, ctl, rc);
+      con.unit(ring + rc.slot * chunk_bytes, row, v_unit, nv, sup);
+      release_unit(ctl, rc, lane);
+      rc.advance(p.stages);
+    }
+    if (!*abort_flag) con.tail(row);
+    con.resolve_index();
+    const Partial r = con.cta_reduce();
+    if (tid == 0) {
+      row_part[j] = r;
+      ctl.cta_best = float_key(kNegInf);  // the next row starts with no pruning floor
+    }
+    named_sync(1, kConsumers);  // warp_part is free again before the next row's reduction
+  }
+  __syncwarp();
+  cluster_sync_all();
+  if (rank != 0) {
+    __syncwarp();
+    cluster_sync_all();
+    return;
+  }
+
+  // Rank 0.  Every bulk copy of this CTA has landed (the producer drained
+  // before the cluster barrier), so the ring holds the rule's inputs now.
+  float* s_conf = reinterpret_cast<float*>(dsmem);
+  float* s_ent = s_conf + kBatchMaxL;
+  int32_t* s_x0 = reinterpret_cast<int32_t*>(s_ent + kBatchMaxL);
+  int32_t* s_tok = s_x0 + kBatchMaxL;
+  uint8_t* s_cand = reinterpret_cast<uint8_t*>(s_tok + kBatchMaxL);
+  uint8_t* s_exotic = s_cand + kBatchMaxL;
+  RowOut o{};
+  const int64_t t = tid;   // the row this thread finishes (L <= kConsumers)
+  if (t < L) {
+    const int64_t k = ((t + 1) * S + L - 1) / L - 1;   // the CTA whose range holds row t
+    const int64_t j = t - (k * L) / S;
+    o = row_out<MODE>(p, load_partial_dsmem(&row_part[j], static_cast<uint32_t>(k)));
+    s_exotic[t] = o.exotic ? 1 : 0;
+  }
+  named_sync(1, kConsumers);
+  cluster_arrive();   // the other CTAs may exit: their partials are read
+  // Rows the streaming pass does not resolve are recomputed, a warp each.
+  for (int64_t e = warp; e < L; e += kConsumerWarps) {
+    if (!s_exotic[e]) continue;
+    const RowOut q = exotic_row<BF16, MODE>(p, b * L + e, lane);
+    if (lane == 0) {
+      s_conf[e] = q.prob;
+      s_ent[e] = q.H;
+      s_x0[e] = q.x0;
+      s_tok[e] = q.argmax;
+      s_cand[e] = 0;
+      *reinterpret_cast<float*>(s_exotic + kBatchMaxL + 4 * e) = q.margin;
+    }
+  }
+  named_sync(1, kConsumers);
+  if (t < L && o.exotic) {
+    o.prob = s_conf[t];
+    o.H = s_ent[t];
+    o.x0 = s_x0[t];
+    o.argmax = s_tok[t];
+    o.margin = *reinterpret_cast<const float*>(s_exotic + kBatchMaxL + 4 * t);
+  }
+  named_sync(1, kConsumers);
+  if (*abort_flag) return;   // a wait ran out (the fault is recorded): write nothing
+  // The rule's inputs and decisions.  When the candidates come from the
+  // candidate mask (an input like the logits), the whole rule is decided
+  // before the grid dependency and only stores follow it; when a canvas
+  // supplies candidates or tokens (rewritten by the step before), the canvas
+  // is read, and the rule decided, after it.
+  const RuleArgs& a = p.rule;
+  const bool reads_canvas = a.canvas != nullptr && (a.edit || a.cand == nullptr);
+  uint8_t* s_flags = s_exotic;               // reused: the exotic marks are consumed
+  int32_t* s_cnt = reinterpret_cast<int32_t*>(s_exotic + kBatchMaxL);
+  RuleScratch rs;
+  rs.keys = reinterpret_cast<uint64_t*>(dsmem + static_cast<size_t>(p.stages) * chunk_bytes);
+  rs.flags = dsmem + static_cast<size_t>(p.stages) * chunk_bytes + static_cast<size_t>(kFusedSortCap) * 8;
+  rs.red64 = ctl.rule_red64;
+  rs.red32 = ctl.rule_red32;
+  rs.cap = kFusedSortCap;
+  auto decide = [&]() {
+    int32_t tok = 0;
+    bool cand = false;
+    if (t < L) {
+      cand = is_candidate(a, b, t, &tok);
+      s_conf[t] = o.prob;
+      s_ent[t] = o.H;
+      s_x0[t] = o.x0;
+      s_tok[t] = tok;
+      s_cand[t] = cand ? 1 : 0;
+    }
+    named_sync(1, kConsumers);
+    run_rule_src<kConsumers, 1>(a, b, rs, tid, SharedRowSrc{s_conf, s_ent, s_x0, s_cand, s_tok},
+                                SharedEmit{s_flags, s_cnt});
+  };
+  if (!reads_canvas) decide();
+  if (p.early) pdl_wait();
+  if (reads_canvas) decide();
+  if (t < L) {
+    const int64_t row = b * L + t;
+    p.x0[row] = o.x0;
+    p.prob[row] = o.prob;
+    p.entropy[row] = o.H;
+    if (p.margin) p.margin[row] = o.margin;
+    if (p.argmax) p.argmax[row] = o.argmax;
+    const uint8_t f = s_flags[t];
+    if (a.commit) a.commit[row] = f & 1;
+    if (a.edit_mask) a.edit_mask[row] = (f >> 1) & 1;
+    if (f != 0 && a.canvas) a.canvas[b * a.canvas_stride + a.canvas_offset + t] = o.x0;
+  }
+  if (tid == 0 && a.counts) {
+    a.counts[3 * b + 0] = s_cnt[0];
+    a.counts[3 * b + 1] = s_cnt[1];
+    a.counts[3 * b + 2] = s_cnt[2];
+  }
+}
+
 // Kernel entry of (dtype, mode, grid kind) as a launchable pointer.
 template <bool BF16, int MODE>
-const void* stats_entry(bool cluster) {
-  return cluster ? reinterpret_cast<const void*>(&stats_cluster_kernel<BF16, MODE>)
-                 : reinterpret_cast<const void*>(&stats_kernel<BF16, MODE>);
+const void* stats_entry(int kind) {
+  if (kind == kGridCluster) return reinterpret_cast<const void*>(&stats_cluster_kernel<BF16, MODE>);
+  if (kind == kGridBatch) return reinterpret_cast<const void*>(&stats_batch_kernel<BF16, MODE>);
+  return reinterpret_cast<const void*>(&stats_kernel<BF16, MODE>);
 }
 
 }  // namespace dllm

@@ -6,12 +6,14 @@ namespace dllm {
 
 template __global__ void stats_kernel<false, 7>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<false, 7>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<false, 7>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<true, 7>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<true, 7>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<true, 7>(const __grid_constant__ StatsParams);
 
-const void* stats_kernel_ptr_margin(bool bf16, int mode, bool cluster) {
+const void* stats_kernel_ptr_margin(bool bf16, int mode, int kind) {
   switch (mode) {
-    case 7: return bf16 ? stats_entry<true, 7>(cluster) : stats_entry<false, 7>(cluster);
+    case 7: return bf16 ? stats_entry<true, 7>(kind) : stats_entry<false, 7>(kind);
     default: return nullptr;
   }
 }

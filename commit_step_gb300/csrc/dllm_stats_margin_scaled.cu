@@ -6,12 +6,14 @@ namespace dllm {
 
 template __global__ void stats_kernel<false, 15>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<false, 15>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<false, 15>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<true, 15>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<true, 15>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<true, 15>(const __grid_constant__ StatsParams);
 
-const void* stats_kernel_ptr_margin_scaled(bool bf16, int mode, bool cluster) {
+const void* stats_kernel_ptr_margin_scaled(bool bf16, int mode, int kind) {
   switch (mode) {
-    case 15: return bf16 ? stats_entry<true, 15>(cluster) : stats_entry<false, 15>(cluster);
+    case 15: return bf16 ? stats_entry<true, 15>(kind) : stats_entry<false, 15>(kind);
     default: return nullptr;
   }
 }

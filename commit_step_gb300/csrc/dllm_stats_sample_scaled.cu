@@ -7,17 +7,21 @@ namespace dllm {
 
 template __global__ void stats_kernel<false, 9>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<false, 9>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<false, 9>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<true, 9>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<true, 9>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<true, 9>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<false, 11>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<false, 11>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<false, 11>(const __grid_constant__ StatsParams);
 template __global__ void stats_kernel<true, 11>(const __grid_constant__ StatsParams);
 template __global__ void stats_cluster_kernel<true, 11>(const __grid_constant__ StatsParams);
+template __global__ void stats_batch_kernel<true, 11>(const __grid_constant__ StatsParams);
 
-const void* stats_kernel_ptr_sample_scaled(bool bf16, int mode, bool cluster) {
+const void* stats_kernel_ptr_sample_scaled(bool bf16, int mode, int kind) {
   switch (mode) {
-    case 9: return bf16 ? stats_entry<true, 9>(cluster) : stats_entry<false, 9>(cluster);
-    case 11: return bf16 ? stats_entry<true, 11>(cluster) : stats_entry<false, 11>(cluster);
+    case 9: return bf16 ? stats_entry<true, 9>(kind) : stats_entry<false, 9>(kind);
+    case 11: return bf16 ? stats_entry<true, 11>(kind) : stats_entry<false, 11>(kind);
     default: return nullptr;
   }
 }

@@ -55,7 +55,10 @@ struct Acc {
   uint64_t S2;      // two partial sums of 2^y y
   float nref;       // -ref, ref = RU(m' log2 e): minus the exponent reference of m
   int32_t idx;      // first index of m among the tail elements (greedy)
-  float vm;         // max of z' over the thread's full vectors (greedy)
+  float vm;         // greedy: z' of the thread's recorded max (its first
+                    // occurrence among the thread's full vectors; in the
+                    // plain greedy mode recorded only when it was the warp's
+                    // new max, so a thread may hold no record of its own max)
   int32_t vv;       // first id of the first vector holding vm, -1 if none
   uint32_t bw[4];   // that vector's sanitized words
   float m2o;        // max of z' over the thread's other full vectors; after
@@ -162,10 +165,12 @@ __device__ __forceinline__ void acc_pair2(uint64_t& Z2, uint64_t& S2, float z0, 
   S2 = fma2(e2, y2, S2);
 }
 
-// Combines b into a (a and b may cover any id sets; m is the raw max, the
-// argmax is decided on the scaled maxima fp32(m s), ties to the lower id).
-// The runner-up of the union is the larger of the winner's runner-up and the
-// loser's (scaled) max.
+// Combines b into a (a and b may cover any id sets; m is the raw max the
+// sums are taken against, the argmax is decided on the scaled maxima
+// fp32(m s), ties to the lower id).  The runner-up of the union is the larger
+// of the winner's runner-up and the loser's largest scaled value: its max,
+// or, for a part that holds no id of its m (idx unset: a lane whose values
+// all lie below its warp's max), the value its m2 carries.
 template <int MODE>
 __device__ __forceinline__ void part_combine(Partial& a, const Partial& b, float s) {
   constexpr bool GUMBEL = mode_sample(MODE), RUNNER = mode_runner(MODE), SCALED = mode_scaled(MODE);
@@ -177,7 +182,10 @@ __device__ __forceinline__ void part_combine(Partial& a, const Partial& b, float
   const float Z = ca * a.Z + cb * b.Z;
   const float S2 = ca * fmaf(da, a.Z, a.S2) + cb * fmaf(db, b.Z, b.S2);
   const bool b_wins = sb > sa || (sb == sa && b.idx < a.idx);
-  if (RUNNER) a.m2 = b_wins ? fmaxf(b.m2, sa) : fmaxf(a.m2, sb);
+  if (RUNNER) {
+    const float ta = a.idx == 0x7FFFFFFF ? a.m2 : sa, tb = b.idx == 0x7FFFFFFF ? b.m2 : sb;
+    a.m2 = b_wins ? fmaxf(b.m2, ta) : fmaxf(a.m2, tb);
+  }
   a.m = m;
   a.Z = Z;
   a.S2 = S2;
@@ -736,10 +744,10 @@ struct Consumer {
       }
     }
     // The plain greedy mode on a full unit needs only the unit's max: one
-    // max tree over all its words; the first vector holding the thread's
-    // max is looked for only when the unit raises it (rare after the first
-    // units).  The other modes keep every vector's max (the Gumbel bound,
-    // the runner-up).
+    // max tree over all its words; the lanes holding a new warp max look for
+    // its first vector (rare after the first units: a lane's value below the
+    // warp's max can be neither the row's max nor its first index).  The
+    // other modes keep every vector's max (the Gumbel bound, the runner-up).
     constexpr bool LEAN = GREEDY && !RUNNER && !GUMBEL && FULL;
     float vmax[NPT];
     float umax;
@@ -761,23 +769,29 @@ struct Consumer {
       }
       umax = kTopClamp;
     }
+    // The warp's running max: every lane's sums take its reference, so they
+    // are rescaled only when it grows (every lane of the warp is here).
+    const float wmax = warp_max_f32(umax);
     float vms[NPT];
     if (LEAN) {
 #pragma unroll
       for (int j = 0; j < NPT; ++j) vms[j] = 0.0f;   // unused: no per-vector bound in this mode
-      const float ums = SCALED ? __fmul_rn(umax, s) : umax;   // the scaling is monotone
-      if (ums > acc.vm) {
-        bool found = false;
+      if (wmax > acc.m) {
+        // The scaling is monotone: the scaled warp max is the largest scaled
+        // value, and a lane holds it when its scaled unit max equals it.
+        const float wms = scaled<SCALED>(wmax, s);
+        if (scaled<SCALED>(umax, s) == wms && wms > scaled<SCALED>(acc.m, s)) {
+          bool found = false;
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) {
-          const float vm = vector_max(w[j]);
-          const bool hit = !found && (SCALED ? __fmul_rn(vm, s) : vm) == ums;
-          if (hit) {
-            found = true;
-            acc.vm = ums;
-            acc.vv = id0 + j * kConsumers * EPV;
+          for (int j = 0; j < NPT; ++j) {
+            const bool hit = !found && scaled<SCALED>(vector_max(w[j]), s) == wms;
+            if (hit) {
+              found = true;
+              acc.vm = wms;
+              acc.vv = id0 + j * kConsumers * EPV;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc.bw[k] = w[j][k];
+              for (int k = 0; k < 4; ++k) acc.bw[k] = w[j][k];
+            }
           }
         }
       }
@@ -802,26 +816,16 @@ struct Consumer {
         }
       }
     }
-    gumbel_and_sums<NPT, FULL>(w, valid, vms, umax, row, id0);
+    gumbel_and_sums<NPT, FULL>(w, valid, vms, wmax, row, id0);
   }
 
   // The rescale, the sums and (Gumbel modes) the samples of one unit's
-  // vectors; vms[j] is vector j's scaled max (unused in the lean mode).
+  // vectors; vms[j] is vector j's scaled max (unused in the lean mode),
+  // wmax the warp's max over the unit.
   template <int NPT, bool FULL>
   __device__ __forceinline__ void gumbel_and_sums(uint32_t (&w)[NPT][4], const bool (&valid)[NPT],
-                                                  const float (&vms)[NPT], float umax, int64_t row, int32_t id0) {
-    // Branch-free rescale to the new running max (factor 1 when it did not grow).
-    {
-      const float mnew = fmaxf(acc.m, umax);
-      const float rn = exp_ref(scaled<SCALED>(mnew, s));
-      const float d = ref_shift(-acc.nref, rn);
-      const float c = ex2_approx(d);
-      const uint64_t d2 = pack2(d, d), c2 = pack2(c, c);
-      acc.S2 = mul2(c2, fma2(d2, acc.Z2, acc.S2));
-      acc.Z2 = mul2(acc.Z2, c2);
-      acc.m = mnew;
-      acc.nref = -rn;
-    }
+                                                  const float (&vms)[NPT], float wmax, int64_t row, int32_t id0) {
+    if (wmax > acc.m) acc_rescale<SCALED>(acc, wmax, s);   // the same in every lane of the warp
     const uint64_t nmc2 = pack2(acc.nref, acc.nref);
     uint64_t Zb = 0, Sb = 0;
 #pragma unroll
@@ -1011,6 +1015,11 @@ struct Consumer {
     } else if (acc.vm_tail == ms && acc.m > kMInit) {
       idx = acc.idx;
       if (RUNNER) r2 = fmaxf(r2, acc.vm);
+    } else if (RUNNER) {
+      // None of the thread's ids holds the max its sums are taken against
+      // (the warp's): all of them are "other" ids, and the runner-up field
+      // carries the largest (see part_combine).
+      r2 = fmaxf(acc.vm, acc.vm_tail);
     }
     acc.idx = idx;
     acc.m2o = r2;

@@ -601,6 +601,32 @@ __device__ __forceinline__ bool consumer_wait(uint32_t bar, uint32_t parity, vol
   }
 }
 
+// Position in the shared-memory ring: stage index and mbarrier phase parity.
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void advance(int stages) {
+    if (++slot == stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// The consumers' wait for a ring stage once the first try failed: bounded,
+// and it gives up at once when the CTA has aborted; a wait that runs out
+// records the fault and aborts the CTA (the loops then run to their end
+// without waiting, and nothing is written).
+static __device__ __noinline__ void wait_unit_slow(const StatsParams& p, SharedCtl& ctl, int slot, uint32_t phase) {
+  volatile int32_t* abort_flag = &ctl.abort_flag;
+  if (!*abort_flag && !consumer_wait(smem_addr(&ctl.full[slot]), phase, abort_flag)) {
+    if (!*abort_flag) {
+      atomicExch(p.fault, kFaultFullWait);
+      *abort_flag = 1;
+    }
+  }
+}
+
 struct VecWords {
   uint32_t w[4];
 };
@@ -685,17 +711,54 @@ struct Consumer {
   static constexpr int kVPT = 1024 / kConsumers;  // vectors per thread in the largest unit
   static constexpr uint32_t kAbsentWord = BF16 ? 0xF680F680u : 0xF6800000u;  // -2^110 in every lane
 
-  // Reduces one unit: nv (<= 1024) vectors in the ring stage at shared
-  // address `base`, the first being vector v_unit of global row `row`.
-  // Dispatches to a version specialised on the vectors each thread holds.
-  __device__ __forceinline__ void unit(uint32_t base, int64_t row, int64_t v_unit, int64_t nv, bool unit_has_sup) {
-    const int32_t vu = static_cast<int32_t>(v_unit);
-    if (nv == p.chunk_vec) {
-      if (p.chunk_vec == 1024) return unit_t<4, true>(base, row, vu, static_cast<int32_t>(nv), unit_has_sup);
-      if (p.chunk_vec == 512) return unit_t<2, true>(base, row, vu, static_cast<int32_t>(nv), unit_has_sup);
-      return unit_t<1, true>(base, row, vu, static_cast<int32_t>(nv), unit_has_sup);
+  // Streams vectors [vb, ve) of global row `row` from the ring: units of
+  // p.chunk_vec vectors from vb, the last one ragged when the range is not a
+  // multiple; an empty range is one empty unit (a row with no full vector).
+  // Every consumer thread runs it, and its control flow is warp-uniform: the
+  // full units run in a loop specialised on the vectors each thread holds.
+  __device__ __forceinline__ void consume(RingPos& rc, int64_t row, int64_t vb, int64_t ve) {
+    const int32_t n = static_cast<int32_t>(ve - vb);
+    int32_t v = static_cast<int32_t>(vb);
+    if (p.chunk_vec == 1024)
+      v = full_units<4>(rc, row, v, n / 1024);
+    else if (p.chunk_vec == 512)
+      v = full_units<2>(rc, row, v, n / 512);
+    else
+      v = full_units<1>(rc, row, v, n / 256);
+    const int32_t rest = static_cast<int32_t>(ve) - v;
+    if (rest > 0 || n == 0) {
+      const bool sup = has_sup(static_cast<int64_t>(v) * EPV, static_cast<int64_t>(v + rest) * EPV);
+      wait_stage(rc);
+      unit_t<kVPT, false>(ring + rc.slot * chunk_bytes, row, v, rest, sup);
+      release_stage(rc);
+      rc.advance(p.stages);
     }
-    unit_t<kVPT, false>(base, row, vu, static_cast<int32_t>(nv), unit_has_sup);
+  }
+
+  template <int NPT>
+  __device__ __forceinline__ int32_t full_units(RingPos& rc, int64_t row, int32_t v, int32_t nfull) {
+    constexpr int32_t CV = NPT * kConsumers;
+    for (int32_t i = 0; i < nfull; ++i, v += CV) {
+      const bool sup = has_sup(static_cast<int64_t>(v) * EPV, static_cast<int64_t>(v + CV) * EPV);
+      wait_stage(rc);
+      unit_t<NPT, true>(ring + rc.slot * chunk_bytes, row, v, CV, sup);
+      release_stage(rc);
+      rc.advance(p.stages);
+    }
+    return v;
+  }
+
+  // Waits for the unit at ring position r (fast path: every lane sees the
+  // phase complete at the first try).
+  __device__ __forceinline__ void wait_stage(const RingPos& r) {
+    const bool ok = mbar_try_wait(smem_addr(&ctl.full[r.slot]), r.phase);
+    if (!__all_sync(0xFFFFFFFFu, ok)) wait_unit_slow(p, ctl, r.slot, r.phase);
+  }
+
+  // The warp is done with the unit at ring position r.
+  __device__ __forceinline__ void release_stage(const RingPos& r) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl.empty[r.slot]));
   }
 
   // Thread tid holds vectors tid, tid + 256, ... (NPT of them; FULL: all of
@@ -725,7 +788,7 @@ struct Consumer {
 #pragma unroll
       for (int k = 0; k < 4; ++k) w[j][k] = BF16 ? bmax2(w[j][k], kSentinelBf16x2) : sanitize_low_bits(w[j][k]);
     const int32_t id0 = (v_unit + tid) * EPV;  // first id of vector j = 0; vector j adds j * 256 * EPV
-    if (unit_has_sup) {
+    if (__any_sync(0xFFFFFFFFu, unit_has_sup)) {   // the same in every thread
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int32_t v0 = id0 + j * kConsumers * EPV;
@@ -760,23 +823,24 @@ struct Consumer {
 #pragma unroll
       for (int j = 1; j < NPT; ++j) umax = fmaxf(umax, vmax[j]);
     }
-    if (umax > kTopClamp) {  // rare: +inf or huge logits count as 2^100
+    if (__any_sync(0xFFFFFFFFu, umax > kTopClamp)) {  // rare: +inf or huge logits count as 2^100
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) w[j][k] = BF16 ? bmin2(w[j][k], kTopBf16x2) : clamp_top_bits(w[j][k]);
         if (!LEAN) vmax[j] = fminf(vmax[j], kTopClamp);
       }
-      umax = kTopClamp;
+      umax = fminf(umax, kTopClamp);
     }
     // The warp's running max: every lane's sums take its reference, so they
     // are rescaled only when it grows (every lane of the warp is here).
     const float wmax = warp_max_f32(umax);
+    const bool grow = __any_sync(0xFFFFFFFFu, wmax > acc.m);
     float vms[NPT];
     if (LEAN) {
 #pragma unroll
       for (int j = 0; j < NPT; ++j) vms[j] = 0.0f;   // unused: no per-vector bound in this mode
-      if (wmax > acc.m) {
+      if (grow) {
         // The scaling is monotone: the scaled warp max is the largest scaled
         // value, and a lane holds it when its scaled unit max equals it.
         const float wms = scaled<SCALED>(wmax, s);
@@ -816,16 +880,18 @@ struct Consumer {
         }
       }
     }
-    gumbel_and_sums<NPT, FULL>(w, valid, vms, wmax, row, id0);
+    gumbel_and_sums<NPT, FULL>(w, valid, vms, wmax, grow, row, id0);
   }
 
   // The rescale, the sums and (Gumbel modes) the samples of one unit's
   // vectors; vms[j] is vector j's scaled max (unused in the lean mode),
-  // wmax the warp's max over the unit.
+  // wmax the warp's max over the unit, grow whether it is above some lane's
+  // running max (a lane already above it keeps its reference).
   template <int NPT, bool FULL>
   __device__ __forceinline__ void gumbel_and_sums(uint32_t (&w)[NPT][4], const bool (&valid)[NPT],
-                                                  const float (&vms)[NPT], float wmax, int64_t row, int32_t id0) {
-    if (wmax > acc.m) acc_rescale<SCALED>(acc, wmax, s);   // the same in every lane of the warp
+                                                  const float (&vms)[NPT], float wmax, bool grow, int64_t row,
+                                                  int32_t id0) {
+    if (grow) acc_rescale<SCALED>(acc, fmaxf(acc.m, wmax), s);
     const uint64_t nmc2 = pack2(acc.nref, acc.nref);
     uint64_t Zb = 0, Sb = 0;
 #pragma unroll
@@ -1072,18 +1138,6 @@ struct Consumer {
   }
 };
 
-// Position in the shared-memory ring: stage index and mbarrier phase parity.
-struct RingPos {
-  int slot = 0;
-  uint32_t phase = 0;
-  __device__ __forceinline__ void advance(int stages) {
-    if (++slot == stages) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
 // Producer: issues the bulk copies of this CTA's n units in order; next(src,
 // bytes) yields each unit's global address and size.  Returns when every
 // issued copy has landed (or, after a fault, when the drain deadline passes).
@@ -1148,22 +1202,6 @@ __device__ __forceinline__ void init_barriers(SharedCtl& ctl, int stages) {
   }
 }
 
-// Consumer wait for the unit at ring position r; records a fault and aborts
-// the CTA on timeout.
-__device__ __forceinline__ void wait_unit(const StatsParams& p, SharedCtl& ctl, const RingPos& r) {
-  volatile int32_t* abort_flag = &ctl.abort_flag;
-  if (!*abort_flag && !consumer_wait(smem_addr(&ctl.full[r.slot]), r.phase, abort_flag)) {
-    if (!*abort_flag) {
-      atomicExch(p.fault, kFaultFullWait);
-      *abort_flag = 1;
-    }
-  }
-}
-
-__device__ __forceinline__ void release_unit(SharedCtl& ctl, const RingPos& r, int lane) {
-  __syncwarp();
-  if (lane == 0 && !ctl.abort_flag) mbar_arrive(smem_addr(&ctl.empty[r.slot]));
-}
 
 // CTAs per SM each kernel is compiled for: three for the plain greedy mode
 // (its per-thread state fits 72 registers without spilling, and three rings
@@ -1213,7 +1251,6 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_kernel(
   Consumer<BF16, MODE> con(p, ctl, ring, chunk_bytes);
   uint8_t* rule_smem = dsmem + static_cast<size_t>(p.stages) * chunk_bytes;
   volatile int32_t* abort_flag = &ctl.abort_flag;
-  int64_t cur_row = -1, seg_uk0 = 0;
   bool first_segment = true;
   bool waited = !p.early;
 
@@ -1281,30 +1318,18 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_kernel(
     first_segment = false;
   };
 
+  // Row segments: units [uk0, uk1) of one row each.
   RingPos rc;
-  int64_t row = u_begin / p.K, uk = u_begin - row * p.K;
-  for (int64_t i = 0; i < n_units; ++i) {
-    if (row != cur_row) {
-      if (cur_row >= 0) flush(cur_row, seg_uk0, p.K - 1);
-      con.reset();
-      cur_row = row;
-      seg_uk0 = uk;
-    }
-    const int64_t v_unit = uk * p.chunk_vec;
-    int64_t nv = p.nvec - v_unit;
-    nv = nv < p.chunk_vec ? nv : p.chunk_vec;
-    const bool sup = con.has_sup(v_unit * con.EPV, (uk == p.K - 1) ? p.V : (v_unit + nv) * con.EPV);
-    wait_unit(p, ctl, rc);
-    con.unit(ring + rc.slot * chunk_bytes, row, v_unit, nv, sup);
-    release_unit(ctl, rc, lane);
-    rc.advance(p.stages);
-    if (uk == p.K - 1 && !*abort_flag) con.tail(row);
-    if (++uk == p.K) {
-      uk = 0;
-      ++row;
-    }
+  for (int64_t u = u_begin; u < u_end;) {
+    const int64_t row = u / p.K, uk0 = u - row * p.K;
+    const int64_t uk1 = (u_end - row * p.K) < p.K ? (u_end - row * p.K) : p.K;
+    con.reset();
+    const int64_t ve = uk1 * p.chunk_vec;
+    con.consume(rc, row, uk0 * p.chunk_vec, ve < p.nvec ? ve : p.nvec);
+    if (uk1 == p.K && !*abort_flag) con.tail(row);
+    flush(row, uk0, uk1 - 1);
+    u = row * p.K + uk1;
   }
-  if (cur_row >= 0) flush(cur_row, seg_uk0, (u_end - 1) - cur_row * p.K);
 }
 
 // ---------------------------------------------------------------------------
@@ -1364,17 +1389,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_cluster
   const bool reads_canvas = p.rule.canvas != nullptr && (p.rule.edit || p.rule.cand == nullptr);
   if (rank == 0 && tid == 0 && (!p.early || !reads_canvas)) pre = load_row_pre(p, row);
   RingPos rc;
-  for (int64_t i = 0; i < n_units; ++i) {
-    const int64_t v_unit = vb + i * p.chunk_vec;
-    int64_t nv = ve - v_unit;
-    nv = nv < p.chunk_vec ? nv : p.chunk_vec;
-    const bool last_unit = rank == static_cast<uint32_t>(S - 1) && i == n_units - 1;
-    const bool sup = con.has_sup(v_unit * con.EPV, last_unit ? p.V : (v_unit + nv) * con.EPV);
-    wait_unit(p, ctl, rc);
-    con.unit(ring + rc.slot * chunk_bytes, row, v_unit, nv, sup);
-    release_unit(ctl, rc, lane);
-    rc.advance(p.stages);
-  }
+  con.consume(rc, row, vb, ve);
   if (rank == static_cast<uint32_t>(S - 1) && !ctl.abort_flag) con.tail(row);
   con.resolve_index();
   const Partial r = con.cta_reduce();
@@ -1511,17 +1526,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_batch_k
   for (int64_t j = 0; j < l1 - l0; ++j) {
     const int64_t row = b * L + l0 + j;
     con.reset();
-    for (int64_t uk = 0; uk < p.K; ++uk) {
-      const int64_t v_unit = uk * p.chunk_vec;
-      int64_t nv = p.nvec - v_unit;
-      nv = nv < p.chunk_vec ? nv : p.chunk_vec;
-      nv = nv > 0 ? nv : 0;
-      const bool sup = con.has_sup(v_unit * con.EPV, (uk == p.K - 1) ? p.V : (v_unit + nv) * con.EPV);
-      wait_unit(p, ctl, rc);
-      con.unit(ring + rc.slot * chunk_bytes, row, v_unit, nv, sup);
-      release_unit(ctl, rc, lane);
-      rc.advance(p.stages);
-    }
+    con.consume(rc, row, 0, p.nvec);
     if (!*abort_flag) con.tail(row);
     con.resolve_index();
     const Partial r = con.cta_reduce();

@@ -727,7 +727,7 @@ struct Consumer {
       v = full_units<1>(rc, row, v, n / 256);
     const int32_t rest = static_cast<int32_t>(ve) - v;
     if (rest > 0 || n == 0) {
-      const bool sup = has_sup(static_cast<int64_t>(v) * EPV, static_cast<int64_t>(v + rest) * EPV);
+      const bool sup = has_sup(static_cast<uint32_t>(v) * EPV, static_cast<uint32_t>(v + rest) * EPV);
       wait_stage(rc);
       unit_t<kVPT, false>(ring + rc.slot * chunk_bytes, row, v, rest, sup);
       release_stage(rc);
@@ -739,7 +739,7 @@ struct Consumer {
   __device__ __forceinline__ int32_t full_units(RingPos& rc, int64_t row, int32_t v, int32_t nfull) {
     constexpr int32_t CV = NPT * kConsumers;
     for (int32_t i = 0; i < nfull; ++i, v += CV) {
-      const bool sup = has_sup(static_cast<int64_t>(v) * EPV, static_cast<int64_t>(v + CV) * EPV);
+      const bool sup = has_sup(static_cast<uint32_t>(v) * EPV, static_cast<uint32_t>(v + CV) * EPV);
       wait_stage(rc);
       unit_t<NPT, true>(ring + rc.slot * chunk_bytes, row, v, CV, sup);
       release_stage(rc);
@@ -1097,19 +1097,32 @@ struct Consumer {
   // row, not one per range (an indexed parameter read costs hundreds of
   // cycles).  reset() restarts it for the next row.
   int32_t sup_i;
-  int64_t sup_next;
+  uint32_t sup_next;   // ids are below V <= 2^31 - 1, and unit ends below 2^31 + 2^13
   __device__ void sup_restart() {
     sup_i = 0;
-    sup_next = p.n_sup > 0 ? p.sup[0] : INT64_MAX;
+    sup_next = p.n_sup > 0 ? static_cast<uint32_t>(p.sup[0]) : 0xFFFFFFFFu;
   }
-  __device__ bool has_sup(int64_t lo, int64_t hi) {
-    while (sup_next < lo) sup_next = (++sup_i < p.n_sup) ? p.sup[sup_i] : INT64_MAX;
+  __device__ bool has_sup(uint32_t lo, uint32_t hi) {
+    while (sup_next < lo) sup_next = (++sup_i < p.n_sup) ? static_cast<uint32_t>(p.sup[sup_i]) : 0xFFFFFFFFu;
     return sup_next < hi;
   }
 
-  // The CTA's reduction of all consumer states; valid in thread 0.
+  // The CTA's reduction of all consumer states; valid in thread 0.  When
+  // every lane of a warp holds the same max (the usual case: the lanes share
+  // the warp's running max), the warp's combine is plain sums and the least
+  // index, bit for bit what part_combine gives for equal maxima.
   __device__ Partial cta_reduce() {
-    Partial part = warp_combine<MODE>(acc_to_partial<RUNNER>(acc), s);
+    Partial part = acc_to_partial<RUNNER>(acc);
+    if (!GUMBEL && !RUNNER && __all_sync(0xFFFFFFFFu, part.m == __shfl_sync(0xFFFFFFFFu, part.m, 0))) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        part.Z = part.Z + __shfl_xor_sync(0xFFFFFFFFu, part.Z, o);
+        part.S2 = part.S2 + __shfl_xor_sync(0xFFFFFFFFu, part.S2, o);
+      }
+      part.idx = static_cast<int32_t>(__reduce_min_sync(0xFFFFFFFFu, static_cast<uint32_t>(part.idx)));
+    } else {
+      part = warp_combine<MODE>(part, s);
+    }
     if (lane == 0) ctl.warp_part[warp] = part;
     named_sync(1, kConsumers);
     Partial r = empty_partial();

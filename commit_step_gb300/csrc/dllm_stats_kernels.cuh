@@ -1237,10 +1237,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_kernel(
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
   const uint32_t ring = smem_addr(dsmem);
 
+  pdl_launch_dependents();   // the next kernel may launch now: it waits for this one before reading its outputs
   init_barriers(ctl, p.stages);
   __syncthreads();
   if (!p.early) pdl_wait();   // inputs may come from the previous kernel in the stream
-  pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
     if (lane == 0) {
@@ -1366,10 +1366,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_cluster
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
   const uint32_t ring = smem_addr(dsmem);
 
+  pdl_launch_dependents();   // the next kernel may launch now: it waits for this one before reading its outputs
   init_barriers(ctl, p.stages);
   __syncthreads();
   if (!p.early) pdl_wait();
-  pdl_launch_dependents();
 
   int32_t rule_b = -1;
   if (warp == kConsumerWarps) {
@@ -1503,10 +1503,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_batch_k
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
   const uint32_t ring = smem_addr(dsmem);
 
+  pdl_launch_dependents();   // the next kernel may launch now: it waits for this one before reading its outputs
   init_barriers(ctl, p.stages);
   __syncthreads();
   if (!p.early) pdl_wait();
-  pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
     if (lane == 0) {
@@ -1535,6 +1535,16 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_batch_k
 
   Consumer<BF16, MODE> con(p, ctl, ring, chunk_bytes);
   volatile int32_t* abort_flag = &ctl.abort_flag;
+  // When no canvas is read, the candidate flags come from the candidate mask
+  // (or none), an input like the logits: rank 0 loads its row's flag now, so
+  // that the load's latency hides behind the stream.
+  const RuleArgs& a = p.rule;
+  const bool reads_canvas = a.canvas != nullptr && (a.edit || a.cand == nullptr);
+  bool pre_cand = false;
+  if (rank == 0 && tid < L && !reads_canvas) {
+    int32_t unused_tok;   // 0: no canvas is read
+    pre_cand = is_candidate(a, b, tid, &unused_tok);
+  }
   RingPos rc;
   for (int64_t j = 0; j < l1 - l0; ++j) {
     const int64_t row = b * L + l0 + j;
@@ -1603,8 +1613,6 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_batch_k
   // before the grid dependency and only stores follow it; when a canvas
   // supplies candidates or tokens (rewritten by the step before), the canvas
   // is read, and the rule decided, after it.
-  const RuleArgs& a = p.rule;
-  const bool reads_canvas = a.canvas != nullptr && (a.edit || a.cand == nullptr);
   uint8_t* s_flags = s_exotic;               // reused: the exotic marks are consumed
   int32_t* s_cnt = reinterpret_cast<int32_t*>(s_exotic + kBatchMaxL);
   RuleScratch rs;
@@ -1617,7 +1625,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_batch_k
     int32_t tok = 0;
     bool cand = false;
     if (t < L) {
-      cand = is_candidate(a, b, t, &tok);
+      cand = reads_canvas ? is_candidate(a, b, t, &tok) : pre_cand;
       s_conf[t] = o.prob;
       s_ent[t] = o.H;
       s_x0[t] = o.x0;

@@ -907,10 +907,11 @@ struct Consumer {
     acc.S2 = add2(acc.S2, Sb);
 
     if (GUMBEL) {
-      const uint32_t row_lo = static_cast<uint32_t>(row);
-      const uint32_t row_hi = static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32);
+      const PhiloxRow pr = philox_row(static_cast<uint32_t>(row),
+                                      static_cast<uint32_t>(static_cast<uint64_t>(row) >> 32), p.keys);
       // The pruning floor: the best score any warp of the CTA has seen in
-      // this row (a lower bound of the row's winning score).
+      // this row (a lower bound of the row's winning score; the same in every
+      // lane of the warp).
       warp_best = fmaxf(warp_best, key_float(*reinterpret_cast<volatile uint32_t*>(&ctl.cta_best)));
       constexpr int PAIR = NPT >= 2 ? 2 : 1;
 #pragma unroll
@@ -923,7 +924,7 @@ struct Consumer {
           const int32_t v0 = id0 + (j0 + q) * kConsumers * EPV;
 #pragma unroll
           for (int h = 0; h < EPV / 4; ++h) {
-            const uint4 o = philox4x32_10(static_cast<uint32_t>(v0 >> 2) + h, row_lo, row_hi, 0u, p.keys);
+            const uint4 o = philox4x32_10_row(static_cast<uint32_t>(v0 >> 2) + h, pr, p.keys);
             r[q].w[4 * h + 0] = o.x;
             r[q].w[4 * h + 1] = o.y;
             r[q].w[4 * h + 2] = o.z;

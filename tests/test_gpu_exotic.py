@@ -132,6 +132,27 @@ def test_extreme_rows_scaled_with_margin(cs, scale, temperature):
         assert bad.size == 0, f"{what}: margin off in rows {bad[:6].tolist()}: {gm[bad[:6]]} vs {om[bad[:6]]}"
 
 
+@pytest.mark.parametrize("scale", [0.5, 256.0])
+def test_extreme_rows_scaled_plain_greedy(cs, scale):
+    """Scaled statistics without the margin or a sample: the plain greedy
+    mode's streaming loop (one running max per warp, the first vector of a
+    new warp max looked for only where it is held), on the extreme rows,
+    rows split across CTAs and the ties they hold; x0 bit for bit."""
+    for V, rows, seed in ((40_003, 1, 6), (997, 40, 7)):
+        host = np.tile(extreme_rows(V, seed), (rows, 1))
+        dev = to_device(host, "f32", stride=padded_stride(V, "f32"))
+        sup = [0, 11, V - 1]
+        x0, prob, ent, mar, am = cs.token_stats_ex(dev, suppress_ids=sup, logit_scale=scale, margin=None,
+                                                   argmax=None)
+        torch.cuda.synchronize()
+        assert mar is None and am is None
+        ox0, op, oe, _, _ = oracle.token_stats_ex(host, logit_scale=scale, suppress_ids=sup)
+        g = lambda t: t.cpu().numpy().reshape(-1)
+        what = f"plain scaled V={V} s={scale}"
+        assert np.array_equal(g(x0), ox0), what
+        assert_stats_close("f32", g(prob), g(ent), op, oe, what)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_extreme_rows_fused_threshold(cs, dtype):
     """The fused step decides on the statistics the exact path emitted: the

@@ -31,8 +31,8 @@ __global__ void __launch_bounds__(kMaskWarps * 32) mask_kernel(int64_t Lq, int64
                                                                 uint32_t attend_bits, uint32_t block_bits,
                                                                 int vec) {
   constexpr int EPV = 16 / ES;
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warp = blockIdx.x * static_cast<int64_t>(kMaskWarps) + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kMaskWarps;

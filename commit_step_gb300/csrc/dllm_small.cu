@@ -20,8 +20,8 @@ __global__ void __launch_bounds__(NT) rules_kernel(const __grid_constant__ RuleA
   extern __shared__ __align__(16) uint8_t dsmem[];
   __shared__ uint64_t red64[NT / 32];
   __shared__ int32_t red32[4 * (NT / 32)];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   RuleScratch s;
   s.keys = reinterpret_cast<uint64_t*>(dsmem);
   s.flags = dsmem + static_cast<size_t>(cap) * 8;
@@ -34,8 +34,8 @@ __global__ void __launch_bounds__(NT) rules_kernel(const __grid_constant__ RuleA
 __global__ void edit_kernel(const int32_t* __restrict__ x0, const float* __restrict__ prob,
                             const int32_t* __restrict__ tokens, const uint8_t* __restrict__ editable,
                             int64_t n, float tau_edit, uint8_t* __restrict__ edit) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float p = nan_to(prob[i], -__int_as_float(0x7F800000));
@@ -45,8 +45,8 @@ __global__ void edit_kernel(const int32_t* __restrict__ x0, const float* __restr
 
 __global__ void schedule_kernel(const int32_t* __restrict__ counts, int64_t B, int32_t steps,
                                 int32_t* __restrict__ quotas) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int64_t total = B * steps;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {

@@ -19,8 +19,8 @@ namespace dllm {
 // b hi, 1), key) word j & 3: one Philox call per four tokens.
 __global__ void uniform_canvas_kernel(const __grid_constant__ PhiloxSchedule ks, int64_t B, int64_t N, uint32_t V,
                                       int32_t* __restrict__ canvas, int64_t stride) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int64_t groups = (N + 3) / 4;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < B * groups;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -41,8 +41,8 @@ __global__ void uniform_canvas_kernel(const __grid_constant__ PhiloxSchedule ks,
 __global__ void renoise_kernel(const int32_t* __restrict__ sample, const uint8_t* __restrict__ accepted,
                                const int32_t* __restrict__ noise, const uint8_t* __restrict__ frozen, int64_t B,
                                int64_t N, int32_t* out) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < B * N;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     if (frozen && frozen[i / N]) continue;
@@ -64,8 +64,8 @@ __global__ void __launch_bounds__(kStopThreads) stop_kernel(const int32_t* __res
                                                              int32_t stability, float threshold, int32_t* prev,
                                                              int32_t* count, uint8_t* stop, uint8_t* done) {
   __shared__ long long part[kStopThreads / 32];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int64_t b = blockIdx.x;
   const int32_t* a = argmax + b * L;
   int32_t* pv = prev + b * L;
@@ -107,8 +107,8 @@ __global__ void __launch_bounds__(kStopThreads) uniform_update_kernel(
     int64_t N, uint32_t V, int32_t stability, float threshold, int32_t* canvas, int32_t* argmax, int32_t* prev,
     int32_t* count, uint8_t* done) {
   __shared__ long long part[kStopThreads / 32];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int64_t b = blockIdx.x;
   const bool frozen = done[b] != 0;
   const int64_t base = b * N;

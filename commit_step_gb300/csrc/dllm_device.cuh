@@ -106,10 +106,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 
 // Programmatic dependent launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// (The memory clobber keeps parameter and memory reads, and the work that
-// depends on them, after it: a kernel that triggers first lets the next one
-// launch without waiting for its own set-up.)
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 // Named barrier among the first `count` threads of the CTA (warps 0..count/32-1).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {

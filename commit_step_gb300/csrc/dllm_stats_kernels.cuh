@@ -1227,9 +1227,6 @@ __host__ __device__ constexpr int min_ctas_per_sm(int mode) { return mode == 0 ?
 // ---------------------------------------------------------------------------
 template <bool BF16, int MODE>
 __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_kernel(const __grid_constant__ StatsParams p) {
-  // First: the next kernel may launch now (every reader of this kernel's
-  // outputs waits on the grid dependency before reading them).
-  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ SharedCtl ctl;
   const int tid = threadIdx.x;
@@ -1241,6 +1238,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_kernel(
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
   const uint32_t ring = smem_addr(dsmem);
 
+  pdl_launch_dependents();   // the next kernel may launch now: it waits for this one before reading its outputs
   init_barriers(ctl, p.stages);
   __syncthreads();
   if (!p.early) pdl_wait();   // inputs may come from the previous kernel in the stream
@@ -1356,9 +1354,6 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_kernel(
 // ---------------------------------------------------------------------------
 template <bool BF16, int MODE>
 __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_cluster_kernel(const __grid_constant__ StatsParams p) {
-  // First: the next kernel may launch now (every reader of this kernel's
-  // outputs waits on the grid dependency before reading them).
-  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ SharedCtl ctl;
   const int tid = threadIdx.x;
@@ -1372,6 +1367,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_cluster
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
   const uint32_t ring = smem_addr(dsmem);
 
+  pdl_launch_dependents();   // the next kernel may launch now: it waits for this one before reading its outputs
   init_barriers(ctl, p.stages);
   __syncthreads();
   if (!p.early) pdl_wait();
@@ -1493,9 +1489,6 @@ struct SharedEmit {
 
 template <bool BF16, int MODE>
 __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_batch_kernel(const __grid_constant__ StatsParams p) {
-  // First: the next kernel may launch now (every reader of this kernel's
-  // outputs waits on the grid dependency before reading them).
-  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ SharedCtl ctl;
   __shared__ Partial row_part[kBatchMaxRowsPerCta];
@@ -1511,6 +1504,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(MODE)) stats_batch_k
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.chunk_vec) * 16u;
   const uint32_t ring = smem_addr(dsmem);
 
+  pdl_launch_dependents();   // the next kernel may launch now: it waits for this one before reading its outputs
   init_barriers(ctl, p.stages);
   __syncthreads();
   if (!p.early) pdl_wait();

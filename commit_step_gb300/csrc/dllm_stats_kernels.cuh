@@ -16,16 +16,22 @@
 //     z' = fp32(z s) (s = 1 unless the caller scales them): running max m of
 //     the raw logits, Z = sum 2^y and S2 = sum 2^y y with y = z' log2 e - ref
 //     and ref = RU(m' log2 e), the product rounded up (packed fp32x2
-//     accumulators, one fused multiply-add per pair), rescaled when the max
-//     grows; entropy = ln Z - S2 ln 2 / Z.  Decisions (argmax, ties, Gumbel
-//     scores) compare the scaled values z' themselves.
+//     accumulators, one fused multiply-add per pair); entropy = ln Z - S2
+//     ln 2 / Z.  The lanes of a warp share one running max (the warp's, by
+//     redux.sync), so the sums are rescaled only when it grows.  Decisions
+//     (argmax, ties, Gumbel scores) compare the scaled values z' themselves.
+//   * Consumer::consume streams a (row, vector range) segment: full units in
+//     a loop specialised on the vectors each thread holds, the ragged last
+//     unit after it, with warp-uniform control flow.
 //   * Rows whose maximum the streaming pass cannot resolve exactly (|ref| >=
 //     2^28, or no logit above the no-mass sentinel -2^100) are recomputed by
 //     one warp from the logits as they are (exotic_row).
 //     The first index of the max is located once per row, from the first
-//     vector that holds the thread's max; the largest value outside that
-//     element (the runner-up of the margin confidence) comes with it.
-//   * Gumbel-max: one Philox4x32-10 call per four ids; a bound on the noise
+//     vector that holds the thread's max (in the plain greedy mode recorded
+//     only by the lanes that hold a new warp max); the largest value outside
+//     that element (the runner-up of the margin confidence) comes with it.
+//   * Gumbel-max: one Philox4x32-10 call per four ids (rounds 0 and 1 folded
+//     per row); a bound on the noise
 //     from the largest uniform of each 16-byte vector lets most vectors skip
 //     the two logarithms; the warp shares its best score to tighten the bound.
 //   * Many rows (persistent kernel): the units are dealt to the CTAs in equal
@@ -35,6 +41,10 @@
 //   * Few rows (cluster kernel): one thread-block cluster per row, each CTA a
 //     contiguous slice; the CTAs' partials are combined through distributed
 //     shared memory by rank 0.
+//   * Short batch rows whose inputs are ready early (batch-row kernel): one
+//     cluster per batch row, each CTA whole rows; rank 0 gathers their
+//     partials through distributed shared memory and decides the rule in
+//     shared memory before the grid dependency, so only stores follow it.
 //   * Fused commit step: the thread that finalizes a row also makes the row's
 //     threshold / edit decision and canvas update; the last row of a batch row
 //     applies the forced commit when nothing passed (or, for the sorting rules,

@@ -148,3 +148,27 @@ def test_invalid_arguments_raise(cs):
         cs.token_stats(zz)
     ws = cs.workspace(4, 1, 64, 0, z.device)
     assert cs.workspace_fault(ws) == 0
+
+
+# Shapes that land on each unit size of the streaming loop (units of 1024,
+# 512 and 256 vectors: 4, 2 or 1 vectors per consumer thread), on the
+# cluster grid (8 rows: a cluster of 16 CTAs per row, a slice of 1200, 600 or
+# 300 vectors per CTA) and on the persistent grid (600 rows dealt to the CTAs
+# in unit ranges that cross rows), each with a ragged last unit.
+UNIT_SHAPES = [  # rows, vectors per row
+    (8, 19_200), (8, 9_600), (8, 4_800),
+    (600, 4_000), (600, 2_400), (600, 1_000),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", UNIT_SHAPES, ids=[f"T{t}nvec{n}" for t, n in UNIT_SHAPES])
+@pytest.mark.parametrize("temperature", [0.0, 0.8])
+def test_every_unit_size(cs, dtype, shape, temperature):
+    rows, nvec = shape
+    V = nvec * (8 if dtype == "bf16" else 4)
+    rng = np.random.default_rng(rows * 7 + nvec)
+    z = gen(rng, rows, V, scale=2.5)
+    z[np.arange(rows), rng.integers(0, V, rows)] += 7.0
+    host = z if dtype == "f32" else f32_to_bf16_bits(z)
+    run_case(cs, host, dtype, temperature=temperature, key=4242, suppress=[3, V - 5])

@@ -216,6 +216,34 @@ def recorded_traffic(workload: str):
     return None
 
 
+def recorded_inst(workload: str):
+    """Warp instructions per launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            e = json.load(f).get(workload)
+        if e and e.get("kernel_hash") == kernel_source_hash() and e.get("warp_inst_per_launch"):
+            return float(e["warp_inst_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+def issue_roofline(inst, ms_per_launch, sms, sm_mhz, alg_bytes, hbm_peak):
+    """The issue roof of a kernel bound by instruction issue rather than DRAM:
+    every SM has four schedulers that each issue at most one warp instruction
+    per cycle, so the peak is SMs x 4 x the SM clock sampled under load."""
+    if not inst or not sm_mhz:
+        return None
+    peak = sms * 4 * sm_mhz * 1e6 / 1e9
+    achieved = inst / (ms_per_launch / 1e3) / 1e9
+    t_full = inst / (peak * 1e9)   # seconds per launch at one instruction per scheduler per cycle
+    return {"bound": "issue", "achieved": round(achieved, 1), "peak": round(peak, 1),
+            "unit": "G warp instructions/s", "frac": round(achieved / peak, 4), "inst_per_launch": inst,
+            "hbm_frac_at_full_issue": round(alg_bytes / t_full / 1e9 / hbm_peak, 4),
+            "peak_derivation": f"{sms} SMs x 4 schedulers x 1 warp instruction per cycle x {sm_mhz:.0f} MHz"}
+
+
 # --------------------------------------------------------------------------
 # multi-rank timing: each rank times its own replica; the job takes the max
 # --------------------------------------------------------------------------
@@ -487,6 +515,10 @@ def sub_record(cs, name, dev, props, l2, world):
            "single_launch_us": round(single_launch_us(runner, 5), 2),
            "traffic": recorded_traffic(name), "kernel": recorded_kernel(name), "clocks": m["clocks"],
            "workspace_fault": cs.workspace_fault(runner.ws)}
+    clk = (m["clocks"] or {}).get("sm_mhz") or getattr(props, "clock_rate", 0) / 1e3
+    roof = issue_roofline(recorded_inst(name), m["ms_per_step"], props.multi_processor_count, clk, alg, peak)
+    if roof:
+        rec["issue_roofline"] = roof
     del runner
     torch.cuda.empty_cache()
     return rec

@@ -64,3 +64,20 @@ def test_recorded_traffic_only_for_the_current_code(monkeypatch):
     assert got is None or got > 8_093_696              # at least the logits, when recorded
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
     assert bench.recorded_traffic("llada") is None
+
+
+def test_issue_roofline_arithmetic(monkeypatch):
+    # 152 SMs x 4 schedulers x 2000 MHz = 1216 G warp instructions/s; 608 M
+    # instructions in 1 ms is 608 G/s, half of it; at full issue the launch
+    # would take 0.5 ms, so 1 GB of logits would stream at 2000 GB/s
+    r = bench.issue_roofline(608e6, 1.0, 152, 2000.0, 10**9, 4000.0)
+    assert r["bound"] == "issue"
+    assert r["peak"] == pytest.approx(1216.0)
+    assert r["achieved"] == pytest.approx(608.0)
+    assert r["frac"] == pytest.approx(0.5)
+    assert r["hbm_frac_at_full_issue"] == pytest.approx(0.5)
+    assert bench.issue_roofline(None, 1.0, 152, 2000.0, 10**9, 4000.0) is None
+    got = bench.recorded_inst("dream")
+    assert got is None or got > 622_891_008 / 16      # at least one warp instruction per 16-byte vector
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.recorded_inst("dream") is None

@@ -784,6 +784,27 @@ def run_mask(args, rank, world):
     nbytes = L * L * 4
     value = nbytes * n * world / (ms / 1e3) / 1e9
     peak, kind = measured_peaks()
+    # the pure-write ceiling beside it: torch's fill of the same two buffers,
+    # replayed the same way (a library kernel, timed for reference only)
+    gf = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(G):
+            outs[i % 2].fill_(0.0)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(gf, stream=stream):
+        for i in range(G):
+            outs[i % 2].fill_(0.0)
+    with torch.cuda.stream(stream):
+        gf.replay()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            gf.replay()
+    f1.record(stream)
+    f1.synchronize()
+    fill_gbs = nbytes * n / (f0.elapsed_time(f1) / 1e3) / 1e9
     return {
         "metric": "block_causal_mask write GB/s", "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": n, "warmup": max(1, warmup // G) * G, "ms_per_step": ms / n, "higher_is_better": True,
@@ -793,6 +814,8 @@ def run_mask(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(value / world / peak, 4), "traffic": None,
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({kind})"},
+        "write_ceiling": {"fill_gbs": round(fill_gbs, 1), "frac_of_fill": round(value / world / fill_gbs, 4),
+                          "what": "torch fill_ of the same two 256 MiB buffers in the same graphs, timed after ours"},
         "gpu_launches": n, "clocks": clk.summary(),
     }
 

@@ -21,6 +21,8 @@ const void* renoise_kernel_ptr();
 const void* stop_kernel_ptr();
 const void* uniform_update_kernel_ptr();
 const void* mask_kernel_ptr(int es);
+int mask_chunk_vec();
+int mask_threads();
 }  // namespace dllm
 
 namespace {
@@ -717,11 +719,17 @@ dllm_status dllm_block_causal_mask(int64_t Lq, int64_t Lk, int64_t q_offset, int
   uint32_t blocked = kind == DLLM_MASK_F32 ? 0xFF800000u : (kind == DLLM_MASK_BF16 ? 0xFF80u : 0u);
   int64_t row_bytes = row_stride * es;
   int vec = ((reinterpret_cast<uintptr_t>(out) & 15u) == 0 && row_bytes % 16 == 0) ? 1 : 0;
-  const int64_t warps = 8;
-  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((Lq + warps - 1) / warps, static_cast<int64_t>(d->sms) * 8));
+  // one block per chunk of mask_chunk_vec() vectors of a row (one per row
+  // when rows are not vector-aligned); the kernel's block loop covers a
+  // grid capped below the launch limit
+  const int64_t nvec = vec ? Lk / (16 / es) : 0;
+  int64_t chunks_per_row = (nvec + mask_chunk_vec() - 1) / mask_chunk_vec();
+  if (chunks_per_row < 1) chunks_per_row = 1;
+  const int64_t blocks = std::min<int64_t>(Lq * chunks_per_row, int64_t{1} << 30);
   uint8_t* o = static_cast<uint8_t*>(out);
-  void* args[] = {&Lq, &Lk, &q_offset, &k_offset, &block_len, &o, &row_bytes, &attend, &blocked, &vec};
-  return launch(mask_kernel_ptr(es), dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+  void* args[] = {&Lq, &Lk, &q_offset, &k_offset, &block_len, &o, &row_bytes, &attend, &blocked, &vec,
+                  &chunks_per_row};
+  return launch(mask_kernel_ptr(es), dim3(static_cast<unsigned>(blocks)), dim3(mask_threads()), 0,
                 reinterpret_cast<cudaStream_t>(stream), args);
 }
 

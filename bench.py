@@ -172,7 +172,7 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     """Hash of the kernel sources with comments and blank space removed, so
     that only a change of code (not of its comments) invalidates the
     recorded ncu traffic."""
@@ -180,7 +180,7 @@ def kernel_source_hash() -> str:
     import re
 
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, "commit_step_gb300", "csrc", name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -204,12 +204,13 @@ def recorded_kernel(workload: str) -> str:
 
 def recorded_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current kernel sources (else None).  An entry that names its own
+    sources is checked against those alone."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("kernel_hash") == kernel_source_hash():
+        if e and e.get("kernel_hash") == kernel_source_hash(e.get("sources")):
             return float(e["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         pass
@@ -812,7 +813,7 @@ def run_mask(args, rank, world):
         "config": {"workload": f"block_causal_mask L={L} block_len={bl} fp32 additive", "l2": "two 256 MiB outputs, "
                    "alternating (each larger than L2)"},
         "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(value / world / peak, 4), "traffic": None,
+                     "frac": round(value / world / peak, 4), "traffic": recorded_traffic("mask"),
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({kind})"},
         "write_ceiling": {"fill_gbs": round(fill_gbs, 1), "frac_of_fill": round(value / world / fill_gbs, 4),
                           "what": "torch fill_ of the same two 256 MiB buffers in the same graphs, timed after ours"},

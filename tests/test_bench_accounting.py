@@ -62,7 +62,7 @@ def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
 def test_recorded_traffic_only_for_the_current_code(monkeypatch):
     got = bench.recorded_traffic("llada")
     assert got is None or got > 8_093_696              # at least the logits, when recorded
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda *a: "0" * 16)
     assert bench.recorded_traffic("llada") is None
 
 
@@ -79,5 +79,14 @@ def test_issue_roofline_arithmetic(monkeypatch):
     assert bench.issue_roofline(None, 1.0, 152, 2000.0, 10**9, 4000.0) is None
     got = bench.recorded_inst("dream")
     assert got is None or got > 622_891_008 / 16      # at least one warp instruction per 16-byte vector
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda *a: "0" * 16)
     assert bench.recorded_inst("dream") is None
+
+
+def test_recorded_traffic_follows_its_own_sources(tmp_path, monkeypatch):
+    # the mask's record is hashed over the mask's own sources, not the statistics kernels'
+    got = bench.recorded_traffic("mask")
+    assert got is None or got > 0
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", ("dllm_rules.cuh",))
+    assert bench.recorded_traffic("mask") == got
+    assert bench.recorded_traffic("llada") is None

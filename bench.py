@@ -8,8 +8,10 @@ rule and the canvas update.  The default workload is one LLaDA-8B-shaped
 block step: B=1, L=32 rows of V=126464 bf16 logits, suppress the mask id,
 greedy, strict threshold 0.95 on 19 candidates.
 
-Our arm replays the steps from a CUDA graph over rotating logit buffers whose
-total exceeds 4x the L2 cache, so every step reads its logits from HBM.  The
+Our arm replays the steps from CUDA graphs over rotating logit buffers whose
+total exceeds 4x the L2 cache, so every step reads its logits from HBM, and
+writes then reads buffers of twice the L2 size before each timed region, so
+that the region starts from a clean L2 holding none of its inputs.  The
 reference arm (--impl reference) times the CPU oracle on the same workload.
 Under torchrun each rank runs its own replica on its own GPU (the path shards
 by batch row with no collective); rank 0 prints one JSON line.
